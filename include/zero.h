@@ -1,0 +1,266 @@
+/*
+ * zero.h -- C ABI of the GB300 (sm_103a) ZeRO-DP partitioned mixed-precision
+ * optimizer step.
+ *
+ * What the library computes (page titles and sections):
+ *  - "01 - ZeRO memory math and Stage 1/2" (DeepSpeed ZeRO stages 1-2
+ *    walkthrough), 4 (1)-(4): flatten a parameter group, pad it to a
+ *    multiple of 2*world_size, split it into world_size contiguous shards
+ *    (base = total // dp, remainder to the first ranks), and map tensors to
+ *    shards;  6: the step -- overflow check (skip on inf/NaN), global gradient
+ *    norm from per-shard partial sums, unscale and clip, Adam on the fp32
+ *    shard, copy of the result to 16 bits in the rank's slot of the flat
+ *    buffer, all-gather.
+ *  - "ZeRO: Memory Optimizations Toward Training Trillion Parameter Models"
+ *    reading notes (papers.chlience.com), 3 (Adam is per coordinate, so the
+ *    update of a shard needs only that shard's state), 4 (the averaged
+ *    gradient shard g_bar^(k) = (1/N_d) sum_r g_r^(k), the reduce-scatter),
+ *    7 and 9 (ZeRO-3: gather a layer's parameter shards before its forward
+ *    and again before its backward; reduce its gradients onto the owner).
+ *  - the ZeRO paper (Chinese translation, aiingo), 5.1-5.3 and Figure 1, and
+ *    the CMU 11-868 lecture notes, slide 64: memory of model states per stage.
+ *
+ * One GPU holds every simulated rank: the N_d ranks' gradients are N_d
+ * buffers in local HBM, the reduce-scatter is N_d coalesced reads fused into
+ * the update, the scalar all-reduce of the norm is a fixed-order combine of
+ * per-block partial sums on the device, and the all-gather destination is the
+ * one flat 16-bit parameter buffer every simulated rank shares.
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are CUDA device (or managed) addresses on the current
+ *    device; host pointers are plain CPU memory.  The caller owns every
+ *    buffer; the library allocates nothing and keeps no state between calls.
+ *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and is asynchronous: results land in caller memory when
+ *    the stream reaches them.  No entry point synchronises.
+ *  - A negative return is an argument or launch error, reported before any
+ *    work is enqueued when it is an argument error; zero_last_error() gives a
+ *    message (per thread).  Conditions found on the device (overflow) are
+ *    reported in zero_result, never by a trap.
+ *  - 16-bit element offsets and counts are in elements, int64.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_MAX_SLICES 64   /* most gradient slices (ranks) one call reduces */
+#define ZERO_MAX_SHARDS 64   /* most shards one call updates */
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = -1,      /* bad argument (null pointer, negative size, unknown dtype or mode) */
+    ZERO_EALIGN = -2,      /* a pointer is not aligned to its element size */
+    ZERO_EWORKSPACE = -3,  /* workspace missing or smaller than zero_workspace_bytes() */
+    ZERO_ECUDA = -4,       /* a CUDA runtime call or launch failed */
+    ZERO_ELIMIT = -5       /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards */
+} zero_status;
+
+typedef enum { ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype;
+
+typedef enum {
+    ZERO_PLAN_PADDED = 0,   /* pad to a multiple of 2*world_size, then split (the walkthrough's rule) */
+    ZERO_PLAN_UNPADDED = 1  /* split the unpadded length; the remainder goes to the first ranks */
+} zero_plan_mode;
+
+/* ------------------------------------------------------------------------
+ * Partition plan.  Host only.
+ * Source: DeepSpeed ZeRO stages 1-2 walkthrough, 4 (1) flatten and align,
+ * 4 (2) get_data_parallel_partitions (base = total // dp, remaining =
+ * total % dp, remainder to the first ranks), 7 (start alignment).
+ *
+ * numels[n_tensors]          host, the group's tensors in declaration order
+ * tensor_offsets[n_tensors]  host out, flat offset of each tensor
+ * rank_offsets[world_size]   host out, first flat element of each rank's shard
+ * rank_numels[world_size]    host out, shard sizes (sum = *padded_total)
+ * padded_total, padding      host out, flat length after padding, and padding
+ * Returns ZERO_OK or ZERO_EINVAL (n_tensors < 0, world_size < 1, negative
+ * numel, unknown mode, null output).  Padding elements sit at the tail of the
+ * last rank's shard; they are part of its shard.
+ * ------------------------------------------------------------------------ */
+int zero_plan(const int64_t* numels, int n_tensors, int world_size, int mode,
+              int64_t* tensor_offsets, int64_t* rank_offsets, int64_t* rank_numels,
+              int64_t* padded_total, int64_t* padding);
+
+/* The tensors that overlap one rank's shard (params_in_partition and the
+ * first offset of the walkthrough's 4 (4)): row k of out[4*k .. 4*k+3] is
+ * (tensor index, first element inside the tensor, first element inside the
+ * shard, length).  out must hold 4*n_tensors values.  Host only.  Returns the
+ * number of rows (>= 0) or ZERO_EINVAL. */
+int zero_plan_intersections(const int64_t* tensor_offsets, const int64_t* numels, int n_tensors,
+                            int64_t rank_offset, int64_t rank_numel, int64_t* out);
+
+/* ------------------------------------------------------------------------
+ * Memory model of model states per device, in bytes.  Host only.
+ * Source: ZeRO paper (Chinese translation), 5.1-5.3 and Figure 1; reading
+ * notes 5.1-5.4; CMU 11-868 notes, slide 64.  K is the optimizer-state bytes
+ * per parameter (12 for mixed-precision Adam):
+ *   stage 0 (DP)        (4 + K) psi
+ *   stage 1 (P_os)      4 psi + K psi / n_d
+ *   stage 2 (P_os+g)    2 psi + (K + 2) psi / n_d
+ *   stage 3 (P_os+g+p)  (4 + K) psi / n_d
+ * Returns ZERO_OK or ZERO_EINVAL (stage outside 0..3, n_d < 1, psi or K < 0,
+ * bytes_out null).
+ * ------------------------------------------------------------------------ */
+int zero_mem_model(double psi, double K, int n_d, int stage, double* bytes_out);
+
+/* ------------------------------------------------------------------------
+ * The step.
+ * ------------------------------------------------------------------------ */
+
+/* Hyper-parameters of one AdamW step (fp32, as the optimizer holds them).
+ * step is t of THIS step, 1-based; the caller owns the counter and advances it
+ * only when zero_result.applied is 1 (a skipped step does not count).
+ * max_grad_norm <= 0 disables clipping. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, max_grad_norm;
+    int64_t step;
+} zero_hyper;
+
+/* One simulated rank's shard.
+ * numel          elements in the shard (may be 0)
+ * grad_offset    element offset of the shard inside every gradient slice
+ *                (all-ranks view: the rank's flat offset into each rank's full
+ *                gradient; rank-local view with staged slices: 0)
+ * param_offset   element offset of the shard inside flat_param
+ * *_in           device fp32 master weights, momentum and variance (numel each)
+ * *_out          device fp32 outputs; equal to *_in for an in-place update, or a
+ *                second state set (ping-pong) that lets the step run in one pass
+ * grad_shard     device 16-bit reduced-gradient shard (numel), written by the
+ *                two-pass path and read by zero_shard_apply; may be NULL for
+ *                calls that take the single pass */
+typedef struct {
+    int64_t numel, grad_offset, param_offset;
+    const float *master_in, *m_in, *v_in;
+    float *master_out, *m_out, *v_out;
+    void* grad_shard;
+} zero_shard;
+
+/* Running gradient statistics in device memory (the scalar all-reduce's
+ * operands): sum of squares of the scaled reduced gradient and an overflow
+ * flag (nonzero once an inf/NaN was reduced). */
+typedef struct {
+    double sumsq;
+    int32_t overflow;
+    int32_t reserved;
+} zero_stats;
+
+/* Outcome of a step, written to device (or mapped host) memory.
+ * overflow   some reduced gradient element, or extra_overflow, was inf/NaN
+ * applied    1 if the update was committed; 0 if the step was skipped --
+ *            then master/m/v/param are as before the call (the *_in set)
+ * path       1 = fused single pass, 2 = two passes (reduce, then apply)
+ * sumsq      sum of squares of the scaled reduced gradient plus extra_sumsq
+ * grad_norm  sqrt(sumsq) / loss_scale
+ * clip_coef  max_grad_norm / (grad_norm + 1e-6) when that is below 1, else 1
+ * grad_mult  fp32(clip_coef / loss_scale), the multiplier applied to the
+ *            reduced gradient before AdamW */
+typedef struct {
+    int32_t overflow, applied, path, reserved;
+    double sumsq, grad_norm, clip_coef;
+    float grad_mult, reserved2;
+} zero_result;
+
+/* Bytes of device workspace zero_shard_step / zero_shard_reduce /
+ * zero3_reduce_bucket need: per-block partial sums, a completion counter and
+ * the step's internal statistics.  The workspace must be zero-filled once
+ * before its first use; every call leaves it ready for the next.  Calls that
+ * share a workspace must not overlap on the device. */
+size_t zero_workspace_bytes(void);
+
+/* The whole partitioned step over n_shards shards that share one global
+ * decision (all simulated ranks, or one rank's shard plus the other ranks'
+ * statistics in extra_sumsq / extra_overflow).
+ *
+ * grad_slices[n_slices]  host array of device pointers: slice r is rank r's
+ *                        16-bit gradient (grad_dtype); shard s reads elements
+ *                        [grad_offset_s, grad_offset_s + numel_s) of each.
+ *                        n_slices = N_d, the averaging divisor.
+ * shards[n_shards]       host array
+ * flat_param             device 16-bit (param_dtype) flat parameter buffer;
+ *                        shard s writes [param_offset_s, + numel_s)
+ * hyper                  host
+ * loss_scale             S > 0; the reduced gradient is divided by it
+ * extra_sumsq, extra_overflow   other ranks' share of the statistics
+ * workspace              device, zero_workspace_bytes() bytes, see above
+ * result                 device (or mapped host) zero_result
+ *
+ * Per element i of a shard, in this order: s = sum_r fp32(g_r[i]) in rank
+ * order; a = round16(s / N_d); overflow if a is inf/NaN; sumsq += a^2;
+ * after all shards: skip if any overflow; k = fp32(c / S) with the clip
+ * coefficient c; g = a k; theta = theta (1 - lr wd); m = b1 m + (1-b1) g;
+ * v = b2 v + (1-b2) g^2; theta = theta - [lr/(1-b1^t)] m / (sqrt(v)/sqrt(1-b2^t) + eps);
+ * flat_param[param_offset + i] = round16(theta).  Every fp32 operation is
+ * rounded on its own (no contraction).
+ *
+ * Path: with clipping off and every shard's *_out distinct from its *_in, one
+ * fused pass reads the slices and the *_in state once and writes the *_out
+ * state and the parameters once; on overflow a second, short kernel restores
+ * the parameters from master_in (parameters always equal round16(master)).
+ * Otherwise two passes: reduce into grad_shard (required then), then apply.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN (16-bit pointers must be 2-byte aligned,
+ * fp32 pointers 4-byte aligned), ZERO_EWORKSPACE, ZERO_ELIMIT, ZERO_ECUDA. */
+int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype,
+                    const zero_shard* shards, int n_shards,
+                    void* flat_param, int param_dtype,
+                    const zero_hyper* hyper, float loss_scale,
+                    double extra_sumsq, int extra_overflow,
+                    void* workspace, size_t workspace_bytes,
+                    zero_result* result, void* stream);
+
+/* First pass alone: reduce each shard's slices into its grad_shard
+ * (a = round16(sum_r fp32(g_r) / n_slices), rank order) and add the shards'
+ * sum of squares and overflow flag to *stats (device).  accumulate = 0 starts
+ * *stats afresh; 1 adds to what is there (stream order makes successive calls
+ * deterministic).  Arguments as for zero_shard_step. */
+int zero_shard_reduce(const void* const* grad_slices, int n_slices, int grad_dtype,
+                      const zero_shard* shards, int n_shards, int accumulate,
+                      zero_stats* stats, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Second pass alone: read each shard's grad_shard and *stats (device), decide
+ * skip and clip from stats->sumsq + extra_sumsq and stats->overflow |
+ * extra_overflow, run AdamW from *_in to *_out and store the parameters, and
+ * write *result.  For ZeRO-3 the parameters are the rank's own parameter
+ * shard buffer (param_offset 0 there). */
+int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype,
+                     void* flat_param, int param_dtype,
+                     const zero_hyper* hyper, float loss_scale,
+                     const zero_stats* stats, double extra_sumsq, int extra_overflow,
+                     zero_result* result, void* stream);
+
+/* ------------------------------------------------------------------------
+ * ZeRO-3 per-layer steps.
+ * Source: reading notes 7 and 9 (stage 3: all-gather a layer's parameter
+ * shards before its forward and again before its backward; reduce-scatter its
+ * gradients to the owner); ZeRO paper (Chinese translation) 7.2.2.
+ * A unit (layer) of unit_numel elements is split into world_size equal parts
+ * (unit_numel must divide by world_size); rank r keeps part r.
+ * ------------------------------------------------------------------------ */
+
+/* layer_out[r * P + j] = part_r[j] for j < P = unit_numel / world_size.
+ * part_ptrs[world_size]: host array of device pointers, each P elements
+ * (dtype); layer_out: device, unit_numel elements.  Bit-exact copy. */
+int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t unit_numel, int dtype,
+                       void* layer_out, void* stream);
+
+/* The owner's share of the unit's gradient reduce-scatter:
+ * grad_part[j] = round16(sum_r fp32(bucket_r[owner * P + j]) / world_size),
+ * and the part's sum of squares / overflow added to *stats (accumulate as for
+ * zero_shard_reduce).  bucket_ptrs[world_size]: host array of device pointers,
+ * each a full unit (unit_numel elements).  grad_part: device, P elements. */
+int zero3_reduce_bucket(const void* const* bucket_ptrs, int world_size, int owner, int64_t unit_numel,
+                        int grad_dtype, void* grad_part, int accumulate, zero_stats* stats,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Message of the last error on this thread ("" if none). */
+const char* zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_GB300_H */

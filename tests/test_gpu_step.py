@@ -1,0 +1,283 @@
+"""GPU parity of the partitioned step against the CPU oracle, at sizes the
+oracle finishes in seconds (several tiles per shard, ragged tails), through
+the C ABI.
+
+Tolerances: plan, overflow flag, reduced gradients bit-exact; without
+clipping every state and parameter is bit-exact too (both sides do the same
+rounded fp32 operations, and the multiplier 1/S is exact); with clipping the
+multiplier depends on the fp64 norm, whose last bits may differ (the device
+sums fp32 partials of exact squares, the oracle sums exactly), so fp32 state
+is compared within rel 2e-6 and 16-bit parameters within 1 ulp; the norm
+within rel 1e-5."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as W
+from helpers import hyper32, make_problem, random_group, t2u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+TDT = {1: torch.float16, 2: torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def Z():
+    import zero_dp_partitioned_gb300 as Z
+    return Z
+
+
+def dev16(a: np.ndarray, dt):
+    return torch.from_numpy(a.view(np.int16).copy()).view(TDT[dt]).to(DEV)
+
+
+def dev32(a: np.ndarray):
+    return torch.from_numpy(a.copy()).to(DEV)
+
+
+class GpuRun:
+    """Device copy of a problem: per-rank grads, flat params, per-shard state (A and optionally B)."""
+
+    def __init__(self, Z, p, flat, dt, ranks, pingpong, want_grad=True, state_pad=0, param_pad=0):
+        self.Z, self.p, self.dt, self.ranks, self.pingpong = Z, p, dt, ranks, pingpong
+        self.param_pad = param_pad
+        base = torch.zeros(flat.size + param_pad, dtype=TDT[dt], device=DEV)
+        base[param_pad:] = dev16(flat, dt)
+        self.flat_base = base
+        self.flat = base[param_pad:]
+        self.state = []
+        for r in ranks:
+            o, n = int(p["rank_offsets"][r]), int(p["rank_numels"][r])
+            mk = lambda v: torch.cat([torch.zeros(state_pad, device=DEV), v])[state_pad:]
+            A = [mk(self.flat[o:o + n].float()), mk(torch.zeros(n, device=DEV)), mk(torch.zeros(n, device=DEV))]
+            B = [mk(torch.empty(n, device=DEV)) for _ in range(3)] if pingpong else A
+            g = torch.empty(n, dtype=TDT[dt], device=DEV) if want_grad else None
+            self.state.append(dict(o=o, n=n, A=A, B=B, g=g))
+        self.ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+        self.res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+
+    def shards(self):
+        return [self.Z.shard(s["n"], s["o"], s["o"], *s["A"], *s["B"], s["g"]) for s in self.state]
+
+    def step(self, grads_u16, h, t, S, extra=(0.0, 0), grad_offsets=None):
+        Z = self.Z
+        slices = [dev16(g, self.dt) for g in grads_u16]
+        sh = self.shards()
+        if grad_offsets is not None:
+            for x, go in zip(sh, grad_offsets):
+                x.grad_offset = go
+        hy = Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], h["max_grad_norm"], t)
+        Z.zero_shard_step(slices, self.dt, sh, self.flat, self.dt, hy, S, extra[0], extra[1], self.ws,
+                          self.ws.numel(), self.res)
+        torch.cuda.synchronize()
+        r = Z.read_result(self.res)
+        if r.applied and self.pingpong:
+            for s in self.state:
+                s["A"], s["B"] = s["B"], s["A"]
+        return r
+
+    def master(self):
+        return [[x.cpu().numpy() for x in s["A"]] for s in self.state]
+
+
+def oracle_shards(p, flat, dt, ranks):
+    out = []
+    for r in ranks:
+        o, n = int(p["rank_offsets"][r]), int(p["rank_numels"][r])
+        out.append(dict(numel=n, grad_off=o, param_off=o, master=orc.widen_16(flat[o:o + n], dt),
+                        m=np.zeros(n, np.float32), v=np.zeros(n, np.float32)))
+    return out
+
+
+def compare(run, osh, oflat, r_gpu, r_or, exact):
+    assert (r_gpu.overflow, r_gpu.applied) == (r_or.overflow, r_or.applied)
+    gflat = t2u16(run.flat)
+    if r_or.applied:
+        assert r_gpu.grad_norm == pytest.approx(r_or.grad_norm, rel=1e-5)
+    if exact:
+        assert np.array_equal(gflat, oflat)
+    else:
+        d = np.abs(gflat.astype(np.int32) - oflat.astype(np.int32))
+        assert d.max() <= 1
+    for (th, m, v), o in zip(run.master(), osh):
+        for got, ref in ((th, o["master"]), (m, o["m"]), (v, o["v"])):
+            if exact:
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+            else:
+                assert np.all(np.abs(got - ref) <= 2e-6 * np.maximum(np.abs(ref), 1e-30))
+
+
+def run_both(Z, numels, nd, dt, mode, seed, h, S, pingpong, steps=3, inject=None, extra=(0.0, 0), ranks=None,
+             state_pad=0, param_pad=0, grad_std=1e-3):
+    p, flat, grads = make_problem(numels, nd, dt, mode, seed, loss_scale=S, grad_std=grad_std, steps=steps)
+    if inject:
+        inject(grads)
+    ranks = list(range(nd)) if ranks is None else ranks
+    run = GpuRun(Z, p, flat, dt, ranks, pingpong, state_pad=state_pad, param_pad=param_pad)
+    osh = oracle_shards(p, flat, dt, ranks)
+    oflat = flat.copy()
+    t, Sg, So = 1, S, S
+    exact = h["max_grad_norm"] <= 0
+    results = []
+    for k in range(steps):
+        r_gpu = run.step(grads[k], h, t, Sg, extra)
+        r_or, _ = orc.zero_step(grads[k], dt, osh, oflat, dt, h, t, So, *extra)
+        compare(run, osh, oflat, r_gpu, r_or, exact)
+        results.append((r_gpu.as_dict(), r_or.as_dict()))
+        if r_or.applied:
+            t += 1
+        else:
+            Sg /= 2
+            So /= 2
+    return results
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("pingpong", [True, False])
+def test_random_groups_match_oracle(Z, dt, pingpong):
+    rng = np.random.default_rng(40 + dt + 2 * pingpong)
+    for trial in range(6):
+        nd = int(rng.choice([1, 2, 3, 4, 5, 8, 13]))
+        numels = random_group(rng, 6, 40000)
+        mode = int(rng.integers(0, 2))
+        h = hyper32()
+        S = 1024.0 if dt == 1 else 1.0
+        run_both(Z, numels, nd, dt, mode, trial, h, S, pingpong)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+def test_clipped_two_pass_matches_oracle(Z, dt):
+    rng = np.random.default_rng(7 + dt)
+    for trial in range(4):
+        nd = int(rng.choice([2, 3, 4, 8]))
+        numels = random_group(rng, 5, 30000)
+        h = hyper32(max_grad_norm=0.01)
+        res = run_both(Z, numels, nd, dt, 0, 100 + trial, h, 8.0 if dt == 1 else 1.0, pingpong=bool(trial % 2),
+                       grad_std=1e-2)
+        assert all(g["clip_coef"] < 1.0 for g, _ in res)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("pingpong", [True, False])
+def test_tiny_workload_with_skip(Z, mode, pingpong):
+    """Tiny fp16 workload: N_d = 3, S = 1024, +inf at flat index 30000 of rank
+    0's gradient at step 2 -> step 2 skipped everywhere, S halves, t stays."""
+    def inject(grads):
+        grads[1][0] = grads[1][0].copy()
+        grads[1][0][30000] = 0x7C00
+    res = run_both(Z, W.numels(W.tiny_group()), 3, 1, mode, 0, hyper32(), 1024.0, pingpong, inject=inject)
+    assert [g["applied"] for g, _ in res] == [1, 0, 1]
+
+
+@pytest.mark.parametrize("bad", [0x7E00, 0xFC00])
+def test_nan_and_negative_inf_skip(Z, bad):
+    def inject(grads):
+        grads[0][2] = grads[0][2].copy()
+        grads[0][2][5] = bad
+    res = run_both(Z, [3000, 5000], 4, 1, 0, 3, hyper32(), 256.0, True, steps=2, inject=inject)
+    assert res[0][0]["overflow"] == 1 and res[0][0]["applied"] == 0
+
+
+def test_finite_inputs_whose_sum_overflows(Z):
+    big = np.uint16(0x7F61)   # bf16 ~2.99e38
+    def inject(grads):
+        for r in range(2):
+            grads[0][r] = grads[0][r].copy()
+            grads[0][r][1234] = big
+    res = run_both(Z, [4096], 2, 2, 0, 5, hyper32(), 1.0, True, steps=2, inject=inject)
+    assert res[0][0]["overflow"] == 1 and res[1][0]["applied"] == 1
+
+
+def test_huge_finite_squares_use_fp64(Z):
+    # bf16 values near 1e20: their squares exceed the fp32 range but the norm is finite
+    def inject(grads):
+        for r in range(2):
+            grads[0][r] = grads[0][r].copy()
+            grads[0][r][100:108] = 0x60AD   # ~1e20
+    res = run_both(Z, [20000], 2, 2, 0, 6, hyper32(), 1.0, True, steps=1, inject=inject)
+    g, o = res[0]
+    assert np.isfinite(g["grad_norm"]) and g["grad_norm"] == pytest.approx(o["grad_norm"], rel=1e-6)
+
+
+@pytest.mark.parametrize("nd", [1, 13, 64])
+def test_slice_counts(Z, nd):
+    run_both(Z, [9000, 1234], nd, 1, 0, nd, hyper32(), 4096.0 / nd, True, steps=2)
+
+
+def test_unaligned_pointers_take_the_scalar_path(Z):
+    # state views 1 float into their buffers and a flat parameter buffer 1 element in: not 16-byte aligned
+    run_both(Z, [5000, 77], 3, 2, 0, 8, hyper32(), 1.0, True, state_pad=1, param_pad=1, steps=2)
+    run_both(Z, [5000, 77], 3, 1, 1, 9, hyper32(), 512.0, False, state_pad=1, param_pad=3, steps=2)
+
+
+def test_empty_shards_and_no_shards(Z):
+    run_both(Z, [3], 8, 2, 1, 11, hyper32(), 1.0, True, steps=2)      # ranks 3..7 own nothing
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    g = torch.zeros(16, dtype=torch.bfloat16, device=DEV)
+    Z.zero_shard_step([g], Z.ZERO_BF16, [], None, Z.ZERO_BF16, Z.hyper(), 1.0, 2.25, 0, ws, ws.numel(), res)
+    torch.cuda.synchronize()
+    r = Z.read_result(res)
+    assert r.applied == 1 and r.sumsq == 2.25 and r.grad_norm == 1.5
+
+
+def test_rank_local_view_with_other_ranks_statistics(Z):
+    numels = [30000, 999]
+    nd, dt = 4, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 12, steps=3)
+    r = 1
+    o, n = int(p["rank_offsets"][r]), int(p["rank_numels"][r])
+    staged = [[g[o:o + n].copy() for g in step] for step in grads]   # the 4 slices staged for rank 1
+    h = hyper32(max_grad_norm=0.02)
+    run = GpuRun(Z, p, flat, dt, [r], pingpong=False)
+    osh = oracle_shards(p, flat, dt, [r])
+    osh[0]["grad_off"] = 0
+    oflat = flat.copy()
+    extra = (0.37, 0)
+    for t in (1, 2, 3):
+        rg = run.step(staged[t - 1], h, t, 1.0, extra, grad_offsets=[0])
+        ro, _ = orc.zero_step(staged[t - 1], dt, osh, oflat, dt, h, t, 1.0, *extra)
+        compare(run, osh, oflat, rg, ro, exact=False)
+        outside = np.concatenate([t2u16(run.flat)[:o], t2u16(run.flat)[o + n:]])
+        assert np.array_equal(outside, np.concatenate([flat[:o], flat[o + n:]]))   # other ranks' slots untouched
+    rg = run.step(staged[0], h, 4, 1.0, (0.0, 1))
+    assert rg.overflow == 1 and rg.applied == 0
+
+
+def test_reduce_and_apply_separately_accumulate(Z):
+    """Two reduce calls (accumulate 0 then 1) over two halves of the shards,
+    then one apply: same as the oracle's single step."""
+    numels = [40000, 333]
+    nd, dt = 3, 1
+    p, flat, grads = make_problem(numels, nd, dt, 0, 13, loss_scale=64.0, steps=1)
+    run = GpuRun(Z, p, flat, dt, list(range(nd)), pingpong=False)
+    slices = [dev16(g, dt) for g in grads[0]]
+    sh = run.shards()
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    Z.zero_shard_reduce(slices, dt, sh[:1], 0, stats, run.ws, run.ws.numel())
+    Z.zero_shard_reduce(slices, dt, sh[1:], 1, stats, run.ws, run.ws.numel())
+    h = hyper32(max_grad_norm=5.0)
+    Z.zero_shard_apply(sh, dt, run.flat, dt, Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"],
+                                                     h["max_grad_norm"], 1), 64.0, stats, 0.0, 0, run.res)
+    torch.cuda.synchronize()
+    osh = oracle_shards(p, flat, dt, list(range(nd)))
+    oflat = flat.copy()
+    ro, red = orc.zero_step(grads[0], dt, osh, oflat, dt, h, 1, 64.0, want_grad=True)
+    for s, rr in zip(run.state, red):
+        assert np.array_equal(t2u16(s["g"]), rr)            # reduced gradients bit-exact
+    st = Z.read_stats(stats)
+    assert st.overflow == 0 and st.sumsq == pytest.approx(ro.sumsq, rel=1e-6)
+    compare(run, osh, oflat, Z.read_result(run.res), ro, exact=False)
+
+
+def test_deterministic(Z):
+    numels = [200000]
+    p, flat, grads = make_problem(numels, 8, 2, 0, 14, steps=1)
+    outs = []
+    for _ in range(2):
+        run = GpuRun(Z, p, flat, 2, list(range(8)), pingpong=True)
+        r = run.step(grads[0], hyper32(), 1, 1.0)
+        outs.append((r.sumsq, t2u16(run.flat)))
+    assert outs[0][0] == outs[1][0] and np.array_equal(outs[0][1], outs[1][1])

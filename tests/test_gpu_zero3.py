@@ -1,0 +1,135 @@
+"""GPU parity of the ZeRO-3 per-layer steps against the CPU oracle.
+
+Stage 3 (ZeRO reading notes, 7 and 9): before a layer's forward, and again
+before its backward, the layer's parameter parts are gathered from every rank
+into one contiguous buffer; after its backward the layer's gradients are
+reduced onto the owner of each part; the owner then runs the shard update.
+Gather and reduce are bit-exact; the update follows the step's tolerances."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as W
+from helpers import hyper32, t2u16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TDT = {1: torch.float16, 2: torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def Z():
+    import zero_dp_partitioned_gb300 as Z
+    return Z
+
+
+def dev16(a, dt):
+    return torch.from_numpy(a.view(np.int16).copy()).view(TDT[dt]).to(DEV)
+
+
+@pytest.mark.parametrize("ws,part", [(1, 5000), (2, 4096), (4, 54528), (4, 1001), (8, 2049), (3, 7)])
+def test_gather_is_exact(Z, ws, part):
+    rng = np.random.default_rng(ws * 1000 + part)
+    parts = [rng.integers(0, 1 << 16, part, dtype=np.uint64).astype(np.uint16) for _ in range(ws)]
+    dparts = [dev16(p, 2) for p in parts]
+    out = torch.full((ws * part,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    Z.zero3_gather_layer(dparts, ws * part, Z.ZERO_BF16, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(t2u16(out), orc.zero3_gather(parts))
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("ws,part", [(4, 54528), (4, 999), (2, 8), (8, 10000)])
+def test_reduce_bucket_is_exact(Z, dt, ws, part):
+    g = W.generator(ws + part, "cpu")
+    buckets = []
+    for r in range(ws):
+        b = torch.zeros(ws * part, dtype=TDT[dt])
+        W.fill_normal_(b, 5e-4, g, 256.0 if dt == 1 else 1.0)
+        buckets.append(t2u16(b))
+    ws_buf = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    acc = orc.ExactAccumulator()
+    for owner in range(ws):
+        out = torch.empty(part, dtype=TDT[dt], device=DEV)
+        Z.zero3_reduce_bucket([dev16(b, dt) for b in buckets], owner, ws * part, dt, out, owner > 0, stats, ws_buf,
+                              ws_buf.numel())
+        torch.cuda.synchronize()
+        ref, ovf = orc.zero3_reduce(buckets, owner, part, dt, acc)
+        assert np.array_equal(t2u16(out), ref) and ovf == 0
+    st = Z.read_stats(stats)
+    assert st.overflow == 0 and st.sumsq == pytest.approx(acc.value(), rel=1e-6)
+
+
+def test_layer_pipeline_three_steps(Z):
+    """A small Llama-shaped group as ZeRO-3 units, rank 1 of 4: each step
+    gathers every unit forward and backward, reduces every unit's gradients
+    onto rank 1's part, and updates rank 1's parameter shard."""
+    specs = W.llama_group(L=3, d=64, hq=4, hkv=2, hd=16, ff=160, V=300)
+    units = W.llama_units(specs, L=3)
+    nd, me, dt = 4, 1, 2
+    assert all(u % nd == 0 for u in units)
+    parts = [u // nd for u in units]
+    uoff = np.concatenate([[0], np.cumsum(parts)[:-1]]).astype(int)
+    shard_len = int(sum(parts))
+    # the full model's parameters, cut into units and parts: rank r's persistent shard is its parts of every unit
+    flat = torch.zeros(sum(units), dtype=torch.bfloat16)
+    W.init_params_(flat, specs, W.generator(3, "cpu"))
+    flat = t2u16(flat)
+    shards = [np.concatenate([flat[sum(units[:u]) + r * parts[u]: sum(units[:u]) + (r + 1) * parts[u]]
+                              for u in range(len(units))]) for r in range(nd)]
+    gens = [W.generator(5 + r, "cpu") for r in range(nd)]
+    h = hyper32()
+
+    d_shards = [dev16(s, dt) for s in shards]
+    master = torch.from_numpy(orc.widen_16(shards[me], dt)).to(DEV)
+    m = torch.zeros(shard_len, device=DEV)
+    v = torch.zeros(shard_len, device=DEV)
+    gshard = torch.empty(shard_len, dtype=torch.bfloat16, device=DEV)
+    layer = torch.empty(max(units), dtype=torch.bfloat16, device=DEV)
+    wsb = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+
+    o_master = orc.widen_16(shards[me], dt)
+    o_m = np.zeros(shard_len, np.float32)
+    o_v = np.zeros(shard_len, np.float32)
+    o_param = shards[me].copy()
+    for t in (1, 2, 3):
+        buckets = []
+        for u, U in enumerate(units):
+            row = []
+            for r in range(nd):
+                b = torch.zeros(U, dtype=torch.bfloat16)
+                W.fill_normal_(b, 5e-4, gens[r])
+                row.append(t2u16(b))
+            buckets.append(row)
+        order = list(range(len(units))) + list(reversed(range(len(units))))   # forward, then backward
+        for u in order:
+            ptrs = [d_shards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)]
+            Z.zero3_gather_layer(ptrs, units[u], dt, layer)
+            torch.cuda.synchronize()
+            host_parts = [s[uoff[u]:uoff[u] + parts[u]] for s in shards]
+            host_parts[me] = t2u16(d_shards[me][uoff[u]:uoff[u] + parts[u]])
+            assert np.array_equal(t2u16(layer[:units[u]]), orc.zero3_gather(host_parts))
+        acc = orc.ExactAccumulator()
+        o_g = np.empty(shard_len, np.uint16)
+        for k, u in enumerate(reversed(range(len(units)))):
+            Z.zero3_reduce_bucket([dev16(b, dt) for b in buckets[u]], me, units[u], dt,
+                                  gshard[uoff[u]:uoff[u] + parts[u]], k > 0, stats, wsb, wsb.numel())
+            o_g[uoff[u]:uoff[u] + parts[u]], _ = orc.zero3_reduce(buckets[u], me, parts[u], dt, acc)
+        sh = [Z.shard(shard_len, 0, 0, master, m, v, grad_shard=gshard)]
+        Z.zero_shard_apply(sh, dt, d_shards[me], dt, Z.hyper(step=t, **{k: h[k] for k in
+                           ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, stats, 0.0, 0, res)
+        torch.cuda.synchronize()
+        # the oracle, in the same order: reduce every unit, then the shard update
+        k_mult, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+        sc = orc.make_scalars(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t)
+        orc.apply(o_g, dt, o_master, o_m, o_v, o_param, dt, k_mult, sc)
+        assert np.array_equal(t2u16(gshard), o_g)
+        r = Z.read_result(res)
+        assert r.applied == 1 and r.grad_norm == pytest.approx(norm, rel=1e-5)
+        assert np.array_equal(t2u16(d_shards[me]), o_param)
+        assert np.array_equal(master.cpu().numpy().view(np.uint32), o_master.view(np.uint32))
+        assert np.array_equal(v.cpu().numpy().view(np.uint32), o_v.view(np.uint32))

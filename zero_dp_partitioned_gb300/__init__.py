@@ -1,0 +1,207 @@
+"""GB300-native ZeRO-DP partitioned mixed-precision optimizer step.
+
+A thin ctypes binding of ``libzero_gb300.so`` (C ABI in ``include/zero.h``):
+the functions here have the C names and only marshal arguments -- every step
+of the path runs in the library's CUDA kernels.  Pointers may be given as
+torch tensors (their ``data_ptr()``) or as integers.  A nonzero status raises
+``ZeroError`` with the library's message.
+
+Importing this package loads the compiled library; if it has not been built
+(``python -m zero_dp_partitioned_gb300.build``) the import fails -- there is
+no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libzero_gb300.so")
+
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA, ZERO_ELIMIT = 0, -1, -2, -3, -4, -5
+ZERO_F16, ZERO_BF16 = 1, 2
+ZERO_PLAN_PADDED, ZERO_PLAN_UNPADDED = 0, 1
+ZERO_MAX_SLICES = ZERO_MAX_SHARDS = 64
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{msg} (status {code})")
+        self.code = code
+
+
+class zero_hyper(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
+                ("step", ctypes.c_int64)]
+
+
+class zero_shard(ctypes.Structure):
+    _fields_ = [("numel", ctypes.c_int64), ("grad_offset", ctypes.c_int64), ("param_offset", ctypes.c_int64),
+                ("master_in", ctypes.c_void_p), ("m_in", ctypes.c_void_p), ("v_in", ctypes.c_void_p),
+                ("master_out", ctypes.c_void_p), ("m_out", ctypes.c_void_p), ("v_out", ctypes.c_void_p),
+                ("grad_shard", ctypes.c_void_p)]
+
+
+class zero_stats(ctypes.Structure):
+    _fields_ = [("sumsq", ctypes.c_double), ("overflow", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class zero_result(ctypes.Structure):
+    _fields_ = [("overflow", ctypes.c_int32), ("applied", ctypes.c_int32), ("path", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("sumsq", ctypes.c_double), ("grad_norm", ctypes.c_double),
+                ("clip_coef", ctypes.c_double), ("grad_mult", ctypes.c_float), ("reserved2", ctypes.c_float)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if not k.startswith("reserved")}
+
+
+assert ctypes.sizeof(zero_hyper) == 32 and ctypes.sizeof(zero_shard) == 80
+assert ctypes.sizeof(zero_stats) == 16 and ctypes.sizeof(zero_result) == 48
+
+_P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+_SIGS = {
+    "zero_plan": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "zero_plan_intersections": (_I, [_P, _P, _I, _I64, _I64, _P]),
+    "zero_mem_model": (_I, [ctypes.c_double, ctypes.c_double, _I, _I, _P]),
+    "zero_workspace_bytes": (ctypes.c_size_t, []),
+    "zero_shard_step": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P,
+                             ctypes.c_size_t, _P, _P]),
+    "zero_shard_reduce": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "zero_shard_apply": (_I, [_P, _I, _I, _P, _I, _P, ctypes.c_float, _P, ctypes.c_double, _I, _P, _P]),
+    "zero3_gather_layer": (_I, [_P, _I, _I64, _I, _P, _P]),
+    "zero3_reduce_bucket": (_I, [_P, _I, _I, _I64, _I, _P, _I, _P, _P, ctypes.c_size_t, _P]),
+    "zero_last_error": (ctypes.c_char_p, []),
+}
+# every symbol include/zero.h declares
+EXPORTS = tuple(_SIGS)
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m zero_dp_partitioned_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream):
+    if stream is not None:
+        return _ptr(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+
+
+def _check(rc):
+    if rc < 0:
+        raise ZeroError(rc, lib.zero_last_error().decode())
+    return rc
+
+
+def _ptrs(xs):
+    return (ctypes.c_void_p * max(1, len(xs)))(*[_ptr(x) for x in xs])
+
+
+# ------------------------------------------------------------------ host-only calls
+def zero_plan(numels, world_size, mode=ZERO_PLAN_PADDED):
+    n = len(numels)
+    arr = (ctypes.c_int64 * max(1, n))(*numels)
+    t_off = (ctypes.c_int64 * max(1, n))()
+    r_off = (ctypes.c_int64 * world_size)()
+    r_num = (ctypes.c_int64 * world_size)()
+    padded, pad = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.zero_plan(arr, n, world_size, mode, t_off, r_off, r_num, ctypes.byref(padded), ctypes.byref(pad)))
+    return {"tensor_offsets": list(t_off)[:n], "rank_offsets": list(r_off), "rank_numels": list(r_num),
+            "padded_total": padded.value, "padding": pad.value}
+
+
+def zero_plan_intersections(tensor_offsets, numels, rank_offset, rank_numel):
+    n = len(numels)
+    t = (ctypes.c_int64 * max(1, n))(*tensor_offsets)
+    m = (ctypes.c_int64 * max(1, n))(*numels)
+    out = (ctypes.c_int64 * (4 * max(1, n)))()
+    k = _check(lib.zero_plan_intersections(t, m, n, rank_offset, rank_numel, out))
+    return [tuple(out[4 * i:4 * i + 4]) for i in range(k)]
+
+
+def zero_mem_model(psi, K, n_d, stage):
+    b = ctypes.c_double()
+    _check(lib.zero_mem_model(psi, K, n_d, stage, ctypes.byref(b)))
+    return b.value
+
+
+def zero_workspace_bytes():
+    return lib.zero_workspace_bytes()
+
+
+# ------------------------------------------------------------------ device calls
+def shard(numel, grad_offset, param_offset, master_in, m_in, v_in, master_out=None, m_out=None, v_out=None,
+          grad_shard=None) -> zero_shard:
+    """A zero_shard; *_out default to *_in (in-place)."""
+    return zero_shard(numel, grad_offset, param_offset, _ptr(master_in), _ptr(m_in), _ptr(v_in),
+                      _ptr(master_out if master_out is not None else master_in),
+                      _ptr(m_out if m_out is not None else m_in),
+                      _ptr(v_out if v_out is not None else v_in), _ptr(grad_shard))
+
+
+def hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_grad_norm=0.0, step=1) -> zero_hyper:
+    return zero_hyper(lr, beta1, beta2, eps, weight_decay, max_grad_norm, step)
+
+
+def zero_shard_step(grad_slices, grad_dtype, shards, flat_param, param_dtype, hyper, loss_scale,
+                    extra_sumsq, extra_overflow, workspace, workspace_bytes, result, stream=None):
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_step(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards), _ptr(flat_param),
+                               param_dtype, ctypes.byref(hyper), loss_scale, extra_sumsq, int(extra_overflow),
+                               _ptr(workspace), workspace_bytes, _ptr(result), _stream(stream)))
+
+
+def zero_shard_reduce(grad_slices, grad_dtype, shards, accumulate, stats, workspace, workspace_bytes, stream=None):
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_reduce(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards), int(accumulate),
+                                 _ptr(stats), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def zero_shard_apply(shards, grad_dtype, flat_param, param_dtype, hyper, loss_scale, stats, extra_sumsq,
+                     extra_overflow, result, stream=None):
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_apply(sh, len(shards), grad_dtype, _ptr(flat_param), param_dtype, ctypes.byref(hyper),
+                                loss_scale, _ptr(stats), extra_sumsq, int(extra_overflow), _ptr(result),
+                                _stream(stream)))
+
+
+def zero3_gather_layer(part_ptrs, unit_numel, dtype, layer_out, stream=None):
+    _check(lib.zero3_gather_layer(_ptrs(part_ptrs), len(part_ptrs), unit_numel, dtype, _ptr(layer_out),
+                                  _stream(stream)))
+
+
+def zero3_reduce_bucket(bucket_ptrs, owner, unit_numel, grad_dtype, grad_part, accumulate, stats, workspace,
+                        workspace_bytes, stream=None):
+    _check(lib.zero3_reduce_bucket(_ptrs(bucket_ptrs), len(bucket_ptrs), owner, unit_numel, grad_dtype,
+                                   _ptr(grad_part), int(accumulate), _ptr(stats), _ptr(workspace), workspace_bytes,
+                                   _stream(stream)))
+
+
+def read_result(t) -> zero_result:
+    """A zero_result from a 48-byte tensor (device or host)."""
+    b = bytes(t.detach().cpu().view(-1).numpy().tobytes()) if hasattr(t, "detach") else bytes(t)
+    return zero_result.from_buffer_copy(b[:ctypes.sizeof(zero_result)])
+
+
+def read_stats(t) -> zero_stats:
+    b = bytes(t.detach().cpu().view(-1).numpy().tobytes())
+    return zero_stats.from_buffer_copy(b[:ctypes.sizeof(zero_stats)])

@@ -1,0 +1,395 @@
+// zero_abi.cu -- the C entry points declared in include/zero.h: argument
+// checks, choice of the single- or two-pass path, packing of the kernel
+// arguments, and the host-only planner and memory model.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+
+#include "zero_internal.h"
+
+namespace zdp {
+
+static thread_local std::string g_err;
+
+void set_error(const std::string& msg) { g_err = msg; }
+
+int cuda_fail(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ZERO_OK;
+    set_error(std::string(what) + ": " + cudaGetErrorString(e));
+    return ZERO_ECUDA;
+}
+
+int grid_for(const void* func, int64_t n_tiles) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> per_sm[16];
+    static int sms[16] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    dev &= 15;
+    int nb = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        auto it = per_sm[dev].find(func);
+        if (it == per_sm[dev].end()) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, TILE_THREADS, 0) != cudaSuccess || nb < 1)
+                nb = 1;
+            per_sm[dev][func] = nb;
+        } else {
+            nb = it->second;
+        }
+    }
+    int64_t g = (int64_t)nb * (sms[dev] > 0 ? sms[dev] : 1);
+    if (g > n_tiles) g = n_tiles;
+    if (g > MAX_BLOCKS) g = MAX_BLOCKS;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static bool valid_dtype(int d) { return d == ZERO_F16 || d == ZERO_BF16; }
+
+static int fail(int code, const char* msg) {
+    set_error(msg);
+    return code;
+}
+
+// Host scalars of one AdamW step: each computed in fp64 from the fp32
+// hyper-parameters and rounded once to fp32; the bias corrections are folded
+// into ss = lr / (1 - b1^t) and rb2 = 1 / sqrt(1 - b2^t).
+static AdamScalars adam_scalars(const zero_hyper& h) {
+    const double t = (double)h.step;
+    const double bc1 = 1.0 - std::pow((double)h.beta1, t);
+    const double bc2 = 1.0 - std::pow((double)h.beta2, t);
+    AdamScalars c;
+    c.b1 = h.beta1;
+    c.b2 = h.beta2;
+    c.omb1 = (float)(1.0 - (double)h.beta1);
+    c.omb2 = (float)(1.0 - (double)h.beta2);
+    c.eps = h.eps;
+    c.wdf = (float)(1.0 - (double)h.lr * (double)h.weight_decay);
+    c.ss = (float)((double)h.lr / bc1);
+    c.rb2 = (float)(1.0 / std::sqrt(bc2));
+    return c;
+}
+
+// Common checks of slices and shards; fills the shard part of a and the tile
+// numbering for vector width vec.  need: 1 = fused (state in/out), 2 = reduce
+// (grad_shard out), 3 = apply (grad_shard in, state in/out).
+static int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int need) {
+    if (n_shards < 0) return fail(ZERO_EINVAL, "n_shards < 0");
+    if (n_shards > ZERO_MAX_SHARDS) return fail(ZERO_ELIMIT, "more than ZERO_MAX_SHARDS shards");
+    if (n_shards > 0 && !shards) return fail(ZERO_EINVAL, "shards is NULL");
+    a.n_shards = n_shards;
+    for (int i = 0; i < n_shards; ++i) {
+        const zero_shard& s = shards[i];
+        if (s.numel < 0 || s.grad_offset < 0 || s.param_offset < 0)
+            return fail(ZERO_EINVAL, "negative shard size or offset");
+        if (s.numel > 0) {
+            if (need != 2) {
+                if (!s.master_in || !s.m_in || !s.v_in || !s.master_out || !s.m_out || !s.v_out)
+                    return fail(ZERO_EINVAL, "shard state pointer is NULL");
+                const void* ps[6] = {s.master_in, s.m_in, s.v_in, s.master_out, s.m_out, s.v_out};
+                for (const void* p : ps)
+                    if (!aligned(p, 4)) return fail(ZERO_EALIGN, "fp32 state pointer not 4-byte aligned");
+            }
+            if (need != 1) {
+                if (!s.grad_shard) return fail(ZERO_EINVAL, "grad_shard is NULL (the two-pass path needs it)");
+                if (!aligned(s.grad_shard, 2)) return fail(ZERO_EALIGN, "grad_shard not 2-byte aligned");
+            }
+        }
+        ShardDev& d = a.shards[i];
+        d.numel = s.numel;
+        d.grad_off = s.grad_offset;
+        d.param_off = s.param_offset;
+        d.mi = s.master_in;
+        d.mmi = s.m_in;
+        d.vi = s.v_in;
+        d.mo = s.master_out;
+        d.mmo = s.m_out;
+        d.vo = s.v_out;
+        d.gshard = s.grad_shard;
+    }
+    return ZERO_OK;
+}
+
+static void number_tiles(StepArgs& a, int vec) {
+    const int64_t tile = (int64_t)TILE_THREADS * vec;
+    int64_t t = 0;
+    for (int i = 0; i < a.n_shards; ++i) {
+        a.shards[i].tile_begin = t;
+        t += (a.shards[i].numel + tile - 1) / tile;
+    }
+    a.n_tiles = t;
+}
+
+static int pack_slices(StepArgs& a, const void* const* slices, int n_slices) {
+    if (!slices) return fail(ZERO_EINVAL, "grad_slices is NULL");
+    if (n_slices < 1) return fail(ZERO_EINVAL, "n_slices < 1");
+    if (n_slices > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "more than ZERO_MAX_SLICES slices");
+    a.n_slices = n_slices;
+    for (int r = 0; r < n_slices; ++r) {
+        if (!slices[r]) return fail(ZERO_EINVAL, "a gradient slice is NULL");
+        if (!aligned(slices[r], 2)) return fail(ZERO_EALIGN, "gradient slice not 2-byte aligned");
+        a.slices[r] = slices[r];
+    }
+    a.divisor = (float)n_slices;
+    return ZERO_OK;
+}
+
+// 16-byte vectors are possible when every gradient address a shard starts at
+// and every pointer the vector path loads from are 16-byte aligned.
+static bool vec8_ok(const StepArgs& a, int need) {
+    for (int i = 0; i < a.n_shards; ++i) {
+        const ShardDev& d = a.shards[i];
+        if (d.numel == 0) continue;
+        if (need != 3)
+            for (int r = 0; r < a.n_slices; ++r)
+                if (!aligned(static_cast<const uint16_t*>(a.slices[r]) + d.grad_off, 16)) return false;
+        if (need != 2) {
+            const void* ps[6] = {d.mi, d.mmi, d.vi, d.mo, d.mmo, d.vo};
+            for (const void* p : ps)
+                if (!aligned(p, 16)) return false;
+        }
+        if (need == 3 && !aligned(d.gshard, 16)) return false;
+    }
+    return true;
+}
+
+static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
+    if (!ws) return fail(ZERO_EWORKSPACE, "workspace is NULL");
+    if (ws_bytes < WS_BYTES) return fail(ZERO_EWORKSPACE, "workspace smaller than zero_workspace_bytes()");
+    if (!aligned(ws, 16)) return fail(ZERO_EALIGN, "workspace not 16-byte aligned");
+    char* w = static_cast<char*>(ws);
+    a.counter = reinterpret_cast<unsigned*>(w + WS_COUNTER);
+    a.partials = reinterpret_cast<double*>(w + WS_PARTIALS);
+    a.block_flags = reinterpret_cast<int*>(w + WS_FLAGS);
+    return ZERO_OK;
+}
+
+static int check_hyper(const zero_hyper* h, float loss_scale) {
+    if (!h) return fail(ZERO_EINVAL, "hyper is NULL");
+    if (h->step < 1) return fail(ZERO_EINVAL, "hyper->step must be >= 1");
+    if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale)) return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
+    return ZERO_OK;
+}
+
+static bool any_elements(const StepArgs& a) {
+    for (int i = 0; i < a.n_shards; ++i)
+        if (a.shards[i].numel > 0) return true;
+    return false;
+}
+
+}  // namespace zdp
+
+using namespace zdp;
+
+extern "C" {
+
+const char* zero_last_error(void) { return g_err.c_str(); }
+
+size_t zero_workspace_bytes(void) { return WS_BYTES; }
+
+int zero_plan(const int64_t* numels, int n_tensors, int world_size, int mode, int64_t* tensor_offsets,
+              int64_t* rank_offsets, int64_t* rank_numels, int64_t* padded_total, int64_t* padding) {
+    if (n_tensors < 0 || world_size < 1 || (mode != ZERO_PLAN_PADDED && mode != ZERO_PLAN_UNPADDED))
+        return fail(ZERO_EINVAL, "zero_plan: bad n_tensors, world_size or mode");
+    if ((n_tensors > 0 && (!numels || !tensor_offsets)) || !rank_offsets || !rank_numels || !padded_total || !padding)
+        return fail(ZERO_EINVAL, "zero_plan: NULL argument");
+    int64_t total = 0;
+    for (int i = 0; i < n_tensors; ++i) {
+        if (numels[i] < 0) return fail(ZERO_EINVAL, "zero_plan: negative numel");
+        tensor_offsets[i] = total;
+        total += numels[i];
+    }
+    int64_t flat = total;
+    if (mode == ZERO_PLAN_PADDED) {
+        const int64_t q = 2 * (int64_t)world_size;      // 16-bit elements: shard starts on 4-byte boundaries
+        flat = (total + q - 1) / q * q;
+    }
+    const int64_t base = flat / world_size, rem = flat % world_size;
+    int64_t off = 0;
+    for (int r = 0; r < world_size; ++r) {
+        rank_offsets[r] = off;
+        rank_numels[r] = base + (r < rem ? 1 : 0);
+        off += rank_numels[r];
+    }
+    *padded_total = flat;
+    *padding = flat - total;
+    return ZERO_OK;
+}
+
+int zero_plan_intersections(const int64_t* tensor_offsets, const int64_t* numels, int n_tensors,
+                            int64_t rank_offset, int64_t rank_numel, int64_t* out) {
+    if (n_tensors < 0 || rank_offset < 0 || rank_numel < 0 || (n_tensors > 0 && (!tensor_offsets || !numels || !out)))
+        return fail(ZERO_EINVAL, "zero_plan_intersections: bad argument");
+    int rows = 0;
+    const int64_t lo = rank_offset, hi = rank_offset + rank_numel;
+    for (int i = 0; i < n_tensors; ++i) {
+        const int64_t a = tensor_offsets[i], b = a + numels[i];
+        const int64_t s = a > lo ? a : lo, e = b < hi ? b : hi;
+        if (e <= s) continue;
+        out[4 * rows + 0] = i;
+        out[4 * rows + 1] = s - a;
+        out[4 * rows + 2] = s - lo;
+        out[4 * rows + 3] = e - s;
+        ++rows;
+    }
+    return rows;
+}
+
+int zero_mem_model(double psi, double K, int n_d, int stage, double* bytes_out) {
+    if (!bytes_out || n_d < 1 || stage < 0 || stage > 3 || !(psi >= 0.0) || !(K >= 0.0))
+        return fail(ZERO_EINVAL, "zero_mem_model: bad argument");
+    const double N = (double)n_d;
+    double b = 0.0;
+    switch (stage) {
+    case 0: b = (4.0 + K) * psi; break;                 // DP: every rank holds everything
+    case 1: b = 4.0 * psi + K * psi / N; break;         // P_os
+    case 2: b = 2.0 * psi + (K + 2.0) * psi / N; break; // P_os+g
+    default: b = (4.0 + K) * psi / N; break;            // P_os+g+p
+    }
+    *bytes_out = b;
+    return ZERO_OK;
+}
+
+int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
+                    int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper, float loss_scale,
+                    double extra_sumsq, int extra_overflow, void* workspace, size_t workspace_bytes,
+                    zero_result* result, void* stream) {
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    int rc;
+    if ((rc = check_hyper(hyper, loss_scale)) != ZERO_OK) return rc;
+    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    if ((rc = pack_slices(a, grad_slices, n_slices)) != ZERO_OK) return rc;
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+
+    bool fused = hyper->max_grad_norm <= 0.0f;
+    for (int i = 0; fused && i < n_shards && shards; ++i)
+        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
+                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
+            fused = false;
+    if ((rc = pack_shards(a, shards, n_shards, fused ? 1 : 2)) != ZERO_OK) return rc;
+    if (!fused && (rc = pack_shards(a, shards, n_shards, 3)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = flat_param;
+    a.sc = adam_scalars(*hyper);
+    a.loss_scale = (double)loss_scale;
+    a.max_norm = (double)hyper->max_grad_norm;
+    a.extra_sumsq = extra_sumsq;
+    a.extra_overflow = extra_overflow ? 1 : 0;
+    a.result = result;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (fused) {
+        a.k = (float)(1.0 / (double)loss_scale);
+        const int vec = vec8_ok(a, 1) ? 8 : 1;
+        number_tiles(a, vec);
+        const int grid = grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles);
+        if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
+        return launch_recover(a, param_dtype, s);
+    }
+    a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
+    a.accumulate = 0;
+    int vec = vec8_ok(a, 2) ? 8 : 1;
+    number_tiles(a, vec);
+    if ((rc = launch_reduce(a, grad_dtype, vec, s)) != ZERO_OK) return rc;
+    vec = vec8_ok(a, 3) ? 8 : 1;
+    number_tiles(a, vec);
+    return launch_apply(a, grad_dtype, param_dtype, vec, s);
+}
+
+int zero_shard_reduce(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
+                      int n_shards, int accumulate, zero_stats* stats, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (!valid_dtype(grad_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (!stats || !aligned(stats, 8)) return fail(ZERO_EINVAL, "stats is NULL or not 8-byte aligned");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    int rc;
+    if ((rc = pack_slices(a, grad_slices, n_slices)) != ZERO_OK) return rc;
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+    if ((rc = pack_shards(a, shards, n_shards, 2)) != ZERO_OK) return rc;
+    a.stats = stats;
+    a.accumulate = accumulate ? 1 : 0;
+    const int vec = vec8_ok(a, 2) ? 8 : 1;
+    number_tiles(a, vec);
+    return launch_reduce(a, grad_dtype, vec, static_cast<cudaStream_t>(stream));
+}
+
+int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, void* flat_param, int param_dtype,
+                     const zero_hyper* hyper, float loss_scale, const zero_stats* stats, double extra_sumsq,
+                     int extra_overflow, zero_result* result, void* stream) {
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    int rc;
+    if ((rc = check_hyper(hyper, loss_scale)) != ZERO_OK) return rc;
+    if (!stats || !aligned(stats, 8)) return fail(ZERO_EINVAL, "stats is NULL or not 8-byte aligned");
+    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    if ((rc = pack_shards(a, shards, n_shards, 3)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = flat_param;
+    a.sc = adam_scalars(*hyper);
+    a.loss_scale = (double)loss_scale;
+    a.max_norm = (double)hyper->max_grad_norm;
+    a.extra_sumsq = extra_sumsq;
+    a.extra_overflow = extra_overflow ? 1 : 0;
+    a.stats = const_cast<zero_stats*>(stats);
+    a.result = result;
+    const int vec = vec8_ok(a, 3) ? 8 : 1;
+    number_tiles(a, vec);
+    return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));
+}
+
+int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t unit_numel, int dtype, void* layer_out,
+                       void* stream) {
+    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (world_size < 1) return fail(ZERO_EINVAL, "world_size < 1");
+    if (world_size > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "world_size above ZERO_MAX_SLICES");
+    if (unit_numel < 0 || unit_numel % world_size != 0)
+        return fail(ZERO_EINVAL, "unit_numel must be >= 0 and divisible by world_size");
+    if (unit_numel == 0) return ZERO_OK;
+    if (!part_ptrs || !layer_out) return fail(ZERO_EINVAL, "NULL pointer");
+    if (!aligned(layer_out, 2)) return fail(ZERO_EALIGN, "layer_out not 2-byte aligned");
+    GatherArgs g;
+    std::memset(&g, 0, sizeof g);
+    g.world_size = world_size;
+    g.part_numel = unit_numel / world_size;
+    g.out = layer_out;
+    bool v8 = aligned(layer_out, 16) && (g.part_numel % 8 == 0);
+    for (int r = 0; r < world_size; ++r) {
+        if (!part_ptrs[r]) return fail(ZERO_EINVAL, "a part pointer is NULL");
+        if (!aligned(part_ptrs[r], 2)) return fail(ZERO_EALIGN, "part pointer not 2-byte aligned");
+        v8 = v8 && aligned(part_ptrs[r], 16);
+        g.parts[r] = part_ptrs[r];
+    }
+    const int vec = v8 ? 8 : 1;
+    const int64_t tile = (int64_t)TILE_THREADS * vec * 2;
+    g.tiles_per_part = (g.part_numel + tile - 1) / tile;
+    return launch_gather(g, vec, static_cast<cudaStream_t>(stream));
+}
+
+int zero3_reduce_bucket(const void* const* bucket_ptrs, int world_size, int owner, int64_t unit_numel, int grad_dtype,
+                        void* grad_part, int accumulate, zero_stats* stats, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    if (world_size < 1 || owner < 0 || owner >= world_size) return fail(ZERO_EINVAL, "bad world_size or owner");
+    if (unit_numel < 0 || unit_numel % world_size != 0)
+        return fail(ZERO_EINVAL, "unit_numel must be >= 0 and divisible by world_size");
+    zero_shard s;
+    std::memset(&s, 0, sizeof s);
+    s.numel = unit_numel / world_size;
+    s.grad_offset = (int64_t)owner * s.numel;
+    s.grad_shard = grad_part;
+    return zero_shard_reduce(bucket_ptrs, world_size, grad_dtype, &s, 1, accumulate, stats, workspace,
+                             workspace_bytes, stream);
+}
+
+}  // extern "C"

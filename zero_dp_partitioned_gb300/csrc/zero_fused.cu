@@ -1,0 +1,46 @@
+// zero_fused.cu -- instantiations and launchers of the fused single pass (K1a)
+// and of the parameter restore that follows it (K1r).
+#include "zero_internal.h"
+
+namespace zdp {
+
+template <int G, int P, int V>
+static const void* fused_ptr(int ns) {
+    if (V == 1) return (const void*)k_step_fused<G, P, 1, 0>;
+    switch (ns) {
+    case 1: return (const void*)k_step_fused<G, P, V, 1>;
+    case 2: return (const void*)k_step_fused<G, P, V, 2>;
+    case 3: return (const void*)k_step_fused<G, P, V, 3>;
+    case 4: return (const void*)k_step_fused<G, P, V, 4>;
+    case 8: return (const void*)k_step_fused<G, P, V, 8>;
+    default: return (const void*)k_step_fused<G, P, V, 0>;
+    }
+}
+
+template <int G, int P>
+static const void* fused_ptr_v(int vec, int ns) {
+    return vec == 8 ? fused_ptr<G, P, 8>(ns) : fused_ptr<G, P, 1>(ns);
+}
+
+const void* fused_kernel(int gdt, int pdt, int vec, int ns) {
+    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_BF16, ZERO_BF16>(vec, ns)
+                                                  : fused_ptr_v<ZERO_BF16, ZERO_F16>(vec, ns);
+    return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_F16, ZERO_BF16>(vec, ns) : fused_ptr_v<ZERO_F16, ZERO_F16>(vec, ns);
+}
+
+int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s) {
+    const void* f = fused_kernel(gdt, pdt, vec, ns_variant(a.n_slices));
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "fused step launch");
+}
+
+int launch_recover(const StepArgs& a, int pdt, cudaStream_t s) {
+    const void* f = pdt == ZERO_BF16 ? (const void*)k_recover<ZERO_BF16> : (const void*)k_recover<ZERO_F16>;
+    int64_t n = 0;
+    for (int i = 0; i < a.n_shards; ++i) n = a.shards[i].numel > n ? a.shards[i].numel : n;
+    const int grid = grid_for(f, (n + TILE_THREADS - 1) / TILE_THREADS);
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "recover launch");
+}
+
+}  // namespace zdp

@@ -1,0 +1,531 @@
+// zero_kernels.cuh -- device code of the partitioned mixed-precision step for
+// sm_103a (GB300).  Everything here is memory-bound streaming: per shard
+// element the fused pass moves 2*N_d bytes of gradient slices, 12 bytes of
+// fp32 state in and 12 out, and 2 bytes of parameter out.  No tensor cores:
+// nothing on this path is a contraction.
+//
+// Design:
+//  * Work unit = a tile of TILE_THREADS x VEC elements of one shard; tiles are
+//    numbered shard after shard and a grid of (SM count x resident blocks)
+//    strides over them.  VEC = 8 uses 128-bit loads of 8 16-bit gradients
+//    per slice and two 128-bit loads per fp32 state array; VEC = 1 is the
+//    path for pointers that are not 16-byte aligned.
+//  * All loads of one vector (state first, then the slices in groups of 8)
+//    are issued before their values are used, so each thread keeps ~100-250
+//    bytes in flight; loads and stores use the streaming cache hints because
+//    no byte is touched twice.
+//  * Gradient statistics: squares of the 16-bit reduced values are exact in
+//    fp32 (at most 22 significant bits) and are summed per vector in fp32,
+//    then in fp64 per thread; a warp-shuffle and a shared-memory pass give
+//    one fp64 partial per block, stored in the workspace; the last block to
+//    finish (one atomic per block) adds the partials in block order, so the
+//    result is deterministic for a given grid.
+//  * Every fp32 operation of the reduction and of AdamW is an explicitly
+//    rounded intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn) so no
+//    multiply-add is contracted: results are those of the plain IEEE sequence.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "zero.h"
+
+namespace zdp {
+
+constexpr int TILE_THREADS = 256;
+constexpr int MAX_BLOCKS = 2048;
+
+// ---------------------------------------------------------------- layout of the workspace
+// [0, 64)              completion counter (unsigned) -- zero between calls
+// [64, 80)             the step's internal zero_stats (two-pass path of zero_shard_step)
+// [128, 128 + 8*MB)    per-block fp64 partial sums of squares
+// [.., + 4*MB)         per-block overflow flags
+constexpr size_t WS_COUNTER = 0;
+constexpr size_t WS_STATS = 64;
+constexpr size_t WS_PARTIALS = 128;
+constexpr size_t WS_FLAGS = WS_PARTIALS + 8 * (size_t)MAX_BLOCKS;
+constexpr size_t WS_BYTES = ((WS_FLAGS + 4 * (size_t)MAX_BLOCKS) + 4095) / 4096 * 4096;
+
+// ---------------------------------------------------------------- kernel arguments
+struct ShardDev {
+    int64_t numel, grad_off, param_off;
+    int64_t tile_begin;             // index of the shard's first tile
+    const float *mi, *mmi, *vi;     // master, m, v in
+    float *mo, *mmo, *vo;           // master, m, v out
+    void* gshard;                   // 16-bit reduced gradient shard
+};
+
+struct AdamScalars {                // fp32, each rounded once from fp64 on the host
+    float b1, b2, omb1, omb2, eps, wdf, ss, rb2;
+};
+
+struct StepArgs {
+    const void* slices[ZERO_MAX_SLICES];
+    ShardDev shards[ZERO_MAX_SHARDS];
+    int n_slices, n_shards;
+    int64_t n_tiles;
+    void* flat_param;
+    float divisor;                  // N_d
+    float k;                        // gradient multiplier (fused path: 1/S, exact for S a power of two)
+    AdamScalars sc;
+    double loss_scale, max_norm, extra_sumsq;
+    int extra_overflow, accumulate;
+    double* partials;
+    int* block_flags;
+    unsigned* counter;
+    zero_stats* stats;
+    zero_result* result;
+};
+
+// ---------------------------------------------------------------- 16-bit conversions
+template <int DT> struct Half16;
+template <> struct Half16<ZERO_BF16> {
+    static __device__ __forceinline__ float widen(uint32_t h) { return __uint_as_float(h << 16); }
+    static __device__ __forceinline__ uint32_t narrow(float x) {
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+    }
+    static __device__ __forceinline__ bool nonfinite(uint32_t h) { return (h & 0x7F80u) == 0x7F80u; }
+};
+template <> struct Half16<ZERO_F16> {
+    static __device__ __forceinline__ float widen(uint32_t h) {
+        return __half2float(__ushort_as_half((unsigned short)h));
+    }
+    static __device__ __forceinline__ uint32_t narrow(float x) {
+        return (uint32_t)__half_as_ushort(__float2half_rn(x));
+    }
+    static __device__ __forceinline__ bool nonfinite(uint32_t h) { return (h & 0x7C00u) == 0x7C00u; }
+};
+
+// 8 packed 16-bit values (one uint4) -> fp32, added in order to s[0..7]
+template <int DT>
+__device__ __forceinline__ void add8(float (&s)[8], const uint4& w) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        s[2 * q] = __fadd_rn(s[2 * q], Half16<DT>::widen(u[q] & 0xFFFFu));
+        s[2 * q + 1] = __fadd_rn(s[2 * q + 1], Half16<DT>::widen(u[q] >> 16));
+    }
+}
+
+// ---------------------------------------------------------------- streaming memory access
+__device__ __forceinline__ uint4 ld_stream(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ float4 ld_stream4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ void st_stream4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
+
+// ---------------------------------------------------------------- per-element arithmetic
+// Reduce-scatter arithmetic for one element: s is the rank-ordered fp32 sum.
+template <int GDT>
+__device__ __forceinline__ uint32_t average16(float s, float divisor) {
+    return Half16<GDT>::narrow(__fdiv_rn(s, divisor));
+}
+
+// AdamW on one coordinate, the operations in the order of the update rule.
+__device__ __forceinline__ void adamw1(float& th, float& m, float& v, float a, float k, const AdamScalars& c) {
+    const float g = __fmul_rn(a, k);
+    th = __fmul_rn(th, c.wdf);
+    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
+    const float g2 = __fmul_rn(g, g);
+    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, g2));
+    const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v), c.rb2), c.eps);
+    th = __fsub_rn(th, __fmul_rn(c.ss, __fdiv_rn(m, den)));
+}
+
+// Store 8 16-bit values at dst + q with the widest stores its address allows
+// (16, 4 or 2 bytes; the choice is uniform across a shard's vectors).
+__device__ __forceinline__ void store8(uint16_t* dst, int64_t q, const uint32_t (&h)[8]) {
+    const int mis = (int)(reinterpret_cast<uintptr_t>(dst + q) & 15u);
+    if (mis == 0) {
+        uint4 w;
+        w.x = h[0] | (h[1] << 16);
+        w.y = h[2] | (h[3] << 16);
+        w.z = h[4] | (h[5] << 16);
+        w.w = h[6] | (h[7] << 16);
+        __stcs(reinterpret_cast<uint4*>(dst + q), w);
+    } else if ((mis & 3) == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) __stcs(reinterpret_cast<unsigned*>(dst + q + e), h[e] | (h[e + 1] << 16));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) __stcs(reinterpret_cast<unsigned short*>(dst + q + e), (unsigned short)h[e]);
+    }
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ double warp_sum(double x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Block-wide sum (fixed order) of x and OR of f; valid in thread 0.
+__device__ __forceinline__ void block_reduce(double& x, int& f) {
+    __shared__ double sx[TILE_THREADS / 32];
+    __shared__ int sf[TILE_THREADS / 32];
+    x = warp_sum(x);
+    f = __any_sync(0xffffffffu, f) ? 1 : 0;
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) { sx[w] = x; sf[w] = f; }
+    __syncthreads();
+    if (w == 0) {
+        x = l < TILE_THREADS / 32 ? sx[l] : 0.0;
+        f = l < TILE_THREADS / 32 ? sf[l] : 0;
+        x = warp_sum(x);
+        f = __any_sync(0xffffffffu, f) ? 1 : 0;
+    }
+}
+
+// Publish this block's partial; returns true in thread 0 of the last block to
+// finish, after which that block may read every partial.
+__device__ __forceinline__ bool publish_partial(const StepArgs& a, double x, int f) {
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+        a.partials[blockIdx.x] = x;
+        a.block_flags[blockIdx.x] = f;
+        __threadfence();
+        const unsigned done = atomicAdd(a.counter, 1u);
+        last = (done == gridDim.x - 1);
+    }
+    __syncthreads();
+    return last;
+}
+
+// In the last block: the sum of all partials in block order and the OR of the
+// flags (thread 0 gets the result); resets the counter for the next call.
+__device__ __forceinline__ void combine_partials(const StepArgs& a, double& sum, int& flag) {
+    __threadfence();
+    // fixed order: thread t adds partials t, t + 256, ... ; then the block sum
+    double x = 0.0;
+    int f = 0;
+    for (int b = threadIdx.x; b < (int)gridDim.x; b += TILE_THREADS) {
+        x += __ldcg(a.partials + b);
+        f |= __ldcg(a.block_flags + b);
+    }
+    block_reduce(x, f);
+    sum = x;
+    flag = f;
+    if (threadIdx.x == 0) *a.counter = 0u;
+}
+
+// Clip decision from the statistics (fp64, the same on every block).
+__device__ __forceinline__ float grad_multiplier(double sumsq, double S, double max_norm, double& norm,
+                                                 double& clip) {
+    norm = sqrt(sumsq) / S;
+    clip = 1.0;
+    if (max_norm > 0.0) {
+        const double c = max_norm / (norm + 1e-6);
+        if (c < 1.0) clip = c;
+    }
+    return (float)(clip / S);
+}
+
+__device__ __forceinline__ int find_shard(const StepArgs& a, int64_t tile) {
+    int s = 0;
+    while (s + 1 < a.n_shards && a.shards[s + 1].tile_begin <= tile) ++s;
+    return s;
+}
+
+// ---------------------------------------------------------------- gradient reduction of one vector
+// Sum of the n slices' 8 values at element offset off (rank order), with the
+// loads of each group of 8 slices issued together.
+template <int GDT, int NS>
+__device__ __forceinline__ void reduce8(const StepArgs& a, int64_t off, float (&s)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] = 0.0f;
+    if (NS > 0) {
+        uint4 w[NS > 0 ? NS : 1];
+#pragma unroll
+        for (int r = 0; r < NS; ++r) w[r] = ld_stream(static_cast<const uint16_t*>(a.slices[r]) + off);
+#pragma unroll
+        for (int r = 0; r < NS; ++r) add8<GDT>(s, w[r]);
+    } else {
+        const int n = a.n_slices;
+        int r = 0;
+        for (; r + 8 <= n; r += 8) {
+            uint4 w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w[q] = ld_stream(static_cast<const uint16_t*>(a.slices[r + q]) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) add8<GDT>(s, w[q]);
+        }
+        for (; r < n; ++r) add8<GDT>(s, ld_stream(static_cast<const uint16_t*>(a.slices[r]) + off));
+    }
+}
+
+template <int GDT>
+__device__ __forceinline__ float reduce1(const StepArgs& a, int64_t off) {
+    float s = 0.0f;
+    for (int r = 0; r < a.n_slices; ++r)
+        s = __fadd_rn(s, Half16<GDT>::widen(static_cast<const uint16_t*>(a.slices[r])[off]));
+    return s;
+}
+
+// ---------------------------------------------------------------- K1a: fused single pass
+// Reads the slices and the *_in state once, writes the *_out state and the
+// 16-bit parameters once.  Speculative: the skip decision is global, so the
+// *_out state is only committed by the caller when result->applied; the
+// parameters are restored by k_recover on overflow.
+template <int GDT, int PDT, int VEC, int NS>
+__global__ void __launch_bounds__(TILE_THREADS)
+k_step_fused(const __grid_constant__ StepArgs a) {
+    constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
+    double acc = 0.0;
+    int ovf = 0;
+    uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+    const float k = a.k;
+    for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+        const int si = find_shard(a, tile);
+        const ShardDev& d = a.shards[si];
+        const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
+        if (j >= d.numel) continue;
+        if (VEC == 8 && j + 8 <= d.numel) {
+            const float4 t0 = ld_stream4(d.mi + j), t1 = ld_stream4(d.mi + j + 4);
+            const float4 m0 = ld_stream4(d.mmi + j), m1 = ld_stream4(d.mmi + j + 4);
+            const float4 v0 = ld_stream4(d.vi + j), v1 = ld_stream4(d.vi + j + 4);
+            float s[8];
+            reduce8<GDT, NS>(a, d.grad_off + j, s);
+            float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t hp[8];
+            float sq = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t h = average16<GDT>(s[e], a.divisor);
+                ovf |= Half16<GDT>::nonfinite(h);
+                const float af = Half16<GDT>::widen(h);
+                sq = __fadd_rn(sq, __fmul_rn(af, af));
+                adamw1(th[e], mm[e], vv[e], af, k, a.sc);
+                hp[e] = Half16<PDT>::narrow(th[e]);
+            }
+            if (isfinite(sq)) {
+                acc += (double)sq;
+            } else {                        // a square above the fp32 range (or an inf/NaN): redo in fp64
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const double x = (double)Half16<GDT>::widen(average16<GDT>(s[e], a.divisor));
+                    acc += x * x;
+                }
+            }
+            st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
+            st_stream4(d.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
+            st_stream4(d.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
+            st_stream4(d.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
+            st_stream4(d.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
+            st_stream4(d.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+            store8(P, d.param_off + j, hp);
+        } else {
+            const int64_t end = (VEC == 8) ? d.numel : j + 1;
+            for (int64_t i = j; i < end; ++i) {
+                const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
+                ovf |= Half16<GDT>::nonfinite(h);
+                const float af = Half16<GDT>::widen(h);
+                acc += (double)af * (double)af;
+                float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
+                adamw1(th, mm, vv, af, k, a.sc);
+                d.mo[i] = th;
+                d.mmo[i] = mm;
+                d.vo[i] = vv;
+                P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
+            }
+        }
+    }
+    block_reduce(acc, ovf);
+    if (!publish_partial(a, acc, ovf)) return;
+    double sum;
+    int flag;
+    combine_partials(a, sum, flag);
+    if (threadIdx.x == 0) {
+        zero_result r;
+        r.overflow = (flag | a.extra_overflow) ? 1 : 0;
+        r.applied = r.overflow ? 0 : 1;
+        r.path = 1;
+        r.reserved = 0;
+        r.sumsq = sum + a.extra_sumsq;
+        r.grad_norm = sqrt(r.sumsq) / a.loss_scale;
+        r.clip_coef = 1.0;
+        r.grad_mult = a.k;
+        r.reserved2 = 0.0f;
+        *a.result = r;
+    }
+}
+
+// ---------------------------------------------------------------- K1r: restore parameters after a skipped fused step
+template <int PDT>
+__global__ void __launch_bounds__(TILE_THREADS) k_recover(const __grid_constant__ StepArgs a) {
+    if (!__ldcg(&a.result->overflow)) return;
+    uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+    for (int si = 0; si < a.n_shards; ++si) {
+        const ShardDev& d = a.shards[si];
+        for (int64_t i = (int64_t)blockIdx.x * TILE_THREADS + threadIdx.x; i < d.numel;
+             i += (int64_t)gridDim.x * TILE_THREADS)
+            P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(d.mi[i]);
+    }
+}
+
+// ---------------------------------------------------------------- K1b / K4: reduce + statistics
+template <int GDT, int VEC, int NS>
+__global__ void __launch_bounds__(TILE_THREADS)
+k_reduce(const __grid_constant__ StepArgs a) {
+    constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
+    double acc = 0.0;
+    int ovf = 0;
+    for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+        const int si = find_shard(a, tile);
+        const ShardDev& d = a.shards[si];
+        const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
+        if (j >= d.numel) continue;
+        uint16_t* G = static_cast<uint16_t*>(d.gshard);
+        if (VEC == 8 && j + 8 <= d.numel) {
+            float s[8];
+            reduce8<GDT, NS>(a, d.grad_off + j, s);
+            uint32_t h[8];
+            float sq = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                h[e] = average16<GDT>(s[e], a.divisor);
+                ovf |= Half16<GDT>::nonfinite(h[e]);
+                const float af = Half16<GDT>::widen(h[e]);
+                sq = __fadd_rn(sq, __fmul_rn(af, af));
+            }
+            if (isfinite(sq)) {
+                acc += (double)sq;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const double x = (double)Half16<GDT>::widen(h[e]);
+                    acc += x * x;
+                }
+            }
+            store8(G, j, h);
+        } else {
+            const int64_t end = (VEC == 8) ? d.numel : j + 1;
+            for (int64_t i = j; i < end; ++i) {
+                const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
+                ovf |= Half16<GDT>::nonfinite(h);
+                const float af = Half16<GDT>::widen(h);
+                acc += (double)af * (double)af;
+                G[i] = (uint16_t)h;
+            }
+        }
+    }
+    block_reduce(acc, ovf);
+    if (!publish_partial(a, acc, ovf)) return;
+    double sum;
+    int flag;
+    combine_partials(a, sum, flag);
+    if (threadIdx.x == 0) {
+        zero_stats st = a.accumulate ? *a.stats : zero_stats{0.0, 0, 0};
+        st.sumsq += sum;
+        st.overflow |= flag;
+        *a.stats = st;
+    }
+}
+
+// ---------------------------------------------------------------- K1c: apply
+// Every block derives the same skip / clip decision from the statistics.
+template <int GDT, int PDT, int VEC>
+__global__ void __launch_bounds__(TILE_THREADS)
+k_apply(const __grid_constant__ StepArgs a) {
+    constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
+    const zero_stats st = *a.stats;
+    const int overflow = (st.overflow | a.extra_overflow) ? 1 : 0;
+    const double sumsq = st.sumsq + a.extra_sumsq;
+    double norm, clip;
+    const float k = grad_multiplier(sumsq, a.loss_scale, a.max_norm, norm, clip);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        zero_result r;
+        r.overflow = overflow;
+        r.applied = overflow ? 0 : 1;
+        r.path = 2;
+        r.reserved = 0;
+        r.sumsq = sumsq;
+        r.grad_norm = norm;
+        r.clip_coef = clip;
+        r.grad_mult = k;
+        r.reserved2 = 0.0f;
+        *a.result = r;
+    }
+    if (overflow) return;
+    uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+    for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+        const int si = find_shard(a, tile);
+        const ShardDev& d = a.shards[si];
+        const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
+        if (j >= d.numel) continue;
+        const uint16_t* G = static_cast<const uint16_t*>(d.gshard);
+        if (VEC == 8 && j + 8 <= d.numel) {
+            const float4 t0 = ld_stream4(d.mi + j), t1 = ld_stream4(d.mi + j + 4);
+            const float4 m0 = ld_stream4(d.mmi + j), m1 = ld_stream4(d.mmi + j + 4);
+            const float4 v0 = ld_stream4(d.vi + j), v1 = ld_stream4(d.vi + j + 4);
+            const uint4 w = ld_stream(G + j);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t hp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t h = (e & 1) ? (u[e >> 1] >> 16) : (u[e >> 1] & 0xFFFFu);
+                adamw1(th[e], mm[e], vv[e], Half16<GDT>::widen(h), k, a.sc);
+                hp[e] = Half16<PDT>::narrow(th[e]);
+            }
+            st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
+            st_stream4(d.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
+            st_stream4(d.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
+            st_stream4(d.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
+            st_stream4(d.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
+            st_stream4(d.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+            store8(P, d.param_off + j, hp);
+        } else {
+            const int64_t end = (VEC == 8) ? d.numel : j + 1;
+            for (int64_t i = j; i < end; ++i) {
+                float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
+                adamw1(th, mm, vv, Half16<GDT>::widen(G[i]), k, a.sc);
+                d.mo[i] = th;
+                d.mmo[i] = mm;
+                d.vo[i] = vv;
+                P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- K3: ZeRO-3 layer gather
+struct GatherArgs {
+    const void* parts[ZERO_MAX_SLICES];
+    int world_size;
+    int64_t part_numel;       // elements per part
+    int64_t tiles_per_part;
+    void* out;
+};
+
+template <int VEC>
+__global__ void __launch_bounds__(TILE_THREADS) k_gather(const __grid_constant__ GatherArgs a) {
+    constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC * 2;   // two vectors per thread per tile
+    const int64_t n_tiles = a.tiles_per_part * a.world_size;
+    uint16_t* O = static_cast<uint16_t*>(a.out);
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int r = (int)(tile / a.tiles_per_part);
+        const int64_t t = tile - (int64_t)r * a.tiles_per_part;
+        const uint16_t* src = static_cast<const uint16_t*>(a.parts[r]);
+        uint16_t* dst = O + (int64_t)r * a.part_numel;
+        const int64_t j0 = t * TILE + (int64_t)threadIdx.x * VEC;
+        const int64_t j1 = j0 + (int64_t)TILE_THREADS * VEC;
+        if (VEC == 8) {
+            const bool f0 = j0 + 8 <= a.part_numel, f1 = j1 + 8 <= a.part_numel;
+            uint4 w0, w1;
+            if (f0) w0 = ld_stream(src + j0);
+            if (f1) w1 = ld_stream(src + j1);
+            if (f0) __stcs(reinterpret_cast<uint4*>(dst + j0), w0);
+            else for (int64_t i = j0; i < a.part_numel; ++i) dst[i] = src[i];
+            if (f1) __stcs(reinterpret_cast<uint4*>(dst + j1), w1);
+            else for (int64_t i = j1; i < a.part_numel; ++i) dst[i] = src[i];
+        } else {
+            if (j0 < a.part_numel) dst[j0] = src[j0];
+            if (j1 < a.part_numel) dst[j1] = src[j1];
+        }
+    }
+}
+
+}  // namespace zdp

@@ -1,0 +1,57 @@
+// zero_twopass.cu -- instantiations and launchers of the reduce + statistics
+// pass (K1b, also the ZeRO-3 bucket reduce K4), the apply pass (K1c) and the
+// ZeRO-3 layer gather (K3).
+#include "zero_internal.h"
+
+namespace zdp {
+
+template <int G, int V>
+static const void* reduce_ptr(int ns) {
+    if (V == 1) return (const void*)k_reduce<G, 1, 0>;
+    switch (ns) {
+    case 1: return (const void*)k_reduce<G, V, 1>;
+    case 2: return (const void*)k_reduce<G, V, 2>;
+    case 3: return (const void*)k_reduce<G, V, 3>;
+    case 4: return (const void*)k_reduce<G, V, 4>;
+    case 8: return (const void*)k_reduce<G, V, 8>;
+    default: return (const void*)k_reduce<G, V, 0>;
+    }
+}
+
+const void* reduce_kernel(int gdt, int vec, int ns) {
+    if (gdt == ZERO_BF16) return vec == 8 ? reduce_ptr<ZERO_BF16, 8>(ns) : reduce_ptr<ZERO_BF16, 1>(ns);
+    return vec == 8 ? reduce_ptr<ZERO_F16, 8>(ns) : reduce_ptr<ZERO_F16, 1>(ns);
+}
+
+template <int G, int P>
+static const void* apply_ptr(int vec) {
+    return vec == 8 ? (const void*)k_apply<G, P, 8> : (const void*)k_apply<G, P, 1>;
+}
+
+const void* apply_kernel(int gdt, int pdt, int vec) {
+    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? apply_ptr<ZERO_BF16, ZERO_BF16>(vec) : apply_ptr<ZERO_BF16, ZERO_F16>(vec);
+    return pdt == ZERO_BF16 ? apply_ptr<ZERO_F16, ZERO_BF16>(vec) : apply_ptr<ZERO_F16, ZERO_F16>(vec);
+}
+
+int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s) {
+    const void* f = reduce_kernel(gdt, vec, ns_variant(a.n_slices));
+    const int grid = grid_for(f, a.n_tiles);
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "reduce launch");
+}
+
+int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s) {
+    const void* f = apply_kernel(gdt, pdt, vec);
+    const int grid = grid_for(f, a.n_tiles);
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "apply launch");
+}
+
+int launch_gather(const GatherArgs& a, int vec, cudaStream_t s) {
+    const void* f = vec == 8 ? (const void*)k_gather<8> : (const void*)k_gather<1>;
+    const int grid = grid_for(f, a.tiles_per_part * a.world_size);
+    void* args[] = {const_cast<GatherArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "gather launch");
+}
+
+}  // namespace zdp
