@@ -140,21 +140,86 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ kernel timing
+class KernelTimer:
+    """CUDA events around each library call on the launching (current) stream,
+    grouped by kernel kind."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.events = []          # (kind, start, end)
+        self.on = False
+
+    def __call__(self, kind):
+        timer = self
+
+        class _Ctx:
+            def __enter__(self):
+                if timer.on:
+                    self.a = timer.torch.cuda.Event(enable_timing=True)
+                    self.a.record()
+
+            def __exit__(self, *exc):
+                if timer.on:
+                    b = timer.torch.cuda.Event(enable_timing=True)
+                    b.record()
+                    timer.events.append((kind, self.a, b))
+        return _Ctx()
+
+    def per_kind(self, steps):
+        out = {}
+        for kind, a, b in self.events:
+            d = out.setdefault(kind, {"ms_total": 0.0, "launches": 0})
+            d["ms_total"] += a.elapsed_time(b)
+            d["launches"] += 1
+        for d in out.values():
+            d["ms_per_launch"] = d["ms_total"] / d["launches"]
+            d["ms_per_step"] = d["ms_total"] / steps
+        return out
+
+
+def _hyper(Z, h, t, clip=0.0):
+    return Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], clip, t)
+
+
+def _finish_step(Z, torch, res, res_h, st):
+    res_h.copy_(res, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    r = Z.read_result(res_h)
+    if r.applied:
+        st["cur"] ^= 1
+        st["t"] += 1
+    else:
+        st["S"] /= 2
+    return r
+
+
+def _pin_copies(torch, bufs, e2e):
+    need = sum(b.numel() * b.element_size() for b in bufs)
+    if not e2e:
+        return None
+    if mem_available_bytes() > 2 * need + (16 << 30):
+        log(f"[bench] pinning {need / 1e9:.1f} GB of host gradients for the end-to-end run")
+        return [torch.empty(b.shape, dtype=b.dtype, pin_memory=True).copy_(b) for b in bufs]
+    log("[bench] not enough host memory for the end-to-end run")
+    return None
+
+
 # ------------------------------------------------------------------ workloads (our path)
-def gpt2_all_ranks(Z, W, torch, dev, e2e):
+def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=48):
     """GPT-2 1.5B-shaped group, N_d = 8, all ranks on this GPU, bf16, ping-pong state (fused single pass)."""
     wl = W.workload("gpt2-1.5b-nd8")
+    specs = wl.specs if layers == 48 else W.gpt2_group(L=layers)
     nd = wl.nd
-    plan = Z.zero_plan(W.numels(wl.specs), nd)
+    plan = Z.zero_plan(W.numels(specs), nd)
     P = plan["padded_total"]
-    log(f"[bench] gpt2-1.5b-nd8: Psi={P} N_d={nd}; generating inputs")
-    flat = torch.zeros(P, dtype=torch.bfloat16, device=dev)
-    W.init_params_(flat, wl.specs, W.generator(wl.param_seed, dev))
-    grads = [W.fill_grad_(torch.empty(P, dtype=torch.bfloat16, device=dev), wl.specs, W.generator(1 + r, dev),
-                          W.gpt2_grad_std()) for r in range(nd)]
-    A = [flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)]
-    B = [torch.empty(P, device=dev) for _ in range(3)]
-    sets = [A, B]
+    name = "gpt2-1.5b-nd8" if layers == 48 else f"gpt2-{layers}layers-nd8"
+    log(f"[bench] {name}: Psi={P} N_d={nd}; generating inputs")
+    flat = W.flat_params(specs, P, torch.bfloat16, wl.param_seed, dev)
+    grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
+        [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(nd)], specs, W.gpt2_grad_std())
+    sets = [[flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)],
+            [torch.empty(P, device=dev) for _ in range(3)]]
 
     def shards(cur):
         i, o = sets[cur], sets[1 - cur]
@@ -167,48 +232,175 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e):
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
-    h = wl.hyper
-    pinned = None
-    if e2e:
-        need = nd * P * 2
-        if mem_available_bytes() > 2 * need + (16 << 30):
-            log(f"[bench] pinning {need / 1e9:.1f} GB of host gradients for the end-to-end run")
-            pinned = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True).copy_(g) for g in grads]
-        else:
-            log("[bench] not enough host memory for the end-to-end run")
+    pinned = _pin_copies(torch, grads, e2e)
 
-    def step(kernel_events=None, from_host=False):
+    def step(from_host=False):
         if from_host:
             for g, hp in zip(grads, pinned):
                 g.copy_(hp, non_blocking=True)
-        if kernel_events is not None:
-            kernel_events[0].record()
-        Z.zero_shard_step(grads, Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16,
-                          Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0.0, st["t"]),
-                          st["S"], 0.0, 0, ws, ws.numel(), res)
-        if kernel_events is not None:
-            kernel_events[1].record()
-        res_h.copy_(res, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        r = Z.read_result(res_h)
-        if r.applied:
-            st["cur"] ^= 1
-            st["t"] += 1
-        else:
-            st["S"] /= 2
+        with timer("k_step_fused+k_recover"):
+            Z.zero_shard_step(grads, Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]),
+                              st["S"], 0.0, 0, ws, ws.numel(), res)
+        _finish_step(Z, torch, res, res_h, st)
 
-    return dict(name="gpt2-1.5b-nd8", step=step, elements=P, nd=nd,
-                bytes_per_elem=2 * nd + 26, launches_per_step=2,
-                dominant="k_step_fused<bf16,bf16,8,8> (+ k_recover, a no-op without overflow)",
-                dominant_key="k_step_fused", dominant_bytes=(2 * nd + 26) * P,
-                h2d=nd * P * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
-                config={"workload": "gpt2-1.5b-nd8: GPT-2 1.5B-shaped group (48 layers, d=1600, vocab 50257, "
-                                    "ctx 1024), N_d=8, all 8 ranks simulated on one GPU",
-                        "psi": P, "n_d": nd, "shard_elements": plan["rank_numels"][0],
-                        "grad_dtype": "bf16", "param_dtype": "bf16", "state": "f32 master/m/v, ping-pong",
-                        "path": "fused single pass", "bytes_per_step": (2 * nd + 26) * P,
-                        "l2": f"inputs larger than L2 ({(2 * nd + 26) * P / 1e9:.1f} GB per step), no flush"},
-                sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
+    bytes_step = (2 * nd + 26) * P
+    return dict(name=name, step=step, elements=P, nd=nd, launches_per_step=2,
+                kernel_bytes={"k_step_fused+k_recover": bytes_step},
+                dominant_label="k_step_fused<bf16,bf16,VEC 8,8 slices> (+ k_recover, which returns at once "
+                               "without an overflow)",
+                h2d=sum(g.numel() * 2 for g in grads) if pinned else None, d2h=48, e2e_ok=pinned is not None,
+                config={"workload": f"{name}: GPT-2-shaped group ({layers} layers, d=1600, vocab 50257, ctx 1024), "
+                                    "N_d=8, all 8 ranks simulated on one GPU",
+                        "psi": P, "n_d": nd, "shard_elements": plan["rank_numels"][0], "grad_dtype": "bf16",
+                        "param_dtype": "bf16", "state": "f32 master/m/v, ping-pong", "path": "fused single pass",
+                        "bytes_per_step": bytes_step,
+                        "l2": f"inputs larger than L2 ({bytes_step / 1e9:.1f} GB per step), no flush"},
+                formula_bytes=bytes_step, sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
+
+
+def llama_rank_local(Z, W, torch, dev, e2e, timer):
+    """Llama-3-8B-shaped group, N_d = 4, rank 1's shard with 4 staged slices,
+    clip 1.0: two passes (reduce + statistics, then apply), state in place."""
+    wl = W.workload("llama3-8b-nd4-r1")
+    nd, me = wl.nd, 1
+    plan = Z.zero_plan(W.numels(wl.specs), nd)
+    P = plan["padded_total"]
+    o, n = plan["rank_offsets"][me], plan["rank_numels"][me]
+    log(f"[bench] llama3-8b-nd4-r1: Psi={P}, shard {n} at {o}; generating inputs")
+    flat = W.flat_params(wl.specs, P, torch.bfloat16, wl.param_seed, dev)
+    slices = W.GradStream([2 + j for j in range(nd)], dev).draw_plain(
+        [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(nd)], wl.grad_std)
+    master, m, v = flat[o:o + n].float(), torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    gshard = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    sh = [Z.shard(n, 0, o, master, m, v, grad_shard=gshard)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(16, dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+    extra = W.other_ranks_sumsq(wl, n)
+    pinned = _pin_copies(torch, slices, e2e)
+
+    def step(from_host=False):
+        if from_host:
+            for g, hp in zip(slices, pinned):
+                g.copy_(hp, non_blocking=True)
+        with timer("k_reduce"):
+            Z.zero_shard_reduce(slices, Z.ZERO_BF16, sh, 0, stats, ws, ws.numel())
+        with timer("k_apply"):
+            Z.zero_shard_apply(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"], wl.max_grad_norm),
+                               st["S"], stats, extra, 0, res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    return dict(name="llama3-8b-nd4-r1", step=step, elements=n, nd=nd, launches_per_step=2,
+                kernel_bytes={"k_reduce": (2 * nd + 2) * n, "k_apply": 28 * n},
+                dominant_label=None, h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
+                formula_bytes=(2 * nd + 26) * n,
+                config={"workload": "llama3-8b-nd4-r1: Llama-3-8B-shaped group, N_d=4, rank 1's shard, 4 staged "
+                                    "bf16 slices, global-norm clip 1.0", "psi": P, "n_d": nd, "shard_elements": n,
+                        "path": "two passes (reduce+stats, apply), state in place",
+                        "bytes_per_step_actual": (2 * nd + 30) * n, "bytes_per_step_formula": (2 * nd + 26) * n,
+                        "l2": "inputs larger than L2, no flush"},
+                sample_for_cpu=None)
+
+
+def gpt75_rank63(Z, W, torch, dev, e2e, timer):
+    """The 7.5B GPT-like group, N_d = 64, rank 63's shard, fp16, S = 65536: fused single pass."""
+    wl = W.workload("gpt-7.5b-nd64-r63")
+    nd, me = wl.nd, 63
+    plan = Z.zero_plan(W.numels(wl.specs), nd)
+    P = plan["padded_total"]
+    o, n = plan["rank_offsets"][me], plan["rank_numels"][me]
+    log(f"[bench] gpt-7.5b-nd64-r63: Psi={P}, shard {n} at {o}; generating inputs")
+    flat = W.flat_params(wl.specs, P, torch.float16, wl.param_seed, dev)
+    slices = W.GradStream([4 + j for j in range(nd)], dev).draw_plain(
+        [torch.empty(n, dtype=torch.float16, device=dev) for _ in range(nd)], wl.grad_std, wl.loss_scale)
+    W.zero_every_100th_(slices[0])
+    sets = [[flat[o:o + n].float(), torch.zeros(n, device=dev), torch.zeros(n, device=dev)],
+            [torch.empty(n, device=dev) for _ in range(3)]]
+    variants = [[Z.shard(n, 0, o, *sets[c], *sets[1 - c])] for c in (0, 1)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+    pinned = _pin_copies(torch, slices, e2e)
+
+    def step(from_host=False):
+        if from_host:
+            for g, hp in zip(slices, pinned):
+                g.copy_(hp, non_blocking=True)
+        with timer("k_step_fused+k_recover"):
+            Z.zero_shard_step(slices, Z.ZERO_F16, variants[st["cur"]], flat, Z.ZERO_F16, _hyper(Z, wl.hyper, st["t"]),
+                              st["S"], 0.0, 0, ws, ws.numel(), res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    return dict(name="gpt-7.5b-nd64-r63", step=step, elements=n, nd=nd, launches_per_step=2,
+                kernel_bytes={"k_step_fused+k_recover": (2 * nd + 26) * n}, dominant_label=None,
+                h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
+                formula_bytes=(2 * nd + 26) * n,
+                config={"workload": "gpt-7.5b-nd64-r63: GPT-like 7.5B group, N_d=64, rank 63's shard "
+                                    "(flat offset = 6 mod 8), fp16, loss scale 65536", "psi": P, "n_d": nd,
+                        "shard_elements": n, "path": "fused single pass, ping-pong state",
+                        "l2": "inputs larger than L2, no flush"},
+                sample_for_cpu=None)
+
+
+def zero3_llama(Z, W, torch, dev, e2e, timer):
+    """ZeRO-3 per-layer path, Llama-3-8B group as 34 units, N_d = 4, rank 1:
+    per step 34 forward gathers, 34 backward gathers (reverse order), 34 bucket
+    reduces onto rank 1's parts, one shard update."""
+    wl = W.workload("zero3-llama3-8b")
+    nd, me = wl.nd, 1
+    units = W.llama_units(wl.specs)
+    parts = [u // nd for u in units]
+    starts = [sum(units[:i]) for i in range(len(units))]
+    uoff = [sum(parts[:i]) for i in range(len(parts))]
+    L = sum(parts)
+    log(f"[bench] zero3-llama3-8b: {len(units)} units, rank shard {L}; generating inputs")
+    flat = W.flat_params(wl.specs, sum(units), torch.bfloat16, wl.param_seed, dev)
+    rshards = [torch.cat([flat[s + r * p: s + (r + 1) * p] for s, p in zip(starts, parts)]) for r in range(nd)]
+    del flat
+    torch.cuda.empty_cache()
+    gs = W.GradStream([5 + r for r in range(nd)], dev)
+    buckets = []          # buckets[u][r]: rank r's full gradient of unit u
+    for u in reversed(range(len(units))):
+        row = [torch.empty(units[u], dtype=torch.bfloat16, device=dev) for _ in range(nd)]
+        gs.draw_plain(row, wl.grad_std)
+        buckets.append((u, row))
+    layer = torch.empty(max(units), dtype=torch.bfloat16, device=dev)
+    master, m, v = rshards[me].float(), torch.zeros(L, device=dev), torch.zeros(L, device=dev)
+    gshard = torch.empty(L, dtype=torch.bfloat16, device=dev)
+    sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(16, dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+    part_ptrs = [[rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)] for u in range(len(units))]
+
+    def step(from_host=False):
+        for u in list(range(len(units))) + list(reversed(range(len(units)))):
+            with timer("k_gather"):
+                Z.zero3_gather_layer(part_ptrs[u], units[u], Z.ZERO_BF16, layer)
+        for k, (u, row) in enumerate(buckets):
+            with timer("k_reduce"):
+                Z.zero3_reduce_bucket(row, me, units[u], Z.ZERO_BF16, gshard[uoff[u]:uoff[u] + parts[u]], k > 0,
+                                      stats, ws, ws.numel())
+        with timer("k_apply"):
+            Z.zero_shard_apply(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"],
+                               stats, 0.0, 0, res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    total_units = sum(units)
+    return dict(name="zero3-llama3-8b", step=step, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
+                kernel_bytes={"k_gather": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False,
+                formula_bytes=2 * 4 * total_units + (2 * nd + 2) * L + 28 * L,
+                config={"workload": "zero3-llama3-8b: Llama-3-8B group as 34 ZeRO-3 units, N_d=4, rank 1",
+                        "units": len(units), "shard_elements": L, "psi": total_units,
+                        "path": "per unit: gather x2, bucket reduce; then apply",
+                        "l2": "inputs larger than L2, no flush"},
+                sample_for_cpu=None)
 
 
 def cpu_sample_gpt2(W, n_per_shard):
@@ -229,7 +421,8 @@ def cpu_sample_gpt2(W, n_per_shard):
     return nd, grads, flat.view(torch.int16).numpy().view(np.uint16).copy(), wl.hyper
 
 
-WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks}
+WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "llama3-8b-nd4-r1": llama_rank_local,
+             "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -257,6 +450,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt2-1.5b-nd8", choices=sorted(WORKLOADS))
+    ap.add_argument("--gpt2-layers", type=int, default=48,
+                    help="layers of the GPT-2-shaped group (48 = the 1.5B workload; fewer gives a small case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -279,7 +474,9 @@ def main():
         if world > 1:
             dist.barrier()
 
-    wl = WORKLOADS[args.workload](Z, W, torch, dev, e2e=not args.no_e2e)
+    timer = KernelTimer(torch)
+    kw = dict(layers=args.gpt2_layers) if args.workload == "gpt2-1.5b-nd8" else {}
+    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, **kw)
     step = wl["step"]
     sampler = ClockSampler(local)
     for _ in range(max(3, args.warmup)):
@@ -288,28 +485,28 @@ def main():
     barrier()
     sampler.start()
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    timer.on = True
     start.record()
-    for k in range(args.steps):
-        step(kernel_events=evs[k])
+    for _ in range(args.steps):
+        step()
     end.record()
     torch.cuda.synchronize()
+    timer.on = False
     barrier()
     clocks = sampler.stop()
     ms = start.elapsed_time(end) / args.steps
-    k_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    kinds = timer.per_kind(args.steps)
     if world > 1:
-        t = torch.tensor([ms, k_ms], device=dev)
+        t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, k_ms = t.tolist()
+        ms = t.item()
 
     e2e = None
     if wl["e2e_ok"]:
-        for _ in range(1):
-            step(from_host=True)
+        step(from_host=True)
         torch.cuda.synchronize()
         barrier()
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -329,13 +526,21 @@ def main():
                "steps": args.e2e_steps}
 
     peak, peak_src = measured_peaks()
-    achieved = wl["dominant_bytes"] / (k_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": ncu_traffic(wl["name"], wl["dominant_key"]), "peak_source": peak_src,
-                "kernel": wl["dominant"], "kernel_ms": k_ms,
-                "algorithmic_bytes_per_launch": wl["dominant_bytes"]}
+    per_kernel = {}
+    for kind, d in kinds.items():
+        per_launch_bytes = wl["kernel_bytes"][kind] / (d["launches"] / args.steps)
+        gbs = per_launch_bytes / (d["ms_per_launch"] / 1e3) / 1e9
+        per_kernel[kind] = dict(d, algorithmic_bytes_per_launch=per_launch_bytes, achieved_gbs=gbs,
+                                frac=gbs / peak)
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
+    dk = per_kernel[dom]
+    roofline = {"bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                "frac": dk["achieved_gbs"] / peak, "traffic": ncu_traffic(wl["name"], dom),
+                "peak_source": peak_src, "kernel": wl["dominant_label"] or dom,
+                "kernel_ms_per_launch": dk["ms_per_launch"],
+                "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"]}
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl["sample_for_cpu"]:
         n, times = time_oracle(W, wl["sample_for_cpu"], 1 << 22, 2)
         cpu = {"value": n / statistics.mean(times), "unit": "elements/s", "cores": 1, "kind": "oracle",
                "sample": f"the first {1 << 22} elements of each of the {wl['nd']} shards "
@@ -345,8 +550,10 @@ def main():
                 "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded torch generators; no data set or weights)",
-                "config": wl["config"], "achieved_gbs_formula": wl["elements"] * wl["bytes_per_elem"] / (ms / 1e3) / 1e9,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "config": wl["config"],
+                "achieved_gbs_formula": wl["elements"] * (2 * wl["nd"] + 26) / (ms / 1e3) / 1e9
+                if wl["name"] != "zero3-llama3-8b" else wl["formula_bytes"] / (ms / 1e3) / 1e9,
+                "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": wl["launches_per_step"] * args.steps, "impl": "ours"}
         print(json.dumps(line), flush=True)
     if world > 1:

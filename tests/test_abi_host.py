@@ -17,8 +17,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def Z():
-    from zero_dp_partitioned_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import zero_dp_partitioned_gb300 as Z
     return Z
 

@@ -1,0 +1,307 @@
+"""GPU parity at the full workload sizes, through the same C-ABI calls and
+launch configuration the benchmark times.
+
+The oracle cannot redo billions of elements one by one in a test, so:
+  * the global statistics (sum of squares, overflow) are computed by the
+    oracle over every element, chunk by chunk (the oracle stays
+    single-threaded; chunks run in a thread pool);
+  * the per-element outputs (reduced gradient, master/m/v, 16-bit parameter)
+    are checked on a sample of indices -- shard starts and ends, tile
+    boundaries, the ragged tail, and random positions -- the oracle carrying
+    its own copy of the sampled state through the three steps;
+  * properties that hold at any size are checked on all elements: the slots of
+    the flat buffer that belong to other ranks are untouched, a gathered layer
+    is the concatenation of its parts.
+Tolerances are those of the small-size tests: bit-exact without clipping;
+with clipping rel 2e-6 (fp32 state) and 1 ulp (16-bit parameters); the norm
+within rel 1e-5; the plan and the overflow flag bit-exact."""
+import concurrent.futures as cf
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads as W
+from helpers import hyper32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TDT = {1: torch.float16, 2: torch.bfloat16}
+TILE = 2048
+
+
+@pytest.fixture(scope="module")
+def Z():
+    import zero_dp_partitioned_gb300 as Z
+    return Z
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def u16(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def sample_idx(numel, seed, n_random=40000):
+    rng = np.random.default_rng(seed)
+    ks = [k * TILE + d for k in (1, 2, 1000, numel // TILE - 1) for d in (-1, 0, 1, 7, 8)]
+    idx = np.concatenate([np.arange(min(16, numel)), np.arange(max(0, numel - 16), numel), ks,
+                          rng.integers(0, numel, n_random)])
+    return np.unique(idx[(idx >= 0) & (idx < numel)]).astype(np.int64)
+
+
+def oracle_stats(slices, gdt, grad_off, numel):
+    """Exact sum of squares and overflow flag of the averaged gradient over
+    [grad_off, grad_off + numel) of every slice, by the oracle."""
+    chunk = max(1 << 20, (1 << 27) // len(slices))
+
+    def work(c0):
+        n = min(chunk, numel - c0)
+        host = [u16(s[grad_off + c0: grad_off + c0 + n]) for s in slices]
+        acc = orc.ExactAccumulator()
+        return acc, orc.reduce_stats(host, gdt, 0, n, acc)
+
+    with cf.ThreadPoolExecutor(min(16, os.cpu_count() or 4)) as ex:
+        parts = list(ex.map(work, range(0, numel, chunk)))
+    total = orc.ExactAccumulator()
+    ovf = 0
+    for a, o in parts:
+        total.merge(a)
+        ovf |= o
+    return total, ovf
+
+
+class Sampled:
+    """The oracle's copy of one shard's state at sampled indices."""
+
+    def __init__(self, idx, params16, dt):
+        self.idx = idx
+        self.master = orc.widen_16(params16, dt)
+        self.m = np.zeros(idx.size, np.float32)
+        self.v = np.zeros(idx.size, np.float32)
+        self.param = params16.copy()
+
+    def step(self, slices_at_idx, dt, k, sc):
+        a = orc.reduce(slices_at_idx, dt, 0, self.idx.size)
+        orc.apply(a, dt, self.master, self.m, self.v, self.param, dt, k, sc)
+        return a
+
+
+def check_state(samp, master, m, v, param16, exact):
+    idx = torch.from_numpy(samp.idx).to(DEV)
+    got = [x[idx].cpu().numpy() for x in (master, m, v)]
+    gp = u16(param16[idx])
+    if exact:
+        for g, r in zip(got, (samp.master, samp.m, samp.v)):
+            assert np.array_equal(g.view(np.uint32), r.view(np.uint32))
+        assert np.array_equal(gp, samp.param)
+    else:
+        for g, r in zip(got, (samp.master, samp.m, samp.v)):
+            assert np.all(np.abs(g - r) <= 2e-6 * np.maximum(np.abs(r), 1e-30))
+        assert np.abs(gp.astype(np.int32) - samp.param.astype(np.int32)).max() <= 1
+
+
+def scalars(h, t):
+    return orc.make_scalars(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t)
+
+
+def test_gpt2_1p5b_all_ranks(Z):
+    """GPT-2 1.5B-shaped group, N_d = 8, all ranks, bf16, fused single pass, 3 steps."""
+    wl = W.workload("gpt2-1.5b-nd8")
+    nd, dt = 8, 2
+    numels = W.numels(wl.specs)
+    plan = Z.zero_plan(numels, nd)
+    op = orc.plan(numels, nd, 0)
+    assert plan["rank_offsets"] == list(op["rank_offsets"]) and plan["padded_total"] == op["padded_total"]
+    P = plan["padded_total"]
+    flat = W.flat_params(wl.specs, P, torch.bfloat16, wl.param_seed, DEV)
+    grads = [torch.empty(P, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([1 + r for r in range(nd)], DEV)
+    sets = [[flat.float(), torch.zeros(P, device=DEV), torch.zeros(P, device=DEV)],
+            [torch.empty(P, device=DEV) for _ in range(3)]]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    samp = []
+    for r in range(nd):
+        o, n = plan["rank_offsets"][r], plan["rank_numels"][r]
+        idx = o + sample_idx(n, r, 8000)
+        samp.append(Sampled(idx, u16(flat[torch.from_numpy(idx).to(DEV)]), dt))
+    h = hyper32()
+    cur = 0
+    for t in (1, 2, 3):
+        gs.draw_flat(grads, wl.specs, W.gpt2_grad_std())
+        A, B = sets[cur], sets[1 - cur]
+        sh = [Z.shard(n, o, o, A[0][o:o + n], A[1][o:o + n], A[2][o:o + n], B[0][o:o + n], B[1][o:o + n],
+                      B[2][o:o + n]) for o, n in zip(plan["rank_offsets"], plan["rank_numels"])]
+        Z.zero_shard_step(grads, dt, sh, flat, dt, Z.hyper(step=t, **{k: h[k] for k in
+                          ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, 0.0, 0, ws,
+                          ws.numel(), res)
+        acc, ovf = oracle_stats(grads, dt, 0, P)
+        r_gpu = Z.read_result(res)
+        k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path == 1
+        assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
+        cur ^= 1
+        for s in samp:
+            ti = torch.from_numpy(s.idx).to(DEV)
+            s.step([u16(g[ti]) for g in grads], dt, k, scalars(h, t))
+            check_state(s, *sets[cur], flat, exact=True)
+
+
+def test_llama3_8b_rank1_clipped(Z):
+    """Llama-3-8B-shaped group, N_d = 4, rank 1's shard (2.0B elements) with 4
+    staged slices, global-norm clip 1.0, in-place two-pass path, 3 steps."""
+    wl = W.workload("llama3-8b-nd4-r1")
+    nd, dt, me = 4, 2, 1
+    numels = W.numels(wl.specs)
+    plan = Z.zero_plan(numels, nd)
+    P = plan["padded_total"]
+    o, n = plan["rank_offsets"][me], plan["rank_numels"][me]
+    assert (o, n) == (2_007_565_312, 2_007_565_312)
+    flat = W.flat_params(wl.specs, P, torch.bfloat16, wl.param_seed, DEV)
+    before = flat.clone()
+    slices = [torch.empty(n, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([2 + j for j in range(nd)], DEV)
+    master = flat[o:o + n].float()
+    m = torch.zeros(n, device=DEV)
+    v = torch.zeros(n, device=DEV)
+    gshard = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    extra = W.other_ranks_sumsq(wl, n)
+    idx = sample_idx(n, 3)
+    ti = torch.from_numpy(idx).to(DEV)
+    samp = Sampled(idx, u16(flat[o + ti]), dt)
+    h = hyper32(max_grad_norm=wl.max_grad_norm)
+    for t in (1, 2, 3):
+        gs.draw_plain(slices, wl.grad_std)
+        sh = [Z.shard(n, 0, o, master, m, v, grad_shard=gshard)]
+        Z.zero_shard_step(slices, dt, sh, flat, dt, Z.hyper(step=t, **{k: h[k] for k in
+                          ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, extra, 0, ws,
+                          ws.numel(), res)
+        acc, ovf = oracle_stats(slices, dt, 0, n)
+        total = acc.value() + extra
+        k, norm, clip = orc.grad_multiplier(total, 1.0, wl.max_grad_norm)
+        r_gpu = Z.read_result(res)
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path == 2
+        assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5) and clip < 1.0
+        assert r_gpu.clip_coef == pytest.approx(clip, rel=1e-5)
+        a = samp.step([u16(s[ti]) for s in slices], dt, k, scalars(h, t))
+        assert np.array_equal(u16(gshard[ti]), a)                       # reduced gradient: bit-exact
+        shard_view = flat[o:o + n]
+        check_state(samp, master, m, v, shard_view, exact=False)
+    for lo, hi in ((0, o), (o + n, P)):                                  # other ranks' slots untouched
+        for c in range(lo, hi, 1 << 30):
+            e = min(hi, c + (1 << 30))
+            assert torch.equal(flat[c:e], before[c:e])
+
+
+def test_gpt_7p5b_rank63_nd64(Z):
+    """The 7.5B GPT-like group, N_d = 64, rank 63's shard (119,259,162
+    elements, flat offset = 6 mod 8), fp16, loss scale 65536, exact zeros in
+    slice 0 at every 100th element, fused single pass, 3 steps."""
+    wl = W.workload("gpt-7.5b-nd64-r63")
+    nd, dt, me = 64, 1, 63
+    plan = Z.zero_plan(W.numels(wl.specs), nd)
+    P = plan["padded_total"]
+    o, n = plan["rank_offsets"][me], plan["rank_numels"][me]
+    assert n == 119_259_162 and o % 8 == 6
+    flat = W.flat_params(wl.specs, P, torch.float16, wl.param_seed, DEV)
+    head = flat[:o].clone()
+    slices = [torch.empty(n, dtype=torch.float16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([4 + j for j in range(nd)], DEV)
+    sets = [[flat[o:o + n].float(), torch.zeros(n, device=DEV), torch.zeros(n, device=DEV)],
+            [torch.empty(n, device=DEV) for _ in range(3)]]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    idx = sample_idx(n, 4)
+    ti = torch.from_numpy(idx).to(DEV)
+    samp = Sampled(idx, u16(flat[o + ti]), dt)
+    h = hyper32()
+    cur, S = 0, wl.loss_scale
+    for t in (1, 2, 3):
+        gs.draw_plain(slices, wl.grad_std, S)
+        W.zero_every_100th_(slices[0])
+        A, B = sets[cur], sets[1 - cur]
+        sh = [Z.shard(n, 0, o, *A, *B)]
+        Z.zero_shard_step(slices, dt, sh, flat, dt, Z.hyper(step=t, **{k: h[k] for k in
+                          ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), S, 0.0, 0, ws,
+                          ws.numel(), res)
+        acc, ovf = oracle_stats(slices, dt, 0, n)
+        k, norm, _ = orc.grad_multiplier(acc.value(), S, 0.0)
+        r_gpu = Z.read_result(res)
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1
+        assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
+        cur ^= 1
+        samp.step([u16(s[ti]) for s in slices], dt, k, scalars(h, t))
+        check_state(samp, *sets[cur], flat[o:o + n], exact=True)
+    assert torch.equal(flat[:o], head)
+
+
+def test_zero3_llama3_8b_rank1(Z):
+    """ZeRO-3 per-layer path on the Llama-3-8B group, N_d = 4, rank 1: for each
+    of the 34 units a forward gather, a backward gather (reverse order) and the
+    bucket reduce onto rank 1's part; then the shard update; 3 steps."""
+    wl = W.workload("zero3-llama3-8b")
+    nd, dt, me = 4, 2, 1
+    units = W.llama_units(wl.specs)
+    parts = [u // nd for u in units]
+    uoff = np.concatenate([[0], np.cumsum(parts)[:-1]]).astype(np.int64)
+    L = int(sum(parts))
+    flat = W.flat_params(wl.specs, sum(units), torch.bfloat16, wl.param_seed, DEV)
+    # rank r's persistent parameter shard: its part of every unit
+    starts = np.concatenate([[0], np.cumsum(units)[:-1]])
+    rshards = [torch.cat([flat[s + r * p: s + (r + 1) * p] for s, p in zip(starts, parts)]) for r in range(nd)]
+    del flat
+    torch.cuda.empty_cache()
+    layer = torch.empty(max(units), dtype=torch.bfloat16, device=DEV)
+    buckets = [torch.empty(max(units), dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([5 + r for r in range(nd)], DEV)
+    master = rshards[me].float()
+    m = torch.zeros(L, device=DEV)
+    v = torch.zeros(L, device=DEV)
+    gshard = torch.empty(L, dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    idx = sample_idx(L, 5)
+    ti = torch.from_numpy(idx).to(DEV)
+    samp = Sampled(idx, u16(rshards[me][ti]), dt)
+    h = hyper32()
+    for t in (1, 2, 3):
+        for u in list(range(len(units))) + list(reversed(range(len(units)))):
+            ptrs = [rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)]
+            Z.zero3_gather_layer(ptrs, units[u], dt, layer)
+            if u in (0, 1, len(units) - 1):
+                assert torch.equal(layer[:units[u]], torch.cat(ptrs))     # gather = inverse of the partition
+        acc = orc.ExactAccumulator()
+        a_samp = np.empty(idx.size, np.uint16)
+        for k_u, u in enumerate(reversed(range(len(units)))):
+            bu = [b[:units[u]] for b in buckets]
+            gs.draw_plain(bu, wl.grad_std)
+            Z.zero3_reduce_bucket(bu, me, units[u], dt, gshard[uoff[u]:uoff[u] + parts[u]], k_u > 0, stats, ws,
+                                  ws.numel())
+            a_u, o_u = oracle_stats(bu, dt, me * parts[u], parts[u])
+            acc.merge(a_u)
+            assert o_u == 0
+            sel = (idx >= uoff[u]) & (idx < uoff[u] + parts[u])
+            if sel.any():
+                loc = torch.from_numpy(idx[sel] - uoff[u] + me * parts[u]).to(DEV)
+                a_samp[sel] = orc.reduce([u16(b[loc]) for b in bu], dt, 0, int(sel.sum()))
+        sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
+        Z.zero_shard_apply(sh, dt, rshards[me], dt, Z.hyper(step=t, **{k: h[k] for k in
+                           ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, stats, 0.0, 0,
+                           res)
+        k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+        r_gpu = Z.read_result(res)
+        assert r_gpu.applied == 1 and r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
+        assert np.array_equal(u16(gshard[ti]), a_samp)
+        orc.apply(a_samp, dt, samp.master, samp.m, samp.v, samp.param, dt, k, scalars(h, t))
+        check_state(samp, master, m, v, rshards[me], exact=True)
