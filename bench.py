@@ -206,9 +206,10 @@ def _pin_copies(torch, bufs, e2e):
 
 
 # ------------------------------------------------------------------ workloads (our path)
-def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=48):
+def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
     """GPT-2 1.5B-shaped group, N_d = 8, all ranks on this GPU, bf16, ping-pong state (fused single pass)."""
     wl = W.workload("gpt2-1.5b-nd8")
+    layers = layers or 48
     specs = wl.specs if layers == 48 else W.gpt2_group(L=layers)
     nd = wl.nd
     plan = Z.zero_plan(W.numels(specs), nd)
@@ -258,10 +259,13 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=48):
                 formula_bytes=bytes_step, sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
 
 
-def llama_rank_local(Z, W, torch, dev, e2e, timer):
+def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
     """Llama-3-8B-shaped group, N_d = 4, rank 1's shard with 4 staged slices,
     clip 1.0: two passes (reduce + statistics, then apply), state in place."""
     wl = W.workload("llama3-8b-nd4-r1")
+    if layers:
+        wl.specs = W.llama_group(L=layers)
+        wl.name = f"llama3-{layers}layers-nd4-r1"
     nd, me = wl.nd, 1
     plan = Z.zero_plan(W.numels(wl.specs), nd)
     P = plan["padded_total"]
@@ -292,11 +296,11 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer):
                                st["S"], stats, extra, 0, res)
         _finish_step(Z, torch, res, res_h, st)
 
-    return dict(name="llama3-8b-nd4-r1", step=step, elements=n, nd=nd, launches_per_step=2,
+    return dict(name=wl.name, step=step, elements=n, nd=nd, launches_per_step=2,
                 kernel_bytes={"k_reduce": (2 * nd + 2) * n, "k_apply": 28 * n},
                 dominant_label=None, h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 formula_bytes=(2 * nd + 26) * n,
-                config={"workload": "llama3-8b-nd4-r1: Llama-3-8B-shaped group, N_d=4, rank 1's shard, 4 staged "
+                config={"workload": f"{wl.name}: Llama-3-8B-shaped group, N_d=4, rank 1's shard, 4 staged "
                                     "bf16 slices, global-norm clip 1.0", "psi": P, "n_d": nd, "shard_elements": n,
                         "path": "two passes (reduce+stats, apply), state in place",
                         "bytes_per_step_actual": (2 * nd + 30) * n, "bytes_per_step_formula": (2 * nd + 26) * n,
@@ -304,9 +308,12 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer):
                 sample_for_cpu=None)
 
 
-def gpt75_rank63(Z, W, torch, dev, e2e, timer):
+def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None):
     """The 7.5B GPT-like group, N_d = 64, rank 63's shard, fp16, S = 65536: fused single pass."""
     wl = W.workload("gpt-7.5b-nd64-r63")
+    if layers:
+        wl.specs = W.gpt2_group(layers, 3456, 50257, 1024)
+        wl.name = f"gpt-{layers}layers-nd64-r63"
     nd, me = wl.nd, 63
     plan = Z.zero_plan(W.numels(wl.specs), nd)
     P = plan["padded_total"]
@@ -334,24 +341,27 @@ def gpt75_rank63(Z, W, torch, dev, e2e, timer):
                               st["S"], 0.0, 0, ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
 
-    return dict(name="gpt-7.5b-nd64-r63", step=step, elements=n, nd=nd, launches_per_step=2,
+    return dict(name=wl.name, step=step, elements=n, nd=nd, launches_per_step=2,
                 kernel_bytes={"k_step_fused+k_recover": (2 * nd + 26) * n}, dominant_label=None,
                 h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 formula_bytes=(2 * nd + 26) * n,
-                config={"workload": "gpt-7.5b-nd64-r63: GPT-like 7.5B group, N_d=64, rank 63's shard "
+                config={"workload": f"{wl.name}: GPT-like 7.5B-shaped group, N_d=64, rank 63's shard "
                                     "(flat offset = 6 mod 8), fp16, loss scale 65536", "psi": P, "n_d": nd,
                         "shard_elements": n, "path": "fused single pass, ping-pong state",
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
 
 
-def zero3_llama(Z, W, torch, dev, e2e, timer):
+def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
     """ZeRO-3 per-layer path, Llama-3-8B group as 34 units, N_d = 4, rank 1:
     per step 34 forward gathers, 34 backward gathers (reverse order), 34 bucket
     reduces onto rank 1's parts, one shard update."""
     wl = W.workload("zero3-llama3-8b")
+    if layers:
+        wl.specs = W.llama_group(L=layers)
+        wl.name = f"zero3-llama3-{layers}layers"
     nd, me = wl.nd, 1
-    units = W.llama_units(wl.specs)
+    units = W.llama_units(wl.specs, L=layers or 32)
     parts = [u // nd for u in units]
     starts = [sum(units[:i]) for i in range(len(units))]
     uoff = [sum(parts[:i]) for i in range(len(parts))]
@@ -392,7 +402,7 @@ def zero3_llama(Z, W, torch, dev, e2e, timer):
         _finish_step(Z, torch, res, res_h, st)
 
     total_units = sum(units)
-    return dict(name="zero3-llama3-8b", step=step, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
+    return dict(name=wl.name, step=step, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
                 kernel_bytes={"k_gather": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
                 dominant_label=None, h2d=None, d2h=48, e2e_ok=False,
                 formula_bytes=2 * 4 * total_units + (2 * nd + 2) * L + 28 * L,
@@ -450,8 +460,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt2-1.5b-nd8", choices=sorted(WORKLOADS))
-    ap.add_argument("--gpt2-layers", type=int, default=48,
-                    help="layers of the GPT-2-shaped group (48 = the 1.5B workload; fewer gives a small case)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer count of the workload's group (default: the full model); fewer gives a small case "
+                         "of the same kernels, e.g. for profiler captures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -475,8 +486,7 @@ def main():
             dist.barrier()
 
     timer = KernelTimer(torch)
-    kw = dict(layers=args.gpt2_layers) if args.workload == "gpt2-1.5b-nd8" else {}
-    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, **kw)
+    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, layers=args.layers)
     step = wl["step"]
     sampler = ClockSampler(local)
     for _ in range(max(3, args.warmup)):
@@ -552,7 +562,7 @@ def main():
                 "data": "synthetic (seeded torch generators; no data set or weights)",
                 "config": wl["config"],
                 "achieved_gbs_formula": wl["elements"] * (2 * wl["nd"] + 26) / (ms / 1e3) / 1e9
-                if wl["name"] != "zero3-llama3-8b" else wl["formula_bytes"] / (ms / 1e3) / 1e9,
+                if not wl["name"].startswith("zero3") else wl["formula_bytes"] / (ms / 1e3) / 1e9,
                 "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": wl["launches_per_step"] * args.steps, "impl": "ours"}
         print(json.dumps(line), flush=True)

@@ -94,18 +94,28 @@ class Sampled:
         return a
 
 
-def check_state(samp, master, m, v, param16, exact):
+def check_state(samp, master, m, v, param16, exact, prev=None, g=None):
+    """Bit-exact, or (clipped steps, where the multiplier k comes from an fp64
+    norm whose last bits differ between the two sides) rel 2e-6 measured
+    against the operands each update combines: theta_new = theta wdf - update
+    and m_new = b1 m + (1-b1) g are differences whose result can be far
+    smaller than their terms, where a relative bound on the result alone is
+    not meaningful; v sums non-negative terms and is compared to itself."""
     idx = torch.from_numpy(samp.idx).to(DEV)
     got = [x[idx].cpu().numpy() for x in (master, m, v)]
     gp = u16(param16[idx])
     if exact:
-        for g, r in zip(got, (samp.master, samp.m, samp.v)):
-            assert np.array_equal(g.view(np.uint32), r.view(np.uint32))
+        for gg, r in zip(got, (samp.master, samp.m, samp.v)):
+            assert np.array_equal(gg.view(np.uint32), r.view(np.uint32))
         assert np.array_equal(gp, samp.param)
-    else:
-        for g, r in zip(got, (samp.master, samp.m, samp.v)):
-            assert np.all(np.abs(g - r) <= 2e-6 * np.maximum(np.abs(r), 1e-30))
-        assert np.abs(gp.astype(np.int32) - samp.param.astype(np.int32)).max() <= 1
+        return
+    th_prev, m_prev = (np.abs(x.astype(np.float64)) for x in prev)
+    upd = np.abs(th_prev - samp.master.astype(np.float64))
+    scale_th = np.maximum(th_prev + upd, np.abs(samp.master))
+    scale_m = np.maximum(0.9 * m_prev + 0.1 * np.abs(g), np.abs(samp.m))
+    for gg, r, sc in ((got[0], samp.master, scale_th), (got[1], samp.m, scale_m), (got[2], samp.v, np.abs(samp.v))):
+        assert np.all(np.abs(gg.astype(np.float64) - r) <= 2e-6 * np.maximum(sc, 1e-30))
+    assert np.abs(gp.astype(np.int32) - samp.param.astype(np.int32)).max() <= 1
 
 
 def scalars(h, t):
@@ -193,10 +203,16 @@ def test_llama3_8b_rank1_clipped(Z):
         assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path == 2
         assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5) and clip < 1.0
         assert r_gpu.clip_coef == pytest.approx(clip, rel=1e-5)
+        prev = (samp.master.copy(), samp.m.copy())
         a = samp.step([u16(s[ti]) for s in slices], dt, k, scalars(h, t))
         assert np.array_equal(u16(gshard[ti]), a)                       # reduced gradient: bit-exact
-        shard_view = flat[o:o + n]
-        check_state(samp, master, m, v, shard_view, exact=False)
+        kg = np.float32(r_gpu.grad_mult)
+        print(f"step {t}: k gpu {kg!r} oracle {np.float32(k)!r} ulps {int(abs(int(kg.view(np.int32)) - int(np.float32(k).view(np.int32))))} "
+              f"sumsq rel diff {(r_gpu.sumsq - total) / total:.3e}")
+        got = master[ti].cpu().numpy()
+        d = got.view(np.int32).astype(np.int64) - samp.master.view(np.int32).astype(np.int64)
+        print(f"  master: {int((d != 0).sum())} of {d.size} sampled elements differ, max {int(np.abs(d).max())} ulps")
+        check_state(samp, master, m, v, flat[o:o + n], exact=False, prev=prev, g=orc.widen_16(a, dt) * k)
     for lo, hi in ((0, o), (o + n, P)):                                  # other ranks' slots untouched
         for c in range(lo, hi, 1 << 30):
             e = min(hi, c + (1 << 30))
