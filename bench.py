@@ -182,10 +182,15 @@ def _hyper(Z, h, t, clip=0.0):
     return Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], clip, t)
 
 
+PATH_NAMES = {1: "k_step_fused (register-staged)", 2: "k_apply (register-staged)",
+              3: "k_stream<fused> (TMA bulk-copy staged)", 4: "k_stream<apply> (TMA bulk-copy staged)"}
+
+
 def _finish_step(Z, torch, res, res_h, st):
     res_h.copy_(res, non_blocking=True)
     torch.cuda.current_stream().synchronize()
     r = Z.read_result(res_h)
+    st["path"] = r.path
     if r.applied:
         st["cur"] ^= 1
         st["t"] += 1
@@ -239,16 +244,15 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
         if from_host:
             for g, hp in zip(grads, pinned):
                 g.copy_(hp, non_blocking=True)
-        with timer("k_step_fused+k_recover"):
+        with timer("fused pass+k_recover"):
             Z.zero_shard_step(grads, Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]),
                               st["S"], 0.0, 0, ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
 
     bytes_step = (2 * nd + 26) * P
-    return dict(name=name, step=step, elements=P, nd=nd, launches_per_step=2,
-                kernel_bytes={"k_step_fused+k_recover": bytes_step},
-                dominant_label="k_step_fused<bf16,bf16,VEC 8,8 slices> (+ k_recover, which returns at once "
-                               "without an overflow)",
+    return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=2,
+                kernel_bytes={"fused pass+k_recover": bytes_step},
+                dominant_label=None,
                 h2d=sum(g.numel() * 2 for g in grads) if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 config={"workload": f"{name}: GPT-2-shaped group ({layers} layers, d=1600, vocab 50257, ctx 1024), "
                                     "N_d=8, all 8 ranks simulated on one GPU",
@@ -293,10 +297,10 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
             Z.zero_shard_reduce(slices, Z.ZERO_BF16, sh, 0, stats, ws, ws.numel())
         with timer("k_apply"):
             Z.zero_shard_apply(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"], wl.max_grad_norm),
-                               st["S"], stats, extra, 0, res)
+                               st["S"], stats, extra, 0, ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
 
-    return dict(name=wl.name, step=step, elements=n, nd=nd, launches_per_step=2,
+    return dict(name=wl.name, step=step, state=st, elements=n, nd=nd, launches_per_step=2,
                 kernel_bytes={"k_reduce": (2 * nd + 2) * n, "k_apply": 28 * n},
                 dominant_label=None, h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 formula_bytes=(2 * nd + 26) * n,
@@ -336,13 +340,13 @@ def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None):
         if from_host:
             for g, hp in zip(slices, pinned):
                 g.copy_(hp, non_blocking=True)
-        with timer("k_step_fused+k_recover"):
+        with timer("fused pass+k_recover"):
             Z.zero_shard_step(slices, Z.ZERO_F16, variants[st["cur"]], flat, Z.ZERO_F16, _hyper(Z, wl.hyper, st["t"]),
                               st["S"], 0.0, 0, ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
 
-    return dict(name=wl.name, step=step, elements=n, nd=nd, launches_per_step=2,
-                kernel_bytes={"k_step_fused+k_recover": (2 * nd + 26) * n}, dominant_label=None,
+    return dict(name=wl.name, step=step, state=st, elements=n, nd=nd, launches_per_step=2,
+                kernel_bytes={"fused pass+k_recover": (2 * nd + 26) * n}, dominant_label=None,
                 h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 formula_bytes=(2 * nd + 26) * n,
                 config={"workload": f"{wl.name}: GPT-like 7.5B-shaped group, N_d=64, rank 63's shard "
@@ -398,11 +402,11 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
                                       stats, ws, ws.numel())
         with timer("k_apply"):
             Z.zero_shard_apply(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"],
-                               stats, 0.0, 0, res)
+                               stats, 0.0, 0, ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
 
     total_units = sum(units)
-    return dict(name=wl.name, step=step, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
+    return dict(name=wl.name, step=step, state=st, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
                 kernel_bytes={"k_gather": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
                 dominant_label=None, h2d=None, d2h=48, e2e_ok=False,
                 formula_bytes=2 * 4 * total_units + (2 * nd + 2) * L + 28 * L,
@@ -544,9 +548,11 @@ def main():
                                 frac=gbs / peak)
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
     dk = per_kernel[dom]
+    wl["config"]["update_kernel"] = PATH_NAMES.get(wl["state"]["path"], "?")
+    wl["config"]["kernel_path_env"] = os.environ.get("ZERO_GB300_PATH", "auto")
     roofline = {"bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dk["achieved_gbs"] / peak, "traffic": ncu_traffic(wl["name"], dom),
-                "peak_source": peak_src, "kernel": wl["dominant_label"] or dom,
+                "peak_source": peak_src, "kernel": f"{dom} [{wl['config']['update_kernel']}]",
                 "kernel_ms_per_launch": dk["ms_per_launch"],
                 "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"]}
     cpu = None

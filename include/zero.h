@@ -58,7 +58,8 @@ typedef enum {
     ZERO_EALIGN = -2,      /* a pointer is not aligned to its element size */
     ZERO_EWORKSPACE = -3,  /* workspace missing or smaller than zero_workspace_bytes() */
     ZERO_ECUDA = -4,       /* a CUDA runtime call or launch failed */
-    ZERO_ELIMIT = -5       /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards */
+    ZERO_ELIMIT = -5,      /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards */
+    ZERO_ETIMEOUT = -6     /* (zero_result.status only) a device-side wait gave up; the step was not applied */
 } zero_status;
 
 typedef enum { ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype;
@@ -153,24 +154,44 @@ typedef struct {
 /* Outcome of a step, written to device (or mapped host) memory.
  * overflow   some reduced gradient element, or extra_overflow, was inf/NaN
  * applied    1 if the update was committed; 0 if the step was skipped --
- *            then master/m/v/param are as before the call (the *_in set)
- * path       1 = fused single pass, 2 = two passes (reduce, then apply)
+ *            then the *_in state is the current state, and the parameters are
+ *            as before the call (restored by the library where a speculative
+ *            pass had written them)
+ * path       which kernels ran the update: 1 = fused single pass (register
+ *            staged), 2 = apply pass (register staged), 3 = fused single pass
+ *            through shared-memory stages fed by bulk asynchronous (TMA)
+ *            copies, 4 = apply pass through such stages
+ * status     0, or ZERO_ETIMEOUT when a device-side wait gave up: the step is
+ *            then reported as not applied, the parameters are restored, and
+ *            the *_out state is indeterminate (for an in-place update that is
+ *            the state itself: treat the state as lost)
  * sumsq      sum of squares of the scaled reduced gradient plus extra_sumsq
  * grad_norm  sqrt(sumsq) / loss_scale
  * clip_coef  max_grad_norm / (grad_norm + 1e-6) when that is below 1, else 1
  * grad_mult  fp32(clip_coef / loss_scale), the multiplier applied to the
  *            reduced gradient before AdamW */
 typedef struct {
-    int32_t overflow, applied, path, reserved;
+    int32_t overflow, applied, path, status;
     double sumsq, grad_norm, clip_coef;
-    float grad_mult, reserved2;
+    float grad_mult, reserved;
 } zero_result;
 
-/* Bytes of device workspace zero_shard_step / zero_shard_reduce /
- * zero3_reduce_bucket need: per-block partial sums, a completion counter and
- * the step's internal statistics.  The workspace must be zero-filled once
- * before its first use; every call leaves it ready for the next.  Calls that
- * share a workspace must not overlap on the device. */
+/* Bytes of device workspace the step calls need (zero_shard_step,
+ * zero_shard_reduce, zero_shard_apply, zero3_reduce_bucket): per-block partial
+ * sums and flags, a completion counter and the step's internal statistics.
+ * The workspace must be zero-filled once before its first use; every call
+ * leaves it ready for the next.  Calls that share a workspace must not overlap
+ * on the device.
+ *
+ * Environment (read at each call; meant for tests and measurements):
+ *   ZERO_GB300_PATH=stream            run the fused and apply passes through
+ *       shared-memory stages fed by bulk asynchronous copies where the
+ *       alignment rules below allow it (default: the register-staged
+ *       kernels, which measure faster on GB300)
+ *   ZERO_GB300_SPIN_LIMIT=n           tries per device-side wait of the
+ *       shared-memory-staged kernels (default 4194304); 0 makes every first
+ *       wait give up, which exercises the ZERO_ETIMEOUT path without hanging
+ *       anything */
 size_t zero_workspace_bytes(void);
 
 /* The whole partitioned step over n_shards shards that share one global
@@ -193,16 +214,22 @@ size_t zero_workspace_bytes(void);
  * Per element i of a shard, in this order: s = sum_r fp32(g_r[i]) in rank
  * order; a = round16(s / N_d); overflow if a is inf/NaN; sumsq += a^2;
  * after all shards: skip if any overflow; k = fp32(c / S) with the clip
- * coefficient c; g = a k; theta = theta (1 - lr wd); m = b1 m + (1-b1) g;
- * v = b2 v + (1-b2) g^2; theta = theta - [lr/(1-b1^t)] m / (sqrt(v)/sqrt(1-b2^t) + eps);
- * flat_param[param_offset + i] = round16(theta).  Every fp32 operation is
- * rounded on its own (no contraction).
+ * coefficient c; g = a k; theta = theta * wdf; m = b1 m + (1-b1) g;
+ * v = b2 v + (1-b2) g^2; theta = theta - ss * (m / (sqrt(v) * rb2 + eps));
+ * flat_param[param_offset + i] = round16(theta), where wdf = fp32(1 - lr wd),
+ * ss = fp32(lr / (1 - b1^t)) and rb2 = fp32(1 / sqrt(1 - b2^t)) are computed
+ * in fp64 on the host.  Every fp32 operation is rounded on its own (no
+ * contraction).
  *
  * Path: with clipping off and every shard's *_out distinct from its *_in, one
  * fused pass reads the slices and the *_in state once and writes the *_out
- * state and the parameters once; on overflow a second, short kernel restores
- * the parameters from master_in (parameters always equal round16(master)).
- * Otherwise two passes: reduce into grad_shard (required then), then apply.
+ * state and the parameters once; if the step is not applied a second, short
+ * kernel restores the parameters from master_in (parameters always equal
+ * round16(master)).  Otherwise two passes: reduce into grad_shard (required
+ * then), then apply.  With ZERO_GB300_PATH=stream the fused and apply
+ * passes run through shared-memory stages fed by bulk asynchronous copies
+ * when there are at most 8 slices and every slice address (+ grad_offset),
+ * state pointer and grad_shard is 16-byte aligned.
  * Errors: ZERO_EINVAL, ZERO_EALIGN (16-bit pointers must be 2-byte aligned,
  * fp32 pointers 4-byte aligned), ZERO_EWORKSPACE, ZERO_ELIMIT, ZERO_ECUDA. */
 int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype,
@@ -226,11 +253,14 @@ int zero_shard_reduce(const void* const* grad_slices, int n_slices, int grad_dty
  * skip and clip from stats->sumsq + extra_sumsq and stats->overflow |
  * extra_overflow, run AdamW from *_in to *_out and store the parameters, and
  * write *result.  For ZeRO-3 the parameters are the rank's own parameter
- * shard buffer (param_offset 0 there). */
+ * shard buffer (param_offset 0 there).  workspace as for zero_shard_step
+ * (it must not be the one *stats lives in if that one is reused concurrently;
+ * sharing the same workspace in stream order is fine). */
 int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype,
                      void* flat_param, int param_dtype,
                      const zero_hyper* hyper, float loss_scale,
                      const zero_stats* stats, double extra_sumsq, int extra_overflow,
+                     void* workspace, size_t workspace_bytes,
                      zero_result* result, void* stream);
 
 /* ------------------------------------------------------------------------

@@ -29,6 +29,17 @@ def Z():
     return Z
 
 
+@pytest.fixture(params=["register", "stream"])
+def kernel_path(request, monkeypatch):
+    """Run a test on the default (register-staged) kernels and again with the
+    shared-memory-staged ones selected wherever the alignment allows them."""
+    if request.param == "stream":
+        monkeypatch.setenv("ZERO_GB300_PATH", "stream")
+    else:
+        monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+    return request.param
+
+
 def dev16(a: np.ndarray, dt):
     return torch.from_numpy(a.view(np.int16).copy()).view(TDT[dt]).to(DEV)
 
@@ -147,7 +158,7 @@ def run_both(Z, numels, nd, dt, mode, seed, h, S, pingpong, steps=3, inject=None
 
 @pytest.mark.parametrize("dt", [1, 2])
 @pytest.mark.parametrize("pingpong", [True, False])
-def test_random_groups_match_oracle(Z, dt, pingpong):
+def test_random_groups_match_oracle(Z, dt, pingpong, kernel_path):
     rng = np.random.default_rng(40 + dt + 2 * pingpong)
     for trial in range(6):
         nd = int(rng.choice([1, 2, 3, 4, 5, 8, 13]))
@@ -159,7 +170,7 @@ def test_random_groups_match_oracle(Z, dt, pingpong):
 
 
 @pytest.mark.parametrize("dt", [1, 2])
-def test_clipped_two_pass_matches_oracle(Z, dt):
+def test_clipped_two_pass_matches_oracle(Z, dt, kernel_path):
     rng = np.random.default_rng(7 + dt)
     for trial in range(4):
         nd = int(rng.choice([2, 3, 4, 8]))
@@ -172,7 +183,7 @@ def test_clipped_two_pass_matches_oracle(Z, dt):
 
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("pingpong", [True, False])
-def test_tiny_workload_with_skip(Z, mode, pingpong):
+def test_tiny_workload_with_skip(Z, mode, pingpong, kernel_path):
     """Tiny fp16 workload: N_d = 3, S = 1024, +inf at flat index 30000 of rank
     0's gradient at step 2 -> step 2 skipped everywhere, S halves, t stays."""
     def inject(grads):
@@ -212,8 +223,8 @@ def test_huge_finite_squares_use_fp64(Z):
     assert np.isfinite(g["grad_norm"]) and g["grad_norm"] == pytest.approx(o["grad_norm"], rel=1e-6)
 
 
-@pytest.mark.parametrize("nd", [1, 13, 64])
-def test_slice_counts(Z, nd):
+@pytest.mark.parametrize("nd", [1, 7, 8, 13, 64])
+def test_slice_counts(Z, nd, kernel_path):
     # the loss scale crosses the C ABI as fp32: give the oracle that same value
     run_both(Z, [9000, 1234], nd, 1, 0, nd, hyper32(), float(np.float32(4096.0 / nd)), True, steps=2)
 
@@ -273,7 +284,8 @@ def test_reduce_and_apply_separately_accumulate(Z):
     Z.zero_shard_reduce(slices, dt, sh[1:], 1, stats, run.ws, run.ws.numel())
     h = hyper32(max_grad_norm=5.0)
     Z.zero_shard_apply(sh, dt, run.flat, dt, Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"],
-                                                     h["max_grad_norm"], 1), 64.0, stats, 0.0, 0, run.res)
+                                                     h["max_grad_norm"], 1), 64.0, stats, 0.0, 0, run.ws, run.ws.numel(),
+                       run.res)
     torch.cuda.synchronize()
     osh = oracle_shards(p, flat, dt, list(range(nd)))
     oflat = flat.copy()
@@ -295,3 +307,84 @@ def test_deterministic(Z):
         r = run.step(grads[0], hyper32(), 1, 1.0)
         outs.append((r.sumsq, t2u16(run.flat)))
     assert outs[0][0] == outs[1][0] and np.array_equal(outs[0][1], outs[1][1])
+
+
+def _staged_rank_local(Z, numel, nd, dt, param_off, clip, steps=3, seed=21, S=1.0):
+    """Rank-local view (staged slices, gradient offset 0): every address the
+    staged kernels copy is 16-byte aligned, so they run; param_off sets the
+    parameter slot's alignment (bulk stores only at a multiple of 8)."""
+    total = param_off + numel + 5
+    p = {"rank_offsets": np.array([param_off]), "rank_numels": np.array([numel])}
+    flat = np.zeros(total, np.uint16)
+    g = W.generator(seed, "cpu")
+    ft = torch.zeros(total, dtype=TDT[dt])
+    W.fill_normal_(ft, 0.02, g)
+    flat[:] = t2u16(ft)
+    gens = [W.generator(seed + 1 + j, "cpu") for j in range(nd)]
+    h = hyper32(max_grad_norm=clip)
+    run = GpuRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
+    osh = oracle_shards(p, flat, dt, [0])
+    osh[0]["grad_off"] = 0
+    oflat = flat.copy()
+    paths = []
+    for t in range(1, steps + 1):
+        staged = []
+        for j in range(nd):
+            x = torch.zeros(numel, dtype=TDT[dt])
+            W.fill_normal_(x, 1e-2, gens[j], S)
+            staged.append(t2u16(x))
+        rg = run.step(staged, h, t, S, grad_offsets=[0])
+        prev = [(o["master"].copy(), o["m"].copy()) for o in osh]
+        ro, red = orc.zero_step(staged, dt, osh, oflat, dt, h, t, S, want_grad=True)
+        compare(run, osh, oflat, rg, ro, clip <= 0.0, prev, red)
+        paths.append(rg.path)
+    return paths
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("numel,param_off", [(1024, 0), (123457, 8), (123457, 3), (5000, 6), (7, 0), (2049, 2)])
+def test_staged_kernels_ragged_and_unaligned_params(Z, dt, numel, param_off, monkeypatch):
+    monkeypatch.setenv("ZERO_GB300_PATH", "stream")
+    S = 256.0 if dt == 1 else 1.0
+    assert set(_staged_rank_local(Z, numel, 4, dt, param_off, 0.0, S=S)) == {3}       # fused, staged
+    assert set(_staged_rank_local(Z, numel, 8, dt, param_off, 0.05, S=S)) == {4}      # two-pass, staged apply
+
+
+def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch):
+    """With the wait limit at 0 every first mbarrier wait of the staged
+    kernels gives up: the step must come back as not applied with status
+    ZERO_ETIMEOUT, the parameters and the *_in state unchanged, and the next
+    call (limit restored) must be correct -- the context stays usable."""
+    monkeypatch.setenv("ZERO_GB300_PATH", "stream")
+    numel, nd, dt = 200000, 4, 2
+    p = {"rank_offsets": np.array([0]), "rank_numels": np.array([numel])}
+    flat = t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 0.02, W.generator(5, "cpu")))
+    staged = [t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 1e-3, W.generator(6 + j, "cpu")))
+              for j in range(nd)]
+    for clip in (0.0, 0.5):                      # fused pass, then the apply pass
+        run = GpuRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
+        h = hyper32(max_grad_norm=clip)
+        before = [x.clone() for x in run.state[0]["A"]]
+        monkeypatch.setenv("ZERO_GB300_SPIN_LIMIT", "0")
+        r = run.step(staged, h, 1, 1.0, grad_offsets=[0])
+        assert r.status == Z.ZERO_ETIMEOUT and r.applied == 0 and r.path in (3, 4)
+        assert np.array_equal(t2u16(run.flat), flat)
+        for x, y in zip(run.state[0]["A"], before):
+            assert torch.equal(x, y)
+        monkeypatch.delenv("ZERO_GB300_SPIN_LIMIT")
+        osh = oracle_shards(p, flat, dt, [0])
+        osh[0]["grad_off"] = 0
+        oflat = flat.copy()
+        rg = run.step(staged, h, 1, 1.0, grad_offsets=[0])
+        prev = [(o["master"].copy(), o["m"].copy()) for o in osh]
+        ro, red = orc.zero_step(staged, dt, osh, oflat, dt, h, 1, 1.0, want_grad=True)
+        assert rg.status == 0 and rg.applied == 1
+        compare(run, osh, oflat, rg, ro, clip <= 0.0, prev, red)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+def test_register_path_reports_register_kernels(Z, dt, monkeypatch):
+    monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+    S = 256.0 if dt == 1 else 1.0
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {1}
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}

@@ -121,7 +121,8 @@ def test_layer_pipeline_three_steps(Z):
             o_g[uoff[u]:uoff[u] + parts[u]], _ = orc.zero3_reduce(buckets[u], me, parts[u], dt, acc)
         sh = [Z.shard(shard_len, 0, 0, master, m, v, grad_shard=gshard)]
         Z.zero_shard_apply(sh, dt, d_shards[me], dt, Z.hyper(step=t, **{k: h[k] for k in
-                           ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, stats, 0.0, 0, res)
+                           ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, stats, 0.0, 0, wsb,
+                           wsb.numel(), res)
         torch.cuda.synchronize()
         # the oracle, in the same order: reduce every unit, then the shard update
         k_mult, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)

@@ -156,7 +156,7 @@ def test_gpt2_1p5b_all_ranks(Z):
         acc, ovf = oracle_stats(grads, dt, 0, P)
         r_gpu = Z.read_result(res)
         k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
-        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path == 1
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (1, 3)
         assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
         cur ^= 1
         for s in samp:
@@ -200,7 +200,7 @@ def test_llama3_8b_rank1_clipped(Z):
         total = acc.value() + extra
         k, norm, clip = orc.grad_multiplier(total, 1.0, wl.max_grad_norm)
         r_gpu = Z.read_result(res)
-        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path == 2
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (2, 4)
         assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5) and clip < 1.0
         assert r_gpu.clip_coef == pytest.approx(clip, rel=1e-5)
         prev = (samp.master.copy(), samp.m.copy())
@@ -314,7 +314,7 @@ def test_zero3_llama3_8b_rank1(Z):
         sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
         Z.zero_shard_apply(sh, dt, rshards[me], dt, Z.hyper(step=t, **{k: h[k] for k in
                            ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, stats, 0.0, 0,
-                           res)
+                           ws, ws.numel(), res)
         k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
         r_gpu = Z.read_result(res)
         assert r_gpu.applied == 1 and r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)

@@ -18,7 +18,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libzero_gb300.so")
 
-ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA, ZERO_ELIMIT = 0, -1, -2, -3, -4, -5
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA, ZERO_ELIMIT, ZERO_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 ZERO_F16, ZERO_BF16 = 1, 2
 ZERO_PLAN_PADDED, ZERO_PLAN_UNPADDED = 0, 1
 ZERO_MAX_SLICES = ZERO_MAX_SHARDS = 64
@@ -49,8 +49,8 @@ class zero_stats(ctypes.Structure):
 
 class zero_result(ctypes.Structure):
     _fields_ = [("overflow", ctypes.c_int32), ("applied", ctypes.c_int32), ("path", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("sumsq", ctypes.c_double), ("grad_norm", ctypes.c_double),
-                ("clip_coef", ctypes.c_double), ("grad_mult", ctypes.c_float), ("reserved2", ctypes.c_float)]
+                ("status", ctypes.c_int32), ("sumsq", ctypes.c_double), ("grad_norm", ctypes.c_double),
+                ("clip_coef", ctypes.c_double), ("grad_mult", ctypes.c_float), ("reserved", ctypes.c_float)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if not k.startswith("reserved")}
@@ -68,7 +68,8 @@ _SIGS = {
     "zero_shard_step": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P,
                              ctypes.c_size_t, _P, _P]),
     "zero_shard_reduce": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
-    "zero_shard_apply": (_I, [_P, _I, _I, _P, _I, _P, ctypes.c_float, _P, ctypes.c_double, _I, _P, _P]),
+    "zero_shard_apply": (_I, [_P, _I, _I, _P, _I, _P, ctypes.c_float, _P, ctypes.c_double, _I, _P, ctypes.c_size_t,
+                              _P, _P]),
     "zero3_gather_layer": (_I, [_P, _I, _I64, _I, _P, _P]),
     "zero3_reduce_bucket": (_I, [_P, _I, _I, _I64, _I, _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
@@ -177,11 +178,11 @@ def zero_shard_reduce(grad_slices, grad_dtype, shards, accumulate, stats, worksp
 
 
 def zero_shard_apply(shards, grad_dtype, flat_param, param_dtype, hyper, loss_scale, stats, extra_sumsq,
-                     extra_overflow, result, stream=None):
+                     extra_overflow, workspace, workspace_bytes, result, stream=None):
     sh = (zero_shard * max(1, len(shards)))(*shards)
     _check(lib.zero_shard_apply(sh, len(shards), grad_dtype, _ptr(flat_param), param_dtype, ctypes.byref(hyper),
-                                loss_scale, _ptr(stats), extra_sumsq, int(extra_overflow), _ptr(result),
-                                _stream(stream)))
+                                loss_scale, _ptr(stats), extra_sumsq, int(extra_overflow), _ptr(workspace),
+                                workspace_bytes, _ptr(result), _stream(stream)))
 
 
 def zero3_gather_layer(part_ptrs, unit_numel, dtype, layer_out, stream=None):

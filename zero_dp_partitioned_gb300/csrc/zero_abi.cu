@@ -3,12 +3,14 @@
 // arguments, and the host-only planner and memory model.
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
 #include <unordered_map>
 
 #include "zero_internal.h"
+#include "zero_stream.cuh"
 
 namespace zdp {
 
@@ -22,7 +24,7 @@ int cuda_fail(cudaError_t e, const char* what) {
     return ZERO_ECUDA;
 }
 
-int grid_for(const void* func, int64_t n_tiles) {
+int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int max_per_sm) {
     static std::mutex mu;
     static std::unordered_map<const void*, int> per_sm[16];
     static int sms[16] = {0};
@@ -35,18 +37,37 @@ int grid_for(const void* func, int64_t n_tiles) {
         if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
         auto it = per_sm[dev].find(func);
         if (it == per_sm[dev].end()) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, TILE_THREADS, 0) != cudaSuccess || nb < 1)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, TILE_THREADS, dynamic_smem) != cudaSuccess ||
+                nb < 1)
                 nb = 1;
             per_sm[dev][func] = nb;
         } else {
             nb = it->second;
         }
     }
+    if (max_per_sm > 0 && nb > max_per_sm) nb = max_per_sm;
     int64_t g = (int64_t)nb * (sms[dev] > 0 ? sms[dev] : 1);
     if (g > n_tiles) g = n_tiles;
     if (g > MAX_BLOCKS) g = MAX_BLOCKS;
     if (g < 1) g = 1;
     return (int)g;
+}
+
+int grid_for(const void* func, int64_t n_tiles, int max_per_sm) {
+    return grid_for_smem(func, n_tiles, 0, max_per_sm);
+}
+
+// Implementation choice and wait limit, from the environment (tests and measurements).
+static int path_choice() {          // 1 register (default), 2 staged
+    const char* e = std::getenv("ZERO_GB300_PATH");
+    if (e && !std::strcmp(e, "stream")) return 2;
+    return 1;
+}
+
+static unsigned spin_limit() {
+    const char* e = std::getenv("ZERO_GB300_SPIN_LIMIT");
+    if (!e) return SPIN_LIMIT;
+    return (unsigned)std::strtoul(e, nullptr, 10);
 }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -157,6 +178,33 @@ static bool vec8_ok(const StepArgs& a, int need) {
         if (need == 3 && !aligned(d.gshard, 16)) return false;
     }
     return true;
+}
+
+// The staged passes need 16-byte aligned bulk-copy addresses: every slice at
+// its shard's gradient offset (fused), the grad shard (apply), every state
+// pointer; and at most MAX_STREAM_SLICES slices.
+static bool stream_ok(const StepArgs& a, bool fused) {
+    if (fused && a.n_slices > MAX_STREAM_SLICES) return false;
+    return vec8_ok(a, fused ? 1 : 3);
+}
+
+static bool param_bulk_ok(const StepArgs& a) {
+    if (!aligned(a.flat_param, 16)) return false;
+    for (int i = 0; i < a.n_shards; ++i)
+        if (a.shards[i].numel > 0 && (a.shards[i].param_off & 7)) return false;
+    return true;
+}
+
+static int run_stream(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s) {
+    StreamArgs sa;
+    std::memset(&sa, 0, sizeof sa);
+    number_tiles(a, CHUNK / TILE_THREADS);     // chunks of CHUNK elements
+    sa.a = a;
+    sa.stages = stream_stages(fused ? a.n_slices : 1);
+    sa.spin_limit = spin_limit();
+    sa.drain_limit = SPIN_LIMIT;
+    sa.param_bulk = param_bulk_ok(a) ? 1 : 0;
+    return launch_stream(sa, gdt, pdt, fused, s);
 }
 
 static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
@@ -287,12 +335,19 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
     a.result = result;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    const int choice = path_choice();
     if (fused) {
         a.k = (float)(1.0 / (double)loss_scale);
-        const int vec = vec8_ok(a, 1) ? 8 : 1;
-        number_tiles(a, vec);
-        const int grid = grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles);
-        if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
+        if (choice == 2 && stream_ok(a, true)) {
+            if ((rc = run_stream(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
+        } else {
+            const int vec = vec8_ok(a, 1) ? 8 : 1;
+            number_tiles(a, vec);
+            const int grid =
+                grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles,
+                         n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+            if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
+        }
         return launch_recover(a, param_dtype, s);
     }
     a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
@@ -300,6 +355,7 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
     int vec = vec8_ok(a, 2) ? 8 : 1;
     number_tiles(a, vec);
     if ((rc = launch_reduce(a, grad_dtype, vec, s)) != ZERO_OK) return rc;
+    if (choice == 2 && stream_ok(a, false)) return run_stream(a, grad_dtype, param_dtype, false, s);
     vec = vec8_ok(a, 3) ? 8 : 1;
     number_tiles(a, vec);
     return launch_apply(a, grad_dtype, param_dtype, vec, s);
@@ -325,7 +381,8 @@ int zero_shard_reduce(const void* const* grad_slices, int n_slices, int grad_dty
 
 int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, void* flat_param, int param_dtype,
                      const zero_hyper* hyper, float loss_scale, const zero_stats* stats, double extra_sumsq,
-                     int extra_overflow, zero_result* result, void* stream) {
+                     int extra_overflow, void* workspace, size_t workspace_bytes, zero_result* result,
+                     void* stream) {
     if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
     int rc;
     if ((rc = check_hyper(hyper, loss_scale)) != ZERO_OK) return rc;
@@ -344,6 +401,9 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
     a.extra_overflow = extra_overflow ? 1 : 0;
     a.stats = const_cast<zero_stats*>(stats);
     a.result = result;
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+    if (path_choice() == 2 && stream_ok(a, false))
+        return run_stream(a, grad_dtype, param_dtype, false, static_cast<cudaStream_t>(stream));
     const int vec = vec8_ok(a, 3) ? 8 : 1;
     number_tiles(a, vec);
     return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));

@@ -38,7 +38,7 @@ int launch_recover(const StepArgs& a, int pdt, cudaStream_t s) {
     const void* f = pdt == ZERO_BF16 ? (const void*)k_recover<ZERO_BF16> : (const void*)k_recover<ZERO_F16>;
     int64_t n = 0;
     for (int i = 0; i < a.n_shards; ++i) n = a.shards[i].numel > n ? a.shards[i].numel : n;
-    const int grid = grid_for(f, (n + TILE_THREADS - 1) / TILE_THREADS);
+    const int grid = grid_for(f, (n + TILE_THREADS - 1) / TILE_THREADS, BPS_RECOVER);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "recover launch");
 }

@@ -13,9 +13,28 @@ namespace zdp {
 void set_error(const std::string& msg);
 int cuda_fail(cudaError_t e, const char* what);
 
+// Resident blocks per SM each pass is launched with (0 = as many as fit).
+// Measured on GB300 over the full workloads: passes that write a third or
+// more of their bytes (the fused pass with few slices, the apply pass) reach
+// more of the HBM bandwidth with fewer concurrent warps -- 2 blocks of 256
+// threads per SM: 10.8 ms vs 11.7 ms for the 8-slice fused GPT-2 step at the 4
+// blocks its registers allow, 8.5 ms vs 9.7 ms for the Llama apply pass --
+// while read-dominated passes want every block they can get (the 64-slice
+// fused pass: 2.63 ms at 4 blocks, 3.11 ms at 2; the reduce is indifferent);
+// the gather (a copy) peaks at 4.
+constexpr int BPS_FUSED_FEW = 2;        // fused pass with at most FEW_SLICES slices
+constexpr int FEW_SLICES = 12;
+constexpr int BPS_FUSED_MANY = 0;
+constexpr int BPS_APPLY = 2;
+constexpr int BPS_REDUCE = 0;
+constexpr int BPS_GATHER = 4;
+constexpr int BPS_RECOVER = 0;
+
 // Blocks of 256 threads to launch for `func` over n_tiles tiles: resident
-// blocks per SM x SM count, capped by the tile count and MAX_BLOCKS.
-int grid_for(const void* func, int64_t n_tiles);
+// blocks per SM (at most max_per_sm when that is > 0) x SM count, capped by
+// the tile count and MAX_BLOCKS.
+int grid_for(const void* func, int64_t n_tiles, int max_per_sm = 0);
+int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int max_per_sm = 0);
 
 // Launchers; each validates nothing (the entry points did) and returns
 // ZERO_OK or ZERO_ECUDA.  vec is 8 or 1.
@@ -24,6 +43,14 @@ int launch_recover(const StepArgs& a, int pdt, cudaStream_t s);
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s);
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s);
 int launch_gather(const GatherArgs& a, int vec, cudaStream_t s);
+
+// The shared-memory-staged passes (zero_stream.cu): selected only by
+// ZERO_GB300_PATH=stream; on GB300 they are slower than the register-staged
+// passes (14.1 ms vs 10.8 ms for the fused GPT-2 step), so the default is the
+// register path.
+struct StreamArgs;
+int stream_stages(int n_grad_arrays);
+int launch_stream(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
 
 // Kernel addresses, for the occupancy query.
 const void* fused_kernel(int gdt, int pdt, int vec, int ns);

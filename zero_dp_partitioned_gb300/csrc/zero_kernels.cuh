@@ -15,11 +15,14 @@
 //    bytes in flight; loads and stores use the streaming cache hints because
 //    no byte is touched twice.
 //  * Gradient statistics: squares of the 16-bit reduced values are exact in
-//    fp32 (at most 22 significant bits) and are summed per vector in fp32,
-//    then in fp64 per thread; a warp-shuffle and a shared-memory pass give
-//    one fp64 partial per block, stored in the workspace; the last block to
-//    finish (one atomic per block) adds the partials in block order, so the
-//    result is deterministic for a given grid.
+//    fp32 (at most 22 significant bits).  Each thread sums them with
+//    Neumaier's compensated summation on the fp32 pipe (GB300's fp64 rate is
+//    far too low for one fp64 add per element), which keeps the rounding
+//    error of the per-thread sum at the level of fp64; the (sum, compensation)
+//    pair is added into an fp64 accumulator at the end.  A warp shuffle and a
+//    shared-memory pass give one fp64 partial per block, stored in the
+//    workspace; the last block to finish (one atomic per block) adds the
+//    partials in block order, so the result is deterministic for a given grid.
 //  * Every fp32 operation of the reduction and of AdamW is an explicitly
 //    rounded intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn) so no
 //    multiply-add is contracted: results are those of the plain IEEE sequence.
@@ -109,6 +112,13 @@ __device__ __forceinline__ void add8(float (&s)[8], const uint4& w) {
 }
 
 // ---------------------------------------------------------------- streaming memory access
+// Data that no thread writes while the kernel runs (gradient slices; the
+// *_in state of the fused pass, whose outputs go to a distinct state set) is
+// read through the non-coherent read-only path; data that may be written in
+// place (the apply pass's state) with streaming loads.  Stores are streaming
+// (evict-first): nothing is read back.
+__device__ __forceinline__ uint4 ld_ro(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ float4 ld_ro4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ uint4 ld_stream(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ float4 ld_stream4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st_stream4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
@@ -152,18 +162,78 @@ __device__ __forceinline__ void store8(uint16_t* dst, int64_t q, const uint32_t 
 }
 
 // ---------------------------------------------------------------- reductions
+// Compensated running sum of non-negative fp32 terms (Neumaier): s + c carries
+// the sum with an error of order n u^2 instead of n u.
+struct SumSq {
+    float s = 0.0f, c = 0.0f;
+    double acc = 0.0;
+
+    __device__ __forceinline__ void add(float x) {
+        const float t = __fadd_rn(s, x);
+        const float big = fmaxf(s, x), small = fminf(s, x);
+        c = __fadd_rn(c, __fadd_rn(__fsub_rn(big, t), small));
+        s = t;
+    }
+    // Add the squares of 8 fp32 values (exact products); vectors whose
+    // squares leave the fp32 range go to fp64 directly.
+    __device__ __forceinline__ void add8(const float (&a)[8]) {
+        float q[8];
+        bool ok = true;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            q[e] = __fmul_rn(a[e], a[e]);
+            ok &= q[e] < 1e30f;          // false for inf, NaN and huge squares
+        }
+        if (ok) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) add(q[e]);
+            if (s > 1e30f) flush();
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc += (double)a[e] * (double)a[e];
+        }
+    }
+    __device__ __forceinline__ void add4(const float (&a)[4]) {
+        float q[4];
+        bool ok = true;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            q[e] = __fmul_rn(a[e], a[e]);
+            ok &= q[e] < 1e30f;
+        }
+        if (ok) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) add(q[e]);
+            if (s > 1e30f) flush();
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc += (double)a[e] * (double)a[e];
+        }
+    }
+    __device__ __forceinline__ void add_fp64(float a) { acc += (double)a * (double)a; }
+    __device__ __forceinline__ void flush() {
+        acc += (double)s + (double)c;
+        s = 0.0f;
+        c = 0.0f;
+    }
+    __device__ __forceinline__ double total() {
+        flush();
+        return acc;
+    }
+};
+
 __device__ __forceinline__ double warp_sum(double x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
 
-// Block-wide sum (fixed order) of x and OR of f; valid in thread 0.
+// Block-wide sum (fixed order) of x and bitwise OR of f; valid in thread 0.
 __device__ __forceinline__ void block_reduce(double& x, int& f) {
     __shared__ double sx[TILE_THREADS / 32];
     __shared__ int sf[TILE_THREADS / 32];
     x = warp_sum(x);
-    f = __any_sync(0xffffffffu, f) ? 1 : 0;
+    f = (int)__reduce_or_sync(0xffffffffu, (unsigned)f);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     if (l == 0) { sx[w] = x; sf[w] = f; }
     __syncthreads();
@@ -171,7 +241,7 @@ __device__ __forceinline__ void block_reduce(double& x, int& f) {
         x = l < TILE_THREADS / 32 ? sx[l] : 0.0;
         f = l < TILE_THREADS / 32 ? sf[l] : 0;
         x = warp_sum(x);
-        f = __any_sync(0xffffffffu, f) ? 1 : 0;
+        f = (int)__reduce_or_sync(0xffffffffu, (unsigned)f);
     }
 }
 
@@ -235,7 +305,7 @@ __device__ __forceinline__ void reduce8(const StepArgs& a, int64_t off, float (&
     if (NS > 0) {
         uint4 w[NS > 0 ? NS : 1];
 #pragma unroll
-        for (int r = 0; r < NS; ++r) w[r] = ld_stream(static_cast<const uint16_t*>(a.slices[r]) + off);
+        for (int r = 0; r < NS; ++r) w[r] = ld_ro(static_cast<const uint16_t*>(a.slices[r]) + off);
 #pragma unroll
         for (int r = 0; r < NS; ++r) add8<GDT>(s, w[r]);
     } else {
@@ -244,11 +314,11 @@ __device__ __forceinline__ void reduce8(const StepArgs& a, int64_t off, float (&
         for (; r + 8 <= n; r += 8) {
             uint4 w[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) w[q] = ld_stream(static_cast<const uint16_t*>(a.slices[r + q]) + off);
+            for (int q = 0; q < 8; ++q) w[q] = ld_ro(static_cast<const uint16_t*>(a.slices[r + q]) + off);
 #pragma unroll
             for (int q = 0; q < 8; ++q) add8<GDT>(s, w[q]);
         }
-        for (; r < n; ++r) add8<GDT>(s, ld_stream(static_cast<const uint16_t*>(a.slices[r]) + off));
+        for (; r < n; ++r) add8<GDT>(s, ld_ro(static_cast<const uint16_t*>(a.slices[r]) + off));
     }
 }
 
@@ -269,7 +339,7 @@ template <int GDT, int PDT, int VEC, int NS>
 __global__ void __launch_bounds__(TILE_THREADS)
 k_step_fused(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
-    double acc = 0.0;
+    SumSq sumsq;
     int ovf = 0;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     const float k = a.k;
@@ -279,34 +349,25 @@ k_step_fused(const __grid_constant__ StepArgs a) {
         const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
         if (j >= d.numel) continue;
         if (VEC == 8 && j + 8 <= d.numel) {
-            const float4 t0 = ld_stream4(d.mi + j), t1 = ld_stream4(d.mi + j + 4);
-            const float4 m0 = ld_stream4(d.mmi + j), m1 = ld_stream4(d.mmi + j + 4);
-            const float4 v0 = ld_stream4(d.vi + j), v1 = ld_stream4(d.vi + j + 4);
+            const float4 t0 = ld_ro4(d.mi + j), t1 = ld_ro4(d.mi + j + 4);
+            const float4 m0 = ld_ro4(d.mmi + j), m1 = ld_ro4(d.mmi + j + 4);
+            const float4 v0 = ld_ro4(d.vi + j), v1 = ld_ro4(d.vi + j + 4);
             float s[8];
             reduce8<GDT, NS>(a, d.grad_off + j, s);
             float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
             float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
             uint32_t hp[8];
-            float sq = 0.0f;
+            float af[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t h = average16<GDT>(s[e], a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h);
-                const float af = Half16<GDT>::widen(h);
-                sq = __fadd_rn(sq, __fmul_rn(af, af));
-                adamw1(th[e], mm[e], vv[e], af, k, a.sc);
+                af[e] = Half16<GDT>::widen(h);
+                adamw1(th[e], mm[e], vv[e], af[e], k, a.sc);
                 hp[e] = Half16<PDT>::narrow(th[e]);
             }
-            if (isfinite(sq)) {
-                acc += (double)sq;
-            } else {                        // a square above the fp32 range (or an inf/NaN): redo in fp64
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const double x = (double)Half16<GDT>::widen(average16<GDT>(s[e], a.divisor));
-                    acc += x * x;
-                }
-            }
+            sumsq.add8(af);
             st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
             st_stream4(d.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
             st_stream4(d.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
@@ -320,7 +381,7 @@ k_step_fused(const __grid_constant__ StepArgs a) {
                 const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h);
                 const float af = Half16<GDT>::widen(h);
-                acc += (double)af * (double)af;
+                sumsq.add_fp64(af);
                 float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
                 adamw1(th, mm, vv, af, k, a.sc);
                 d.mo[i] = th;
@@ -330,6 +391,7 @@ k_step_fused(const __grid_constant__ StepArgs a) {
             }
         }
     }
+    double acc = sumsq.total();
     block_reduce(acc, ovf);
     if (!publish_partial(a, acc, ovf)) return;
     double sum;
@@ -340,12 +402,12 @@ k_step_fused(const __grid_constant__ StepArgs a) {
         r.overflow = (flag | a.extra_overflow) ? 1 : 0;
         r.applied = r.overflow ? 0 : 1;
         r.path = 1;
-        r.reserved = 0;
+        r.status = 0;
         r.sumsq = sum + a.extra_sumsq;
         r.grad_norm = sqrt(r.sumsq) / a.loss_scale;
         r.clip_coef = 1.0;
         r.grad_mult = a.k;
-        r.reserved2 = 0.0f;
+        r.reserved = 0.0f;
         *a.result = r;
     }
 }
@@ -353,7 +415,7 @@ k_step_fused(const __grid_constant__ StepArgs a) {
 // ---------------------------------------------------------------- K1r: restore parameters after a skipped fused step
 template <int PDT>
 __global__ void __launch_bounds__(TILE_THREADS) k_recover(const __grid_constant__ StepArgs a) {
-    if (!__ldcg(&a.result->overflow)) return;
+    if (__ldcg(&a.result->applied)) return;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     for (int si = 0; si < a.n_shards; ++si) {
         const ShardDev& d = a.shards[si];
@@ -368,7 +430,7 @@ template <int GDT, int VEC, int NS>
 __global__ void __launch_bounds__(TILE_THREADS)
 k_reduce(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
-    double acc = 0.0;
+    SumSq sumsq;
     int ovf = 0;
     for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
@@ -380,35 +442,26 @@ k_reduce(const __grid_constant__ StepArgs a) {
             float s[8];
             reduce8<GDT, NS>(a, d.grad_off + j, s);
             uint32_t h[8];
-            float sq = 0.0f;
+            float af[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 h[e] = average16<GDT>(s[e], a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h[e]);
-                const float af = Half16<GDT>::widen(h[e]);
-                sq = __fadd_rn(sq, __fmul_rn(af, af));
+                af[e] = Half16<GDT>::widen(h[e]);
             }
-            if (isfinite(sq)) {
-                acc += (double)sq;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const double x = (double)Half16<GDT>::widen(h[e]);
-                    acc += x * x;
-                }
-            }
+            sumsq.add8(af);
             store8(G, j, h);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
             for (int64_t i = j; i < end; ++i) {
                 const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h);
-                const float af = Half16<GDT>::widen(h);
-                acc += (double)af * (double)af;
+                sumsq.add_fp64(Half16<GDT>::widen(h));
                 G[i] = (uint16_t)h;
             }
         }
     }
+    double acc = sumsq.total();
     block_reduce(acc, ovf);
     if (!publish_partial(a, acc, ovf)) return;
     double sum;
@@ -438,12 +491,12 @@ k_apply(const __grid_constant__ StepArgs a) {
         r.overflow = overflow;
         r.applied = overflow ? 0 : 1;
         r.path = 2;
-        r.reserved = 0;
+        r.status = 0;
         r.sumsq = sumsq;
         r.grad_norm = norm;
         r.clip_coef = clip;
         r.grad_mult = k;
-        r.reserved2 = 0.0f;
+        r.reserved = 0.0f;
         *a.result = r;
     }
     if (overflow) return;

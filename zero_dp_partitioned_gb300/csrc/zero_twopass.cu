@@ -35,21 +35,21 @@ const void* apply_kernel(int gdt, int pdt, int vec) {
 
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s) {
     const void* f = reduce_kernel(gdt, vec, ns_variant(a.n_slices));
-    const int grid = grid_for(f, a.n_tiles);
+    const int grid = grid_for(f, a.n_tiles, BPS_REDUCE);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "reduce launch");
 }
 
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s) {
     const void* f = apply_kernel(gdt, pdt, vec);
-    const int grid = grid_for(f, a.n_tiles);
+    const int grid = grid_for(f, a.n_tiles, BPS_APPLY);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "apply launch");
 }
 
 int launch_gather(const GatherArgs& a, int vec, cudaStream_t s) {
     const void* f = vec == 8 ? (const void*)k_gather<8> : (const void*)k_gather<1>;
-    const int grid = grid_for(f, a.tiles_per_part * a.world_size);
+    const int grid = grid_for(f, a.tiles_per_part * a.world_size, BPS_GATHER);
     void* args[] = {const_cast<GatherArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "gather launch");
 }
