@@ -287,6 +287,39 @@ int zero3_reduce_bucket(const void* const* bucket_ptrs, int world_size, int owne
                         int grad_dtype, void* grad_part, int accumulate, zero_stats* stats,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * The step without caller scratch.  The pages have no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory --
+ * code that must not call cudaMalloc because it can synchronise the device
+ * and stall other work, callers inside a program whose own allocator owns all
+ * device memory, plugins that only receive device pointers through a C
+ * interface, code that must not run out of memory in the middle of a step.
+ *
+ * It computes exactly what zero_shard_step computes, with the same arguments
+ * except that there is no workspace, and grad_shard is not used: the step's
+ * workspace and, on the two-pass path (clipping on, or some shard updated in
+ * place), the shards' 16-bit reduced gradients live in one scratch array built
+ * into the library -- WS (the zero_workspace_bytes() amount) plus 2097152
+ * reduced-gradient elements, about 4 MB, held on every GPU that loads the
+ * library until the process exits.  On the two-pass path the shards together
+ * may need at most 2097152 elements (each shard's count rounded up to 128);
+ * a larger call returns ZERO_ELIMIT and does nothing.  The fused single pass
+ * has no such limit.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the array and clears its counter and statistics on `stream`
+ * before its kernels run; calls whose work can overlap on the GPU (other
+ * streams, other host threads) race on the array and must be serialised by
+ * the caller.  No device memory is allocated or freed.
+ * ------------------------------------------------------------------------ */
+int zero_shard_step_noalloc(const void* const* grad_slices, int n_slices, int grad_dtype,
+                            const zero_shard* shards, int n_shards,
+                            void* flat_param, int param_dtype,
+                            const zero_hyper* hyper, float loss_scale,
+                            double extra_sumsq, int extra_overflow,
+                            zero_result* result, void* stream);
+
 /* Message of the last error on this thread ("" if none). */
 const char* zero_last_error(void);
 

@@ -7,7 +7,7 @@ torch tensors (their ``data_ptr()``) or as integers.  A nonzero status raises
 ``ZeroError`` with the library's message.
 
 Importing this package loads the compiled library; if it has not been built
-(``python -m zero_dp_partitioned_gb300.build``) the import fails -- there is
+(``python zero_dp_partitioned_gb300/build.py``) the import fails -- there is
 no fallback.
 """
 from __future__ import annotations
@@ -72,6 +72,7 @@ _SIGS = {
                               _P, _P]),
     "zero3_gather_layer": (_I, [_P, _I, _I64, _I, _P, _P]),
     "zero3_reduce_bucket": (_I, [_P, _I, _I, _I64, _I, _P, _I, _P, _P, ctypes.c_size_t, _P]),
+    "zero_shard_step_noalloc": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 # every symbol include/zero.h declares
@@ -80,7 +81,7 @@ EXPORTS = tuple(_SIGS)
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m zero_dp_partitioned_gb300.build`")
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python zero_dp_partitioned_gb300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in _SIGS.items():
         fn = getattr(lib, name)
@@ -169,6 +170,17 @@ def zero_shard_step(grad_slices, grad_dtype, shards, flat_param, param_dtype, hy
     _check(lib.zero_shard_step(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards), _ptr(flat_param),
                                param_dtype, ctypes.byref(hyper), loss_scale, extra_sumsq, int(extra_overflow),
                                _ptr(workspace), workspace_bytes, _ptr(result), _stream(stream)))
+
+
+def zero_shard_step_noalloc(grad_slices, grad_dtype, shards, flat_param, param_dtype, hyper, loss_scale,
+                            extra_sumsq, extra_overflow, result, stream=None):
+    """zero_shard_step without caller scratch (for callers that cannot allocate
+    device memory): the library's built-in scratch array stands in for the
+    workspace and the two-pass path's reduced-gradient buffers."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_step_noalloc(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards),
+                                       _ptr(flat_param), param_dtype, ctypes.byref(hyper), loss_scale, extra_sumsq,
+                                       int(extra_overflow), _ptr(result), _stream(stream)))
 
 
 def zero_shard_reduce(grad_slices, grad_dtype, shards, accumulate, stats, workspace, workspace_bytes, stream=None):

@@ -1,7 +1,8 @@
 """Build step of the CUDA library: compiles csrc/*.cu for sm_103a (GB300) in
 parallel and links zero_dp_partitioned_gb300/_build/libzero_gb300.so.
 
-    python -m zero_dp_partitioned_gb300.build
+    python zero_dp_partitioned_gb300/build.py   (a standalone script: importing the
+    package loads the library this builds)
 """
 from __future__ import annotations
 
