@@ -20,13 +20,14 @@ int cuda_fail(cudaError_t e, const char* what);
 // threads per SM: 10.8 ms vs 11.7 ms for the 8-slice fused GPT-2 step at the 4
 // blocks its registers allow, 8.5 ms vs 9.7 ms for the Llama apply pass --
 // while read-dominated passes want every block they can get (the 64-slice
-// fused pass: 2.63 ms at 4 blocks, 3.11 ms at 2; the reduce is indifferent);
+// fused pass: 2.63 ms at 4 blocks, 3.11 ms at 2; the reduce pass is best at
+// 6: 2.98 ms, against 3.13 at 4 and 3.11 at the 8 its 32 registers allow);
 // the gather (a copy) peaks at 4.
 constexpr int BPS_FUSED_FEW = 2;        // fused pass with at most FEW_SLICES slices
 constexpr int FEW_SLICES = 12;
 constexpr int BPS_FUSED_MANY = 0;
 constexpr int BPS_APPLY = 2;
-constexpr int BPS_REDUCE = 0;
+constexpr int BPS_REDUCE = 6;
 constexpr int BPS_GATHER = 4;
 constexpr int BPS_RECOVER = 0;
 

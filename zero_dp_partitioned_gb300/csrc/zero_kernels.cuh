@@ -89,6 +89,11 @@ template <> struct Half16<ZERO_BF16> {
         return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
     }
     static __device__ __forceinline__ bool nonfinite(uint32_t h) { return (h & 0x7F80u) == 0x7F80u; }
+    // two values, rounded as narrow() does, packed low | high << 16
+    static __device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&p);
+    }
 };
 template <> struct Half16<ZERO_F16> {
     static __device__ __forceinline__ float widen(uint32_t h) {
@@ -98,6 +103,10 @@ template <> struct Half16<ZERO_F16> {
         return (uint32_t)__half_as_ushort(__float2half_rn(x));
     }
     static __device__ __forceinline__ bool nonfinite(uint32_t h) { return (h & 0x7C00u) == 0x7C00u; }
+    static __device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
+        const __half2 p = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&p);
+    }
 };
 
 // 8 packed 16-bit values (one uint4) -> fp32, added in order to s[0..7]
@@ -128,6 +137,15 @@ __device__ __forceinline__ void st_stream4(float* p, float4 v) { __stcs(reinterp
 template <int GDT>
 __device__ __forceinline__ uint32_t average16(float s, float divisor) {
     return Half16<GDT>::narrow(__fdiv_rn(s, divisor));
+}
+
+// The same with the slice count known at compile time: a power-of-two
+// divisor is a multiplication by its exact reciprocal, which rounds the same
+// exact value s / 2^k once -- the identical result, in one instruction.
+template <int GDT, int NS>
+__device__ __forceinline__ uint32_t average16n(float s, float divisor) {
+    if (NS == 1 || NS == 2 || NS == 4 || NS == 8) return Half16<GDT>::narrow(__fmul_rn(s, 1.0f / (float)NS));
+    return average16<GDT>(s, divisor);
 }
 
 // AdamW on one coordinate, the operations in the order of the update rule.
@@ -162,16 +180,16 @@ __device__ __forceinline__ void store8(uint16_t* dst, int64_t q, const uint32_t 
 }
 
 // ---------------------------------------------------------------- reductions
-// Compensated running sum of non-negative fp32 terms (Neumaier): s + c carries
-// the sum with an error of order n u^2 instead of n u.
+// Compensated running sum of non-negative fp32 terms (Kahan): s - c carries
+// the sum with an error of order n u^2 of the sum instead of n u.
 struct SumSq {
     float s = 0.0f, c = 0.0f;
     double acc = 0.0;
 
     __device__ __forceinline__ void add(float x) {
-        const float t = __fadd_rn(s, x);
-        const float big = fmaxf(s, x), small = fminf(s, x);
-        c = __fadd_rn(c, __fadd_rn(__fsub_rn(big, t), small));
+        const float y = __fsub_rn(x, c);
+        const float t = __fadd_rn(s, y);
+        c = __fsub_rn(__fsub_rn(t, s), y);
         s = t;
     }
     // Add the squares of 8 fp32 values (exact products); vectors whose
@@ -212,7 +230,7 @@ struct SumSq {
     }
     __device__ __forceinline__ void add_fp64(float a) { acc += (double)a * (double)a; }
     __device__ __forceinline__ void flush() {
-        acc += (double)s + (double)c;
+        acc += (double)s - (double)c;
         s = 0.0f;
         c = 0.0f;
     }
@@ -357,15 +375,20 @@ k_step_fused(const __grid_constant__ StepArgs a) {
             float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
             float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            uint32_t hp[8];
             float af[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const uint32_t h = average16<GDT>(s[e], a.divisor);
+                const uint32_t h = average16n<GDT, NS>(s[e], a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h);
                 af[e] = Half16<GDT>::widen(h);
                 adamw1(th[e], mm[e], vv[e], af[e], k, a.sc);
-                hp[e] = Half16<PDT>::narrow(th[e]);
+            }
+            uint32_t hp[8];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const uint32_t w = Half16<PDT>::narrow2(th[e], th[e + 1]);
+                hp[e] = w & 0xFFFFu;
+                hp[e + 1] = w >> 16;
             }
             sumsq.add8(af);
             st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
@@ -445,7 +468,7 @@ k_reduce(const __grid_constant__ StepArgs a) {
             float af[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                h[e] = average16<GDT>(s[e], a.divisor);
+                h[e] = average16n<GDT, NS>(s[e], a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h[e]);
                 af[e] = Half16<GDT>::widen(h[e]);
             }
@@ -516,12 +539,17 @@ k_apply(const __grid_constant__ StepArgs a) {
             float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
             float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            uint32_t hp[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t h = (e & 1) ? (u[e >> 1] >> 16) : (u[e >> 1] & 0xFFFFu);
                 adamw1(th[e], mm[e], vv[e], Half16<GDT>::widen(h), k, a.sc);
-                hp[e] = Half16<PDT>::narrow(th[e]);
+            }
+            uint32_t hp[8];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const uint32_t w = Half16<PDT>::narrow2(th[e], th[e + 1]);
+                hp[e] = w & 0xFFFFu;
+                hp[e + 1] = w >> 16;
             }
             st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
             st_stream4(d.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
