@@ -263,6 +263,50 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                 formula_bytes=bytes_step, sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
 
 
+def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None):
+    """The GPT-2 1.5B group with stage 1's full all-reduce: the reduce pass
+    writes the whole averaged gradient (the all-reduce result every rank
+    holds), then each rank's shard is updated from its slice of it."""
+    wl = W.workload("gpt2-1.5b-nd8")
+    layers = layers or 48
+    specs = wl.specs if layers == 48 else W.gpt2_group(L=layers)
+    nd = wl.nd
+    plan = Z.zero_plan(W.numels(specs), nd)
+    P = plan["padded_total"]
+    name = "gpt2-1.5b-nd8-allreduce" if layers == 48 else f"gpt2-{layers}layers-nd8-allreduce"
+    log(f"[bench] {name}: Psi={P} N_d={nd}; generating inputs")
+    flat = W.flat_params(specs, P, torch.bfloat16, wl.param_seed, dev)
+    grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
+        [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(nd)], specs, W.gpt2_grad_std())
+    state = [flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)]
+    avg = torch.empty(P, dtype=torch.bfloat16, device=dev)          # the all-reduced gradient
+    sh = [Z.shard(n, off, off, *(x[off:off + n] for x in state), grad_shard=avg[off:off + n])
+          for off, n in zip(plan["rank_offsets"], plan["rank_numels"])]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(16, dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+
+    def step(from_host=False):
+        with timer("k_reduce"):
+            Z.zero_shard_reduce(grads, Z.ZERO_BF16, sh, 0, stats, ws, ws.numel())
+        with timer("k_apply"):
+            Z.zero_shard_apply(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"], stats,
+                               0.0, 0, ws, ws.numel(), res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=2,
+                kernel_bytes={"k_reduce": (2 * nd + 2) * P, "k_apply": 28 * P}, dominant_label=None,
+                h2d=None, d2h=48, e2e_ok=False, formula_bytes=(2 * nd + 26) * P,
+                config={"workload": f"{name}: GPT-2-shaped group, N_d=8, all ranks, stage 1 with a full "
+                                    "all-reduce of the gradient then a per-shard update",
+                        "psi": P, "n_d": nd, "path": "reduce into a full averaged-gradient buffer, then apply",
+                        "bytes_per_step_actual": (2 * nd + 30) * P, "bytes_per_step_formula": (2 * nd + 26) * P,
+                        "l2": "inputs larger than L2, no flush"},
+                sample_for_cpu=None)
+
+
 def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
     """Llama-3-8B-shaped group, N_d = 4, rank 1's shard with 4 staged slices,
     clip 1.0: two passes (reduce + statistics, then apply), state in place."""
@@ -435,7 +479,8 @@ def cpu_sample_gpt2(W, n_per_shard):
     return nd, grads, flat.view(torch.int16).numpy().view(np.uint16).copy(), wl.hyper
 
 
-WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "llama3-8b-nd4-r1": llama_rank_local,
+WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_allreduce,
+             "llama3-8b-nd4-r1": llama_rank_local,
              "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama}
 
 
@@ -520,7 +565,8 @@ def main():
 
     e2e = None
     if wl["e2e_ok"]:
-        step(from_host=True)
+        for _ in range(2):
+            step(from_host=True)
         torch.cuda.synchronize()
         barrier()
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

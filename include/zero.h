@@ -111,6 +111,30 @@ int zero_plan_intersections(const int64_t* tensor_offsets, const int64_t* numels
 int zero_mem_model(double psi, double K, int n_d, int stage, double* bytes_out);
 
 /* ------------------------------------------------------------------------
+ * Communication volume per rank and step, in elements.  Host only.
+ * Source: ZeRO paper (Chinese translation), 7.1 (a reduce-scatter or an
+ * all-gather of Psi elements moves Psi; data parallelism's all-reduce is one
+ * of each: 2 Psi), 7.2.1 (P_os+g: gradient reduce-scatter + parameter
+ * all-gather, 2 Psi), 7.2.2 (P_os+g+p: parameter all-gathers for the forward
+ * and the backward plus the gradient reduce-scatter, 3 Psi = 1.5x); reading
+ * notes 5.5 (P_os with the optimised schedule: 2 Psi) and 4 (a ring moves
+ * (N_d - 1)/N_d Psi per phase).
+ * ring = 0 gives the pages' Psi-per-phase accounting, ring = 1 the ring's
+ * exact figure.  Returns ZERO_OK or ZERO_EINVAL (stage outside 0..3, n_d < 1,
+ * psi < 0, null output).
+ * ------------------------------------------------------------------------ */
+int zero_comm_volume(double psi, int n_d, int stage, int ring, double* elements_out);
+
+/* Round-robin order of a group's tensors before flattening.  Host only.
+ * Source: DeepSpeed ZeRO stages 1-2 walkthrough, 4.1 (round_robin_gradients):
+ * tensor i goes to group i mod world_size and the groups are laid out one
+ * after another, each in its original order, so that tensors adjacent in the
+ * original (backward) order land in different ranks' shards.
+ * order_out[k] = original index of the tensor placed k-th (n_tensors values);
+ * feed the reordered sizes to zero_plan.  Returns ZERO_OK or ZERO_EINVAL. */
+int zero_plan_round_robin(int n_tensors, int world_size, int64_t* order_out);
+
+/* ------------------------------------------------------------------------
  * The step.
  * ------------------------------------------------------------------------ */
 

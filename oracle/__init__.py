@@ -98,6 +98,8 @@ def lib():
                 "orc_ddp_step": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P, ctypes.c_int]
                                  + [ctypes.c_float] * 6 + [_I64, ctypes.c_double, _P]),
                 "orc_zero3_gather": (None, [_P, ctypes.c_int, _I64, _P]),
+                "orc_comm_volume": (ctypes.c_double, [ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+                "orc_round_robin": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P]),
                 "orc_zero3_reduce": (None, [_P, ctypes.c_int, ctypes.c_int, _I64, ctypes.c_int, _P, _P, _P]),
             }
             for name, (res, args) in sig.items():
@@ -184,6 +186,17 @@ def plan_intersections(tensor_offsets, numels, rank_offset: int, rank_numel: int
 
 def mem_model(psi: float, K: float, nd: int, stage: int) -> float:
     return lib().orc_mem_model(psi, K, nd, stage)
+
+
+def comm_volume(psi: float, nd: int, stage: int, ring: bool = False) -> float:
+    return lib().orc_comm_volume(psi, nd, stage, int(ring))
+
+
+def round_robin(n: int, ws: int) -> np.ndarray:
+    out = np.zeros(max(n, 1), np.int64)
+    if lib().orc_round_robin(n, ws, _ptr(out)) != 0:
+        raise ValueError("invalid round-robin arguments")
+    return out[:n]
 
 
 # ---------------------------------------------------------------- the step

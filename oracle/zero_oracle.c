@@ -570,3 +570,39 @@ void orc_zero3_reduce(const uint16_t* const* buckets, int n, int owner, int64_t 
     orc_reduce(buckets, n, gdt, (int64_t)owner * part_numel, part_numel, grad_part);
     orc_stats(grad_part, part_numel, gdt, acc, overflow);
 }
+
+/* ======================================================================
+ * 7. Communication volume ([paper] 7.1-7.2; [notes] 4 and 5.5).
+ * Elements one data-parallel rank sends (and receives) per step in the
+ * data-parallel collectives.  A reduce-scatter or an all-gather of Psi
+ * elements is counted as Psi ([paper] 7.1); with ring = 1 a ring moves
+ * (N_d - 1)/N_d of that per phase ([notes] 4).
+ *   stage 0 (DP): all-reduce = reduce-scatter + all-gather      2 phases
+ *   stage 1, 2:   gradient reduce-scatter + parameter all-gather 2 phases
+ *   stage 3:      parameter all-gather for the forward and again for the
+ *                 backward, plus the gradient reduce-scatter     3 phases
+ * ====================================================================== */
+
+double orc_comm_volume(double psi, int nd, int stage, int ring)
+{
+    if (nd < 1 || stage < 0 || stage > 3) return -1.0;
+    const double phase = ring ? psi * (double)(nd - 1) / (double)nd : psi;
+    return (stage == 3 ? 3.0 : 2.0) * phase;
+}
+
+/* ======================================================================
+ * 8. Round-robin order of a group's tensors ([stages] 4.1): before
+ * flattening, tensor i is put in group i mod world_size and the groups are
+ * laid out one after another, each in its original order, so that tensors
+ * that are adjacent in the original (backward) order land in different
+ * ranks' shards.  order[k] = original index of the tensor placed k-th.
+ * ====================================================================== */
+
+int orc_round_robin(int n, int ws, int64_t* order)
+{
+    if (n < 0 || ws < 1) return -1;
+    int k = 0;
+    for (int g = 0; g < ws; g++)
+        for (int i = g; i < n; i += ws) order[k++] = i;
+    return 0;
+}

@@ -126,3 +126,21 @@ def test_argument_errors_before_any_device_work(Z):
     assert e.value.code == Z.ZERO_EINVAL
     with pytest.raises(Z.ZeroError):
         Z.zero_plan([1, 2], 0)
+
+
+def test_comm_volume_equals_oracle(Z, orc):
+    for psi in (7.5e9, 1e12, 123.0):
+        for nd in (1, 2, 8, 64, 1024):
+            for st in range(4):
+                for ring in (False, True):
+                    assert Z.zero_comm_volume(psi, nd, st, ring) == orc.comm_volume(psi, nd, st, ring)
+    with pytest.raises(Z.ZeroError):
+        Z.zero_comm_volume(1e9, 8, 4)
+
+
+def test_round_robin_equals_oracle(Z, orc):
+    for n in (0, 1, 5, 17, 580):
+        for ws in (1, 2, 3, 8, 64):
+            assert Z.zero_plan_round_robin(n, ws) == orc.round_robin(n, ws).tolist()
+    with pytest.raises(Z.ZeroError):
+        Z.zero_plan_round_robin(4, 0)

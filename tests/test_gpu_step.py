@@ -388,3 +388,32 @@ def test_register_path_reports_register_kernels(Z, dt, monkeypatch):
     S = 256.0 if dt == 1 else 1.0
     assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {1}
     assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}
+
+
+def test_stage1_full_allreduce_then_shard_update(Z):
+    """Stage 1 without reduce-scatter: the reduce pass writes the whole
+    averaged gradient into one buffer (every rank's copy of the all-reduce),
+    then each shard is updated from its slice of it."""
+    numels = [33333, 2222, 4444]
+    nd, dt = 4, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 41, steps=2)
+    P = p["padded_total"]
+    run = GpuRun(Z, p, flat, dt, list(range(nd)), pingpong=False, want_grad=False)
+    avg = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    for s_, o, n in zip(run.state, p["rank_offsets"], p["rank_numels"]):
+        s_["g"] = avg[int(o):int(o) + int(n)]
+    osh = oracle_shards(p, flat, dt, list(range(nd)))
+    oflat = flat.copy()
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    h = hyper32()
+    for t in (1, 2):
+        slices = [dev16(g, dt) for g in grads[t - 1]]
+        sh = run.shards()
+        Z.zero_shard_reduce(slices, dt, sh, 0, stats, run.ws, run.ws.numel())
+        Z.zero_shard_apply(sh, dt, run.flat, dt, Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"],
+                                                         h["weight_decay"], 0.0, t), 1.0, stats, 0.0, 0, run.ws,
+                           run.ws.numel(), run.res)
+        torch.cuda.synchronize()
+        assert np.array_equal(t2u16(avg), orc.reduce(grads[t - 1], dt, 0, P))     # the full all-reduce
+        ro, _ = orc.zero_step(grads[t - 1], dt, osh, oflat, dt, h, t, 1.0)
+        compare(run, osh, oflat, Z.read_result(run.res), ro, True)

@@ -64,6 +64,8 @@ _SIGS = {
     "zero_plan": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "zero_plan_intersections": (_I, [_P, _P, _I, _I64, _I64, _P]),
     "zero_mem_model": (_I, [ctypes.c_double, ctypes.c_double, _I, _I, _P]),
+    "zero_comm_volume": (_I, [ctypes.c_double, _I, _I, _I, _P]),
+    "zero_plan_round_robin": (_I, [_I, _I, _P]),
     "zero_workspace_bytes": (ctypes.c_size_t, []),
     "zero_shard_step": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P,
                              ctypes.c_size_t, _P, _P]),
@@ -144,6 +146,18 @@ def zero_mem_model(psi, K, n_d, stage):
     b = ctypes.c_double()
     _check(lib.zero_mem_model(psi, K, n_d, stage, ctypes.byref(b)))
     return b.value
+
+
+def zero_comm_volume(psi, n_d, stage, ring=False):
+    v = ctypes.c_double()
+    _check(lib.zero_comm_volume(psi, n_d, stage, int(ring), ctypes.byref(v)))
+    return v.value
+
+
+def zero_plan_round_robin(n_tensors, world_size):
+    out = (ctypes.c_int64 * max(1, n_tensors))()
+    _check(lib.zero_plan_round_robin(n_tensors, world_size, out))
+    return list(out)[:n_tensors]
 
 
 def zero_workspace_bytes():

@@ -304,6 +304,25 @@ int zero_mem_model(double psi, double K, int n_d, int stage, double* bytes_out) 
     return ZERO_OK;
 }
 
+int zero_comm_volume(double psi, int n_d, int stage, int ring, double* elements_out) {
+    if (!elements_out || n_d < 1 || stage < 0 || stage > 3 || !(psi >= 0.0))
+        return fail(ZERO_EINVAL, "zero_comm_volume: bad argument");
+    // one reduce-scatter or all-gather of psi elements; a ring moves (n_d-1)/n_d of it
+    const double phase = ring ? psi * (double)(n_d - 1) / (double)n_d : psi;
+    const int phases = stage == 3 ? 3 : 2;   // ZeRO-3 gathers the parameters twice
+    *elements_out = phases * phase;
+    return ZERO_OK;
+}
+
+int zero_plan_round_robin(int n_tensors, int world_size, int64_t* order_out) {
+    if (n_tensors < 0 || world_size < 1 || (n_tensors > 0 && !order_out))
+        return fail(ZERO_EINVAL, "zero_plan_round_robin: bad argument");
+    int k = 0;
+    for (int g = 0; g < world_size; ++g)
+        for (int i = g; i < n_tensors; i += world_size) order_out[k++] = i;
+    return ZERO_OK;
+}
+
 int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
                     int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper, float loss_scale,
                     double extra_sumsq, int extra_overflow, void* workspace, size_t workspace_bytes,
