@@ -461,6 +461,77 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
                 sample_for_cpu=None)
 
 
+def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
+    """ZeRO-3 with owner broadcast on the Llama-3-8B group, N_d = 4, rank 1:
+    each rank keeps one contiguous segment of the flat vector (the plan's
+    partition); per step every one of the 34 units is rebuilt forward and
+    backward from the pieces of its owners' segments, rank 1 reduces every
+    rank's gradient over the pieces it owns, and updates its segment."""
+    wl = W.workload("zero3-llama3-8b")
+    if layers:
+        wl.specs = W.llama_group(L=layers)
+    name = "zero3-bcast-llama3-8b" if not layers else f"zero3-bcast-llama3-{layers}layers"
+    nd, me = wl.nd, 1
+    units = W.llama_units(wl.specs, L=layers or 32)
+    plan = Z.zero_plan(units, nd)
+    P = plan["padded_total"]
+    pieces = {u: [] for u in range(len(units))}
+    for r in range(nd):
+        for u, u0, s0, ln in Z.zero_plan_intersections(plan["tensor_offsets"], units, plan["rank_offsets"][r],
+                                                       plan["rank_numels"][r]):
+            pieces[u].append((r, u0, s0, ln))
+    log(f"[bench] {name}: {len(units)} units, segment of rank 1 {plan['rank_numels'][me]}; generating inputs")
+    flat = W.flat_params(wl.specs, P, torch.bfloat16, wl.param_seed, dev)
+    segs = [flat[o:o + n].clone() for o, n in zip(plan["rank_offsets"], plan["rank_numels"])]
+    del flat
+    torch.cuda.empty_cache()
+    L = plan["rank_numels"][me]
+    gs = W.GradStream([5 + r for r in range(nd)], dev)
+    mine = [u for u in reversed(range(len(units))) if any(r == me for r, *_ in pieces[u])]
+    buckets = {}
+    for u in mine:          # only the units whose gradient rank 1 reduces are read by it
+        buckets[u] = gs.draw_plain([torch.empty(units[u], dtype=torch.bfloat16, device=dev) for _ in range(nd)],
+                                   wl.grad_std)
+    layer = torch.empty(max(units), dtype=torch.bfloat16, device=dev)
+    master, m, v = segs[me].float(), torch.zeros(L, device=dev), torch.zeros(L, device=dev)
+    gseg = torch.empty(L, dtype=torch.bfloat16, device=dev)
+    sh_apply = [Z.shard(L, 0, 0, master, m, v, grad_shard=gseg)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(16, dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+    gathers = [([segs[r][s0:s0 + ln] for r, u0, s0, ln in pieces[u]], [ln for *_, ln in pieces[u]])
+               for u in range(len(units))]
+    reduces = [(buckets[u], [Z.shard(ln, u0, 0, None, None, None, grad_shard=gseg[s0:s0 + ln])])
+               for u in mine for r, u0, s0, ln in pieces[u] if r == me]
+
+    def step(from_host=False):
+        for u in list(range(len(units))) + list(reversed(range(len(units)))):
+            with timer("k_gather"):
+                Z.zero3_gather_segments(gathers[u][0], gathers[u][1], Z.ZERO_BF16, layer)
+        for k, (bk, sh) in enumerate(reduces):
+            with timer("k_reduce"):
+                Z.zero_shard_reduce(bk, Z.ZERO_BF16, sh, k > 0, stats, ws, ws.numel())
+        with timer("k_apply"):
+            Z.zero_shard_apply(sh_apply, Z.ZERO_BF16, segs[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]),
+                               st["S"], stats, 0.0, 0, ws, ws.numel(), res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    total = sum(units)
+    return dict(name=name, step=step, state=st, elements=L, nd=nd,
+                launches_per_step=2 * len(units) + len(reduces) + 1,
+                kernel_bytes={"k_gather": 2 * 4 * total, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False,
+                formula_bytes=2 * 4 * total + (2 * nd + 2) * L + 28 * L,
+                config={"workload": f"{name}: Llama-3-8B group as {len(units)} ZeRO-3 units, owner broadcast "
+                                    "from contiguous rank segments, N_d=4, rank 1",
+                        "units": len(units), "segment_elements": L, "psi": total,
+                        "path": "per unit: gather of the owners' pieces x2, reduce of rank 1's pieces; then apply",
+                        "l2": "inputs larger than L2, no flush"},
+                sample_for_cpu=None)
+
+
 def cpu_sample_gpt2(W, n_per_shard):
     """The first n_per_shard elements of each of the 8 shards of the GPT-2 1.5B
     group, with seeded inputs drawn for that sample (CPU generators)."""
@@ -481,7 +552,8 @@ def cpu_sample_gpt2(W, n_per_shard):
 
 WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_allreduce,
              "llama3-8b-nd4-r1": llama_rank_local,
-             "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama}
+             "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama,
+             "zero3-bcast-llama3-8b": zero3_broadcast}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -499,6 +571,32 @@ def time_oracle(W, wl_fn, n_per_shard, steps):
         oracle.zero_step(grads, 2, shards, flat, 2, hh, t, 1.0)
         times.append(time.perf_counter() - t0)
     return nd * n_per_shard, times
+
+
+# ------------------------------------------------------------------ multi-rank timing and the output line
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the step time the job is charged)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def build_line(world, steps, warmup, ms, elements, nd, config, roofline, kernels, cpu, e2e, clocks, launches,
+               formula_bytes=None):
+    """The JSON line rank 0 prints: value is the whole job's shard elements per
+    second (every rank runs its own copy of the workload, so scaling is weak)."""
+    fb = formula_bytes if formula_bytes is not None else elements * (2 * nd + 26)
+    return {"metric": METRIC, "value": world * elements / (ms / 1e3), "unit": "elements/s",
+            "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded torch generators; no data set or weights)",
+            "config": config, "achieved_gbs_formula": fb / (ms / 1e3) / 1e9,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": launches, "impl": "ours"}
 
 
 # ------------------------------------------------------------------ main
@@ -556,12 +654,8 @@ def main():
     timer.on = False
     barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, dev)
     kinds = timer.per_kind(args.steps)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
 
     e2e = None
     if wl["e2e_ok"]:
@@ -576,11 +670,7 @@ def main():
         e2.record()
         torch.cuda.synchronize()
         barrier()
-        ms_e2e = s2.elapsed_time(e2) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = t.item()
+        ms_e2e = max_over_ranks(s2.elapsed_time(e2) / args.e2e_steps, world, dev)
         e2e = {"value": world * wl["elements"] / (ms_e2e / 1e3), "unit": "elements/s",
                "h2d_bytes_per_step": wl["h2d"], "d2h_bytes_per_step": wl["d2h"], "ms_per_step": ms_e2e,
                "steps": args.e2e_steps}
@@ -608,15 +698,9 @@ def main():
                "sample": f"the first {1 << 22} elements of each of the {wl['nd']} shards "
                          f"({n} elements), 2 steps, single-threaded plain C oracle"}
     if rank == 0:
-        line = {"metric": METRIC, "value": world * wl["elements"] / (ms / 1e3), "unit": "elements/s",
-                "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-                "data": "synthetic (seeded torch generators; no data set or weights)",
-                "config": wl["config"],
-                "achieved_gbs_formula": wl["elements"] * (2 * wl["nd"] + 26) / (ms / 1e3) / 1e9
-                if not wl["name"].startswith("zero3") else wl["formula_bytes"] / (ms / 1e3) / 1e9,
-                "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": wl["launches_per_step"] * args.steps, "impl": "ours"}
+        line = build_line(world, args.steps, max(3, args.warmup), ms, wl["elements"], wl["nd"], wl["config"],
+                          roofline, per_kernel, cpu, e2e, clocks, wl["launches_per_step"] * args.steps,
+                          wl["formula_bytes"] if wl["name"].startswith("zero3") else None)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -302,6 +302,20 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype,
 int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t unit_numel, int dtype,
                        void* layer_out, void* stream);
 
+/* The owner-broadcast form of the same materialisation: each rank keeps one
+ * contiguous segment of the flat parameter vector (the partition of
+ * zero_plan), and a layer is rebuilt from the pieces of the owners' segments
+ * it spans -- one or two pieces -- each broadcast by its owner.
+ * Source: ZeRO paper (Chinese translation), 5.3 and 7.2.2 (the owner of a
+ * partition broadcasts it before the forward of that part of the model, and
+ * again before its backward); CMU 11-868 notes, slides 51-63.
+ * layer_out = segment 0 | segment 1 | ...: segment_ptrs[n_segments] is a host
+ * array of device pointers, segment_numels[n_segments] host element counts.
+ * Bit-exact copy.  Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ELIMIT (more than
+ * ZERO_MAX_SLICES segments), ZERO_ECUDA. */
+int zero3_gather_segments(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments,
+                          int dtype, void* layer_out, void* stream);
+
 /* The owner's share of the unit's gradient reduce-scatter:
  * grad_part[j] = round16(sum_r fp32(bucket_r[owner * P + j]) / world_size),
  * and the part's sum of squares / overflow added to *stats (accumulate as for

@@ -98,6 +98,7 @@ def lib():
                 "orc_ddp_step": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P, ctypes.c_int]
                                  + [ctypes.c_float] * 6 + [_I64, ctypes.c_double, _P]),
                 "orc_zero3_gather": (None, [_P, ctypes.c_int, _I64, _P]),
+                "orc_gather_segments": (None, [_P, _P, ctypes.c_int, _P]),
                 "orc_comm_volume": (ctypes.c_double, [ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
                 "orc_round_robin": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P]),
                 "orc_zero3_reduce": (None, [_P, ctypes.c_int, ctypes.c_int, _I64, ctypes.c_int, _P, _P, _P]),
@@ -283,6 +284,13 @@ def zero3_gather(parts) -> np.ndarray:
     part = parts[0].size
     out = np.empty(part * len(parts), np.uint16)
     lib().orc_zero3_gather(_ptr_array(parts), len(parts), part, _ptr(out))
+    return out
+
+
+def gather_segments(segs) -> np.ndarray:
+    lens = np.array([s.size for s in segs] or [0], np.int64)
+    out = np.empty(int(lens.sum()), np.uint16)
+    lib().orc_gather_segments(_ptr_array(segs), _ptr(lens), len(segs), _ptr(out) if out.size else None)
     return out
 
 

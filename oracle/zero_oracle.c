@@ -606,3 +606,16 @@ int orc_round_robin(int n, int ws, int64_t* order)
         for (int i = g; i < n; i += ws) order[k++] = i;
     return 0;
 }
+
+/* ======================================================================
+ * 9. ZeRO-3 owner broadcast ([paper] 5.3 and 7.2.2): each rank keeps a
+ * contiguous segment of the flat parameter vector; a layer is rebuilt from
+ * the pieces of the owners' segments it spans, laid end to end.
+ * ====================================================================== */
+
+void orc_gather_segments(const uint16_t* const* segs, const int64_t* lens, int n, uint16_t* out)
+{
+    int64_t o = 0;
+    for (int p = 0; p < n; p++)
+        for (int64_t j = 0; j < lens[p]; j++) out[o++] = segs[p][j];
+}

@@ -1,0 +1,61 @@
+"""CPU tests of bench.py's host logic: the max-over-ranks step time across
+two real processes (torch.distributed, gloo), and the fields of the JSON line
+the driver reads."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, port, out):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    import bench
+    got = bench.max_over_ranks(10.0 + 3.5 * rank, 2, "cpu")          # rank 1 is the slower one
+    dist.barrier()
+    open(f"{out}.{rank}", "w").write(repr(got))
+    dist.destroy_process_group()
+
+
+@pytest.mark.timeout(300)
+def test_max_over_two_ranks(tmp_path):
+    out = str(tmp_path / "r")
+    mp.start_processes(_worker, args=(_port(), out), nprocs=2, start_method="spawn", join=True)
+    assert [float(open(f"{out}.{r}").read()) for r in range(2)] == [13.5, 13.5]
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.max_over_ranks(4.25, 1, "cpu") == 4.25
+
+
+def test_line_fields():
+    import bench
+    roof = {"bound": "hbm", "achieved": 6500.0, "peak": 6792.1, "unit": "GB/s", "frac": 6500.0 / 6792.1,
+            "traffic": None}
+    cpu = {"value": 1.2e7, "unit": "elements/s", "cores": 1, "kind": "oracle", "sample": "x"}
+    e2e = {"value": 1e10, "unit": "elements/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 48}
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    line = bench.build_line(4, 100, 5, 10.0, 1_557_611_200, 8, {"workload": "w"}, roof, {}, cpu, e2e, clocks, 200)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+        assert k in line, k
+    assert line["value"] == pytest.approx(4 * 1_557_611_200 / 0.010)            # whole job: all ranks
+    assert line["scaling"] == "weak" and line["higher_is_better"] is True and line["n_gpus"] == 4
+    assert set(line["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
+    assert line["achieved_gbs_formula"] == pytest.approx(1_557_611_200 * 42 / 0.010 / 1e9)
+    assert line["config"]["workload"] == "w" and "model" not in line["config"]

@@ -134,3 +134,99 @@ def test_layer_pipeline_three_steps(Z):
         assert np.array_equal(t2u16(d_shards[me]), o_param)
         assert np.array_equal(master.cpu().numpy().view(np.uint32), o_master.view(np.uint32))
         assert np.array_equal(v.cpu().numpy().view(np.uint32), o_v.view(np.uint32))
+
+
+def test_gather_segments_is_exact(Z):
+    rng = np.random.default_rng(12)
+    for trial in range(12):
+        n = int(rng.integers(1, 6))
+        lens = [int(x) for x in rng.choice([0, 1, 7, 8, 1000, 4097, 54528], n)]
+        host = [rng.integers(0, 1 << 16, L + 3, dtype=np.uint64).astype(np.uint16) for L in lens]
+        shift = int(rng.integers(0, 2))                  # 2-byte offset: the unaligned path
+        dev = [dev16(h, 2)[shift:shift + L] for h, L in zip(host, lens)]
+        out = torch.zeros(max(1, sum(lens)), dtype=torch.bfloat16, device=DEV)
+        Z.zero3_gather_segments(dev, lens, Z.ZERO_BF16, out)
+        torch.cuda.synchronize()
+        ref = orc.gather_segments([h[shift:shift + L].copy() for h, L in zip(host, lens)])
+        assert np.array_equal(t2u16(out)[:sum(lens)], ref)
+
+
+def _pieces(plan_fn, inter_fn, units, nd):
+    """pieces[u] = [(rank, first element in the unit, first element in the rank's segment, length)]."""
+    p = plan_fn(units, nd)
+    offs, rnum = list(p["tensor_offsets"]), list(p["rank_numels"])
+    out = {u: [] for u in range(len(units))}
+    for r in range(nd):
+        for u, u0, s0, ln in inter_fn(offs, units, int(p["rank_offsets"][r]), int(rnum[r])):
+            out[int(u)].append((r, int(u0), int(s0), int(ln)))
+    return p, out
+
+
+def test_owner_broadcast_pipeline_three_steps(Z):
+    """ZeRO-3 with owner broadcast, rank 1 of 4 on a small Llama-shaped group:
+    each rank keeps one contiguous segment of the flat vector; every unit is
+    rebuilt forward and backward from the pieces of its owners' segments;
+    rank 1 reduces every rank's gradient over the pieces it owns and updates
+    its segment.  Bit-exact against the oracle."""
+    specs = W.llama_group(L=3, d=64, hq=4, hkv=2, hd=16, ff=160, V=300)
+    units = W.llama_units(specs, L=3)
+    nd, me, dt = 4, 1, 2
+    p, pieces = _pieces(Z.zero_plan, Z.zero_plan_intersections, units, nd)
+    po, pieces_o = _pieces(lambda u, n: orc.plan(u, n, 0), orc.plan_intersections, units, nd)
+    assert pieces == pieces_o and list(p["rank_offsets"]) == list(po["rank_offsets"])
+    P = p["padded_total"]
+    flat = torch.zeros(P, dtype=torch.bfloat16)
+    W.init_params_(flat, specs, W.generator(3, "cpu"))
+    flat = t2u16(flat)
+    segs_h = [flat[int(o):int(o) + int(n)].copy() for o, n in zip(p["rank_offsets"], p["rank_numels"])]
+    segs = [dev16(s, dt) for s in segs_h]
+    L = int(p["rank_numels"][me])
+    master = torch.from_numpy(orc.widen_16(segs_h[me], dt)).to(DEV)
+    m, v = torch.zeros(L, device=DEV), torch.zeros(L, device=DEV)
+    gseg = torch.zeros(L, dtype=torch.bfloat16, device=DEV)
+    layer = torch.empty(max(units), dtype=torch.bfloat16, device=DEV)
+    wsb = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    o_master, o_m, o_v = orc.widen_16(segs_h[me], dt), np.zeros(L, np.float32), np.zeros(L, np.float32)
+    o_param = segs_h[me].copy()
+    gens = [W.generator(5 + r, "cpu") for r in range(nd)]
+    h = hyper32()
+    for t in (1, 2, 3):
+        buckets = {}
+        for u, U in enumerate(units):
+            buckets[u] = [t2u16(W.fill_normal_(torch.zeros(U, dtype=torch.bfloat16), 5e-4, gens[r])) for r in range(nd)]
+        host_segs = list(segs_h)
+        host_segs[me] = t2u16(segs[me])
+        for u in list(range(len(units))) + list(reversed(range(len(units)))):
+            Z.zero3_gather_segments([segs[r][s0:s0 + ln] for r, u0, s0, ln in pieces[u]],
+                                    [ln for *_, ln in pieces[u]], dt, layer)
+            torch.cuda.synchronize()
+            ref = orc.gather_segments([host_segs[r][s0:s0 + ln] for r, u0, s0, ln in pieces[u]])
+            assert np.array_equal(t2u16(layer[:units[u]]), ref)
+        acc = orc.ExactAccumulator()
+        o_g = np.zeros(L, np.uint16)
+        first = True
+        for u in reversed(range(len(units))):
+            for r, u0, s0, ln in pieces[u]:
+                if r != me:
+                    continue
+                sh = [Z.shard(ln, u0, 0, None, None, None, grad_shard=gseg[s0:s0 + ln])]
+                Z.zero_shard_reduce([dev16(b, dt) for b in buckets[u]], dt, sh, not first, stats, wsb, wsb.numel())
+                first = False
+                o_g[s0:s0 + ln] = orc.reduce(buckets[u], dt, u0, ln)
+                orc.stats(o_g[s0:s0 + ln], dt, acc)
+        Z.zero_shard_apply([Z.shard(L, 0, 0, master, m, v, grad_shard=gseg)], dt, segs[me], dt,
+                           Z.hyper(step=t, **{k: h[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay",
+                                                                  "max_grad_norm")}),
+                           1.0, stats, 0.0, 0, wsb, wsb.numel(), res)
+        torch.cuda.synchronize()
+        k_mult, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+        orc.apply(o_g, dt, o_master, o_m, o_v, o_param, dt, k_mult,
+                  orc.make_scalars(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t))
+        r_ = Z.read_result(res)
+        assert r_.applied == 1 and r_.grad_norm == pytest.approx(norm, rel=1e-5)
+        assert np.array_equal(t2u16(gseg), o_g)
+        assert np.array_equal(t2u16(segs[me]), o_param)
+        assert np.array_equal(master.cpu().numpy().view(np.uint32), o_master.view(np.uint32))
+        assert np.array_equal(m.cpu().numpy().view(np.uint32), o_m.view(np.uint32))

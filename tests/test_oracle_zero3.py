@@ -53,3 +53,35 @@ def test_bucket_reduce_statistics(orc):
     _, o0 = orc.zero3_reduce(bad, 0, part, dt, orc.ExactAccumulator())
     _, o1 = orc.zero3_reduce(bad, 1, part, dt, orc.ExactAccumulator())
     assert (o0, o1) == (0, 1)
+
+
+def test_segment_gather_inverts_any_cut(orc):
+    """Owner broadcast ([paper] 5.3): a layer rebuilt from the pieces of the
+    owners' contiguous segments it spans is the layer."""
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        layer = rng.integers(0, 1 << 16, int(rng.integers(0, 3000)), dtype=np.uint64).astype(np.uint16)
+        cuts = np.sort(rng.integers(0, layer.size + 1, int(rng.integers(0, 5))))
+        pieces = [layer[a:b].copy() for a, b in zip(np.concatenate([[0], cuts]), np.concatenate([cuts, [layer.size]]))]
+        assert np.array_equal(orc.gather_segments(pieces), layer)
+
+
+def test_broadcast_pieces_cover_each_unit_once(orc):
+    """The pieces of a unit owned by each rank (the partition's intersections
+    with the unit) cover the unit exactly once, in order."""
+    units = [300, 1000, 48, 5000, 7]
+    for nd in (1, 2, 4, 7):
+        p = orc.plan(units, nd, 0)
+        seen = {u: [] for u in range(len(units))}
+        for r in range(nd):
+            for u, u0, s0, ln in orc.plan_intersections(p["tensor_offsets"], units, int(p["rank_offsets"][r]),
+                                                         int(p["rank_numels"][r])):
+                seen[int(u)].append((int(u0), int(ln), r))
+        for u, rows in seen.items():
+            rows.sort()
+            pos = 0
+            for u0, ln, r in rows:
+                assert u0 == pos
+                pos += ln
+            assert pos == units[u]
+            assert [r for _, _, r in rows] == sorted(r for _, _, r in rows)     # owners in rank order

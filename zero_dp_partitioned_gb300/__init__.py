@@ -73,6 +73,7 @@ _SIGS = {
     "zero_shard_apply": (_I, [_P, _I, _I, _P, _I, _P, ctypes.c_float, _P, ctypes.c_double, _I, _P, ctypes.c_size_t,
                               _P, _P]),
     "zero3_gather_layer": (_I, [_P, _I, _I64, _I, _P, _P]),
+    "zero3_gather_segments": (_I, [_P, _P, _I, _I, _P, _P]),
     "zero3_reduce_bucket": (_I, [_P, _I, _I, _I64, _I, _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "zero_shard_step_noalloc": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
@@ -214,6 +215,12 @@ def zero_shard_apply(shards, grad_dtype, flat_param, param_dtype, hyper, loss_sc
 def zero3_gather_layer(part_ptrs, unit_numel, dtype, layer_out, stream=None):
     _check(lib.zero3_gather_layer(_ptrs(part_ptrs), len(part_ptrs), unit_numel, dtype, _ptr(layer_out),
                                   _stream(stream)))
+
+
+def zero3_gather_segments(segment_ptrs, segment_numels, dtype, layer_out, stream=None):
+    n = len(segment_ptrs)
+    lens = (ctypes.c_int64 * max(1, n))(*segment_numels)
+    _check(lib.zero3_gather_segments(_ptrs(segment_ptrs), lens, n, dtype, _ptr(layer_out), _stream(stream)))
 
 
 def zero3_reduce_bucket(bucket_ptrs, owner, unit_numel, grad_dtype, grad_part, accumulate, stats, workspace,

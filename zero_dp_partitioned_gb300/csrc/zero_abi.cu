@@ -457,6 +457,41 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
     return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));
 }
 
+// Copy n segments end to end into out (the layer buffer).
+static int gather_segments(const void* const* src, const int64_t* len, int n, int dtype, void* out, void* stream) {
+    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (n < 1) return fail(ZERO_EINVAL, "no segments");
+    if (n > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "more than ZERO_MAX_SLICES segments");
+    if (!src || !len || !out) return fail(ZERO_EINVAL, "NULL pointer");
+    if (!aligned(out, 2)) return fail(ZERO_EALIGN, "layer_out not 2-byte aligned");
+    GatherArgs g;
+    std::memset(&g, 0, sizeof g);
+    g.n = n;
+    g.out = out;
+    int64_t off = 0;
+    bool v8 = aligned(out, 16);
+    for (int p = 0; p < n; ++p) {
+        if (len[p] < 0) return fail(ZERO_EINVAL, "negative segment length");
+        if (len[p] > 0 && !src[p]) return fail(ZERO_EINVAL, "a segment pointer is NULL");
+        if (!aligned(src[p], 2)) return fail(ZERO_EALIGN, "segment pointer not 2-byte aligned");
+        g.src[p] = src[p];
+        g.len[p] = len[p];
+        g.dst_off[p] = off;
+        v8 = v8 && aligned(src[p], 16) && (off % 8 == 0);
+        off += len[p];
+    }
+    if (off == 0) return ZERO_OK;
+    const int vec = v8 ? 8 : 1;
+    const int64_t tile = (int64_t)TILE_THREADS * vec * 2;
+    int64_t t = 0;
+    for (int p = 0; p < n; ++p) {
+        g.tile_begin[p] = t;
+        t += (g.len[p] + tile - 1) / tile;
+    }
+    g.tile_begin[n] = t;
+    return launch_gather(g, vec, static_cast<cudaStream_t>(stream));
+}
+
 int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t unit_numel, int dtype, void* layer_out,
                        void* stream) {
     if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "unknown dtype");
@@ -466,23 +501,14 @@ int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t uni
         return fail(ZERO_EINVAL, "unit_numel must be >= 0 and divisible by world_size");
     if (unit_numel == 0) return ZERO_OK;
     if (!part_ptrs || !layer_out) return fail(ZERO_EINVAL, "NULL pointer");
-    if (!aligned(layer_out, 2)) return fail(ZERO_EALIGN, "layer_out not 2-byte aligned");
-    GatherArgs g;
-    std::memset(&g, 0, sizeof g);
-    g.world_size = world_size;
-    g.part_numel = unit_numel / world_size;
-    g.out = layer_out;
-    bool v8 = aligned(layer_out, 16) && (g.part_numel % 8 == 0);
-    for (int r = 0; r < world_size; ++r) {
-        if (!part_ptrs[r]) return fail(ZERO_EINVAL, "a part pointer is NULL");
-        if (!aligned(part_ptrs[r], 2)) return fail(ZERO_EALIGN, "part pointer not 2-byte aligned");
-        v8 = v8 && aligned(part_ptrs[r], 16);
-        g.parts[r] = part_ptrs[r];
-    }
-    const int vec = v8 ? 8 : 1;
-    const int64_t tile = (int64_t)TILE_THREADS * vec * 2;
-    g.tiles_per_part = (g.part_numel + tile - 1) / tile;
-    return launch_gather(g, vec, static_cast<cudaStream_t>(stream));
+    int64_t len[ZERO_MAX_SLICES];
+    for (int r = 0; r < world_size; ++r) len[r] = unit_numel / world_size;
+    return gather_segments(part_ptrs, len, world_size, dtype, layer_out, stream);
+}
+
+int zero3_gather_segments(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments,
+                          int dtype, void* layer_out, void* stream) {
+    return gather_segments(segment_ptrs, segment_numels, n_segments, dtype, layer_out, stream);
 }
 
 int zero3_reduce_bucket(const void* const* bucket_ptrs, int world_size, int owner, int64_t unit_numel, int grad_dtype,

@@ -599,38 +599,44 @@ k_apply(const __grid_constant__ StepArgs a) {
 }
 
 // ---------------------------------------------------------------- K3: ZeRO-3 layer gather
+// out[dst_off[p] + j] = src[p][j] for j < len[p]: the per-layer all-gather
+// (equal parts, one per rank) and the owner broadcast (the pieces of the
+// owners' contiguous segments a layer spans) are both this copy.
 struct GatherArgs {
-    const void* parts[ZERO_MAX_SLICES];
-    int world_size;
-    int64_t part_numel;       // elements per part
-    int64_t tiles_per_part;
+    const void* src[ZERO_MAX_SLICES];
+    int64_t len[ZERO_MAX_SLICES];              // elements of each segment
+    int64_t dst_off[ZERO_MAX_SLICES];          // where each segment starts in out
+    int64_t tile_begin[ZERO_MAX_SLICES + 1];   // first tile of each segment; [n] = tile count
+    int n;
     void* out;
 };
 
 template <int VEC>
 __global__ void __launch_bounds__(TILE_THREADS) k_gather(const __grid_constant__ GatherArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC * 2;   // two vectors per thread per tile
-    const int64_t n_tiles = a.tiles_per_part * a.world_size;
+    const int64_t n_tiles = a.tile_begin[a.n];
     uint16_t* O = static_cast<uint16_t*>(a.out);
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int r = (int)(tile / a.tiles_per_part);
-        const int64_t t = tile - (int64_t)r * a.tiles_per_part;
-        const uint16_t* src = static_cast<const uint16_t*>(a.parts[r]);
-        uint16_t* dst = O + (int64_t)r * a.part_numel;
+        int p = 0;
+        while (p + 1 < a.n && a.tile_begin[p + 1] <= tile) ++p;
+        const int64_t t = tile - a.tile_begin[p];
+        const int64_t L = a.len[p];
+        const uint16_t* src = static_cast<const uint16_t*>(a.src[p]);
+        uint16_t* dst = O + a.dst_off[p];
         const int64_t j0 = t * TILE + (int64_t)threadIdx.x * VEC;
         const int64_t j1 = j0 + (int64_t)TILE_THREADS * VEC;
         if (VEC == 8) {
-            const bool f0 = j0 + 8 <= a.part_numel, f1 = j1 + 8 <= a.part_numel;
+            const bool f0 = j0 + 8 <= L, f1 = j1 + 8 <= L;
             uint4 w0, w1;
             if (f0) w0 = ld_stream(src + j0);
             if (f1) w1 = ld_stream(src + j1);
             if (f0) __stcs(reinterpret_cast<uint4*>(dst + j0), w0);
-            else for (int64_t i = j0; i < a.part_numel; ++i) dst[i] = src[i];
+            else for (int64_t i = j0; i < L; ++i) dst[i] = src[i];
             if (f1) __stcs(reinterpret_cast<uint4*>(dst + j1), w1);
-            else for (int64_t i = j1; i < a.part_numel; ++i) dst[i] = src[i];
+            else for (int64_t i = j1; i < L; ++i) dst[i] = src[i];
         } else {
-            if (j0 < a.part_numel) dst[j0] = src[j0];
-            if (j1 < a.part_numel) dst[j1] = src[j1];
+            if (j0 < L) dst[j0] = src[j0];
+            if (j1 < L) dst[j1] = src[j1];
         }
     }
 }

@@ -49,7 +49,7 @@ int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s) {
 
 int launch_gather(const GatherArgs& a, int vec, cudaStream_t s) {
     const void* f = vec == 8 ? (const void*)k_gather<8> : (const void*)k_gather<1>;
-    const int grid = grid_for(f, a.tiles_per_part * a.world_size, BPS_GATHER);
+    const int grid = grid_for(f, a.tile_begin[a.n], BPS_GATHER);
     void* args[] = {const_cast<GatherArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "gather launch");
 }
