@@ -199,13 +199,32 @@ def _finish_step(Z, torch, res, res_h, st):
     return r
 
 
+E2E_SOURCE = {"mode": None}
+
+
 def _pin_copies(torch, bufs, e2e):
-    need = sum(b.numel() * b.element_size() for b in bufs)
+    """Pinned host copies of a step's input buffers for the end-to-end run.
+    Every rank of the job pins at the same time, so the check is on the job's
+    whole footprint: with room for all ranks' distinct buffers (and margin),
+    each buffer gets its own pinned copy; otherwise one pinned buffer of the
+    largest size is the host source of every device buffer -- the same bytes
+    cross the link each step -- and the JSON line says so."""
     if not e2e:
         return None
-    if mem_available_bytes() > 2 * need + (16 << 30):
+    world = dist_env()[1]
+    need = sum(b.numel() * b.element_size() for b in bufs)
+    one = max(b.numel() * b.element_size() for b in bufs)
+    avail = mem_available_bytes()
+    if avail > 1.25 * world * need + (32 << 30):
         log(f"[bench] pinning {need / 1e9:.1f} GB of host gradients for the end-to-end run")
+        E2E_SOURCE["mode"] = "a pinned host copy of every input buffer"
         return [torch.empty(b.shape, dtype=b.dtype, pin_memory=True).copy_(b) for b in bufs]
+    if avail > 1.25 * world * one + (32 << 30):
+        log(f"[bench] pinning one {one / 1e9:.1f} GB host buffer as the source of every input buffer")
+        E2E_SOURCE["mode"] = "one pinned host buffer copied into every input buffer (host memory too small for all)"
+        src = torch.empty(max(b.numel() for b in bufs), dtype=bufs[0].dtype, pin_memory=True)
+        src[:bufs[0].numel()].copy_(bufs[0])
+        return [src[:b.numel()] for b in bufs]
     log("[bench] not enough host memory for the end-to-end run")
     return None
 
@@ -673,7 +692,8 @@ def main():
         ms_e2e = max_over_ranks(s2.elapsed_time(e2) / args.e2e_steps, world, dev)
         e2e = {"value": world * wl["elements"] / (ms_e2e / 1e3), "unit": "elements/s",
                "h2d_bytes_per_step": wl["h2d"], "d2h_bytes_per_step": wl["d2h"], "ms_per_step": ms_e2e,
-               "steps": args.e2e_steps}
+               "steps": args.e2e_steps, "source": E2E_SOURCE["mode"],
+               "note": "bound by the host link: ~211 GB/s at best on this host, shared with other tenants"}
 
     peak, peak_src = measured_peaks()
     per_kernel = {}
