@@ -349,7 +349,7 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
-    extra = W.other_ranks_sumsq(wl, n)
+    extra = W.other_ranks_sumsq(wl)
     pinned = _pin_copies(torch, slices, e2e)
 
     def step(from_host=False):

@@ -48,7 +48,7 @@ def dev32(a: np.ndarray):
     return torch.from_numpy(a.copy()).to(DEV)
 
 
-class GpuRun:
+class DeviceRun:
     """Device copy of a problem: per-rank grads, flat params, per-shard state (A and optionally B)."""
 
     def __init__(self, Z, p, flat, dt, ranks, pingpong, want_grad=True, state_pad=0, param_pad=0):
@@ -136,7 +136,7 @@ def run_both(Z, numels, nd, dt, mode, seed, h, S, pingpong, steps=3, inject=None
     if inject:
         inject(grads)
     ranks = list(range(nd)) if ranks is None else ranks
-    run = GpuRun(Z, p, flat, dt, ranks, pingpong, state_pad=state_pad, param_pad=param_pad)
+    run = DeviceRun(Z, p, flat, dt, ranks, pingpong, state_pad=state_pad, param_pad=param_pad)
     osh = oracle_shards(p, flat, dt, ranks)
     oflat = flat.copy()
     t, Sg, So = 1, S, S
@@ -254,7 +254,7 @@ def test_rank_local_view_with_other_ranks_statistics(Z):
     o, n = int(p["rank_offsets"][r]), int(p["rank_numels"][r])
     staged = [[g[o:o + n].copy() for g in step] for step in grads]   # the 4 slices staged for rank 1
     h = hyper32(max_grad_norm=0.02)
-    run = GpuRun(Z, p, flat, dt, [r], pingpong=False)
+    run = DeviceRun(Z, p, flat, dt, [r], pingpong=False)
     osh = oracle_shards(p, flat, dt, [r])
     osh[0]["grad_off"] = 0
     oflat = flat.copy()
@@ -276,7 +276,7 @@ def test_reduce_and_apply_separately_accumulate(Z):
     numels = [40000, 333]
     nd, dt = 3, 1
     p, flat, grads = make_problem(numels, nd, dt, 0, 13, loss_scale=64.0, steps=1)
-    run = GpuRun(Z, p, flat, dt, list(range(nd)), pingpong=False)
+    run = DeviceRun(Z, p, flat, dt, list(range(nd)), pingpong=False)
     slices = [dev16(g, dt) for g in grads[0]]
     sh = run.shards()
     stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
@@ -303,7 +303,7 @@ def test_deterministic(Z):
     p, flat, grads = make_problem(numels, 8, 2, 0, 14, steps=1)
     outs = []
     for _ in range(2):
-        run = GpuRun(Z, p, flat, 2, list(range(8)), pingpong=True)
+        run = DeviceRun(Z, p, flat, 2, list(range(8)), pingpong=True)
         r = run.step(grads[0], hyper32(), 1, 1.0)
         outs.append((r.sumsq, t2u16(run.flat)))
     assert outs[0][0] == outs[1][0] and np.array_equal(outs[0][1], outs[1][1])
@@ -322,7 +322,7 @@ def _staged_rank_local(Z, numel, nd, dt, param_off, clip, steps=3, seed=21, S=1.
     flat[:] = t2u16(ft)
     gens = [W.generator(seed + 1 + j, "cpu") for j in range(nd)]
     h = hyper32(max_grad_norm=clip)
-    run = GpuRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
+    run = DeviceRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
     osh = oracle_shards(p, flat, dt, [0])
     osh[0]["grad_off"] = 0
     oflat = flat.copy()
@@ -362,7 +362,7 @@ def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch):
     staged = [t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 1e-3, W.generator(6 + j, "cpu")))
               for j in range(nd)]
     for clip in (0.0, 0.5):                      # fused pass, then the apply pass
-        run = GpuRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
+        run = DeviceRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
         h = hyper32(max_grad_norm=clip)
         before = [x.clone() for x in run.state[0]["A"]]
         monkeypatch.setenv("ZERO_GB300_SPIN_LIMIT", "0")
@@ -398,7 +398,7 @@ def test_stage1_full_allreduce_then_shard_update(Z):
     nd, dt = 4, 2
     p, flat, grads = make_problem(numels, nd, dt, 0, 41, steps=2)
     P = p["padded_total"]
-    run = GpuRun(Z, p, flat, dt, list(range(nd)), pingpong=False, want_grad=False)
+    run = DeviceRun(Z, p, flat, dt, list(range(nd)), pingpong=False, want_grad=False)
     avg = torch.empty(P, dtype=torch.bfloat16, device=DEV)
     for s_, o, n in zip(run.state, p["rank_offsets"], p["rank_numels"]):
         s_["g"] = avg[int(o):int(o) + int(n)]

@@ -185,7 +185,7 @@ def test_llama3_8b_rank1_clipped(Z):
     gshard = torch.empty(n, dtype=torch.bfloat16, device=DEV)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
     res = torch.zeros(48, dtype=torch.uint8, device=DEV)
-    extra = W.other_ranks_sumsq(wl, n)
+    extra = W.other_ranks_sumsq(wl)
     idx = sample_idx(n, 3)
     ti = torch.from_numpy(idx).to(DEV)
     samp = Sampled(idx, u16(flat[o + ti]), dt)
