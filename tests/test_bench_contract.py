@@ -59,3 +59,20 @@ def test_line_fields():
     assert set(line["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
     assert line["achieved_gbs_formula"] == pytest.approx(1_557_611_200 * 42 / 0.010 / 1e9)
     assert line["config"]["workload"] == "w" and "model" not in line["config"]
+
+
+def test_every_input_helper_bench_and_tests_use_exists():
+    """bench.py and the GPU tests build their inputs from workloads.py; a
+    helper they name but the module lacks would only fail on a GPU."""
+    import ast
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    files = [os.path.join(ROOT, "bench.py")] + [os.path.join(ROOT, "tests", f)
+                                                for f in os.listdir(os.path.join(ROOT, "tests")) if f.endswith(".py")]
+    missing = set()
+    for f in files:
+        for node in ast.walk(ast.parse(open(f).read())):
+            if isinstance(node, ast.Attribute) and isinstance(node.value, ast.Name) and node.value.id == "W":
+                if not hasattr(W, node.attr):
+                    missing.add(f"{os.path.basename(f)}: W.{node.attr}")
+    assert not missing, sorted(missing)

@@ -187,3 +187,37 @@ def other_ranks_sumsq(wl: Workload) -> float:
     give (Llama-3-8B rank 1: three shards of 2.0e9 elements of averaged
     N(0, 5e-4^2) gradients)."""
     return {"llama3-8b-nd4-r1": 376.42}.get(wl.name, 0.0)
+
+
+# ------------------------------------------------------------------ device-side input sets
+class GradStream:
+    """Seeded gradient draws that continue across steps: one generator per
+    rank (or staged slice), seeds as listed with each workload."""
+
+    def __init__(self, seeds, device):
+        self.gens = [generator(s, device) for s in seeds]
+
+    def draw_flat(self, outs, specs, std_of, scale=1.0):
+        """Full flat gradients (all-ranks view): rank r's buffer from generator r."""
+        for g, o in zip(self.gens, outs):
+            fill_grad_(o, specs, g, std_of, scale)
+        return outs
+
+    def draw_plain(self, outs, std, scale=1.0):
+        """Staged slices (rank-local view): slice j ~ N(0, std) * scale from generator j."""
+        for g, o in zip(self.gens, outs):
+            fill_normal_(o, std, g, scale)
+        return outs
+
+
+def zero_every_100th_(t: torch.Tensor):
+    """Exact zeros at every element whose index is a multiple of 100 (the 7.5B workload's slice 0)."""
+    t[::100] = 0
+    return t
+
+
+def flat_params(specs, total: int, dtype, seed: int, device):
+    """The group's 16-bit parameters laid out flat over `total` elements (the
+    plan's padded length); padding is 0."""
+    flat = torch.zeros(total, dtype=dtype, device=device)
+    return init_params_(flat, specs, generator(seed, device))
