@@ -430,3 +430,99 @@ def test_unaligned_shard_heads(Z, dt, total, nd, monkeypatch):
     S = 512.0 if dt == 1 else 1.0
     run_both(Z, [total], nd, dt, 0, total + nd, hyper32(), S, True, steps=2)
     run_both(Z, [total], nd, dt, 0, total + nd, hyper32(max_grad_norm=0.01), S, False, steps=2, grad_std=1e-2)
+
+
+@pytest.mark.parametrize("gdt,pdt", [(2, 1), (1, 2)])
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_mixed_gradient_and_parameter_dtypes(Z, gdt, pdt, clip):
+    """bf16 gradients with fp16 parameters and the reverse: the reduce rounds
+    to the gradient dtype, the store to the parameter dtype."""
+    numels = [20000, 555]
+    nd = 4
+    p = orc.plan(numels, nd, 0)
+    P = p["padded_total"]
+    specs = [W.ParamSpec(f"t{i}", n) for i, n in enumerate(numels)]
+    ft = torch.zeros(P, dtype=TDT[pdt])
+    W.init_params_(ft, specs, W.generator(7, "cpu"))
+    flat = t2u16(ft)
+    gens = [W.generator(8 + r, "cpu") for r in range(nd)]
+    S = 64.0 if gdt == 1 else 1.0
+    grads = [[t2u16(W.fill_grad_(torch.zeros(P, dtype=TDT[gdt]), specs, gens[r], lambda s: 1e-2, S))
+              for r in range(nd)] for _ in range(2)]
+    h = hyper32(max_grad_norm=clip)
+    dflat = dev16(flat, pdt)
+    st = []
+    for o, n in zip(p["rank_offsets"], p["rank_numels"]):
+        o, n = int(o), int(n)
+        A = [dflat[o:o + n].float(), torch.zeros(n, device=DEV), torch.zeros(n, device=DEV)]
+        B = [torch.empty(n, device=DEV) for _ in range(3)] if clip == 0.0 else A
+        st.append(dict(o=o, n=n, A=A, B=B, g=torch.empty(n, dtype=TDT[gdt], device=DEV)))
+    osh = [dict(numel=s_["n"], grad_off=s_["o"], param_off=s_["o"], master=orc.widen_16(flat[s_["o"]:s_["o"] + s_["n"]], pdt),
+                m=np.zeros(s_["n"], np.float32), v=np.zeros(s_["n"], np.float32)) for s_ in st]
+    oflat = flat.copy()
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    for t in (1, 2):
+        sh = [Z.shard(s_["n"], s_["o"], s_["o"], *s_["A"], *s_["B"], s_["g"]) for s_ in st]
+        Z.zero_shard_step([dev16(g, gdt) for g in grads[t - 1]], gdt, sh, dflat, pdt,
+                          Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], h["max_grad_norm"], t),
+                          S, 0.0, 0, ws, ws.numel(), res)
+        torch.cuda.synchronize()
+        rg = Z.read_result(res)
+        prev = [(o["master"].copy(), o["m"].copy()) for o in osh]
+        ro, red = orc.zero_step(grads[t - 1], gdt, osh, oflat, pdt, h, t, S, want_grad=True)
+        assert (rg.overflow, rg.applied) == (ro.overflow, ro.applied) == (0, 1)
+        if clip == 0.0:
+            for s_ in st:
+                s_["A"], s_["B"] = s_["B"], s_["A"]
+        got_flat = t2u16(dflat)
+        if clip == 0.0:
+            assert np.array_equal(got_flat, oflat)
+        else:
+            assert np.abs(got_flat.astype(np.int32) - oflat.astype(np.int32)).max() <= 1
+        for s_, o, pv, rd in zip(st, osh, prev, red):
+            if clip == 0.0:
+                assert np.array_equal(s_["A"][0].cpu().numpy().view(np.uint32), o["master"].view(np.uint32))
+            else:
+                assert np.array_equal(t2u16(s_["g"]), rd)
+                th_prev = np.abs(pv[0].astype(np.float64))
+                sc = np.maximum(th_prev + np.abs(th_prev - o["master"]), np.abs(o["master"]))
+                assert np.all(np.abs(s_["A"][0].cpu().numpy().astype(np.float64) - o["master"]) <= 2e-6 * np.maximum(sc, 1e-30))
+
+
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_step_captured_in_a_cuda_graph(Z, clip):
+    """The step enqueues only kernels on the caller's stream (no allocation,
+    no synchronisation), so a call can be captured into a CUDA graph and
+    replayed: the replay must equal the same call made eagerly."""
+    numels = [70000, 123]
+    nd, dt = 3, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 51, steps=1)
+    h = hyper32(max_grad_norm=clip)
+    outs = []
+    for mode in ("eager", "graph"):
+        run = DeviceRun(Z, p, flat, dt, list(range(nd)), pingpong=(clip == 0.0))
+        slices = [dev16(g, dt) for g in grads[0]]
+        hy = Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], h["max_grad_norm"], 1)
+        sh = run.shards()
+        if mode == "eager":
+            Z.zero_shard_step(slices, dt, sh, run.flat, dt, hy, 1.0, 0.0, 0, run.ws, run.ws.numel(), run.res)
+        else:
+            # one eager call on scratch copies first, so the library's one-time per-kernel set-up is done
+            warm = DeviceRun(Z, p, flat, dt, list(range(nd)), pingpong=(clip == 0.0))
+            Z.zero_shard_step(slices, dt, warm.shards(), warm.flat, dt, hy, 1.0, 0.0, 0, warm.ws, warm.ws.numel(),
+                              warm.res)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            with torch.cuda.graph(g, stream=s):
+                Z.zero_shard_step(slices, dt, sh, run.flat, dt, hy, 1.0, 0.0, 0, run.ws, run.ws.numel(), run.res)
+            g.replay()
+        torch.cuda.synchronize()
+        r = Z.read_result(run.res)
+        state = run.state[0]["B"] if clip == 0.0 else run.state[0]["A"]
+        outs.append((t2u16(run.flat), [x.cpu().numpy() for x in state], r.as_dict()))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert outs[0][2] == outs[1][2]
