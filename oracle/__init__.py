@@ -86,6 +86,9 @@ def lib():
                 "orc_plan": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _P]),
                 "orc_plan_intersections": (ctypes.c_int, [_P, _P, ctypes.c_int, _I64, _I64, _P]),
                 "orc_mem_model": (ctypes.c_double, [ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int]),
+                "orc_mem_model_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                      ctypes.POINTER(ctypes.c_double)]),
                 "orc_make_scalars": (None, [ctypes.c_float] * 5 + [_I64, _P]),
                 "orc_grad_multiplier": (ctypes.c_float, [ctypes.c_double] * 3 + [_P, _P]),
                 "orc_reduce": (None, [_P, ctypes.c_int, ctypes.c_int, _I64, _I64, _P]),
@@ -187,6 +190,15 @@ def plan_intersections(tensor_offsets, numels, rank_offset: int, rank_numel: int
 
 def mem_model(psi: float, K: float, nd: int, stage: int) -> float:
     return lib().orc_mem_model(psi, K, nd, stage)
+
+
+def mem_model_plan(flat_numel: int, shard_numel: int, K: float, stage: int, sets: int = 1, fp32_temp: int = 0,
+                   b16_temp: int = 0):
+    """Plan-exact bytes of one rank: dict of params, grads, states, temp, total (None on a bad argument)."""
+    out = (ctypes.c_double * 5)()
+    if lib().orc_mem_model_plan(flat_numel, shard_numel, K, stage, sets, fp32_temp, b16_temp, out) != 0:
+        return None
+    return dict(zip(("params", "grads", "states", "temp", "total"), list(out)))
 
 
 def comm_volume(psi: float, nd: int, stage: int, ring: bool = False) -> float:

@@ -323,6 +323,35 @@ double orc_mem_model(double psi, double K, int nd, int stage)
     }
 }
 
+/* Plan-exact model states of one rank, with temporaries.  The stage
+ * formulas above take a rank's share as Psi / N_d; here each term takes the
+ * plan's own sizes: F = elements of a 16-bit flat buffer the stage keeps
+ * whole (the padded total; Psi for stage 0), n = the rank's shard.  Which
+ * buffers a stage keeps whole and which it partitions follows [paper]
+ * 5.1-5.3: P_os partitions the optimizer states, P_os+g the gradients too,
+ * P_os+g+p the parameters too.  `sets` copies of the optimizer state are
+ * held (2 when the state is double-buffered).  The temporaries are the
+ * fp32 fused flat buffer of [paper] 3.2 and 6.2 (4 bytes an element) and
+ * 16-bit buffers (2 bytes an element).
+ * out[0] parameters, out[1] gradients, out[2] optimizer states,
+ * out[3] temporaries, out[4] their sum.  Returns 0, or -1 on a bad argument. */
+int orc_mem_model_plan(int64_t F, int64_t n, double K, int stage, int sets,
+                       int64_t fp32_temp, int64_t b16_temp, double* out)
+{
+    if (F < 0 || n < 0 || K < 0.0 || stage < 0 || stage > 3 || sets < 1 ||
+        fp32_temp < 0 || b16_temp < 0)
+        return -1;
+    const double params_whole = (stage <= 2) ? (double)F : (double)n;
+    const double grads_whole = (stage <= 1) ? (double)F : (double)n;
+    const double states_of = (stage == 0) ? (double)F : (double)n;
+    out[0] = 2.0 * params_whole;
+    out[1] = 2.0 * grads_whole;
+    out[2] = K * states_of * (double)sets;
+    out[3] = 4.0 * (double)fp32_temp + 2.0 * (double)b16_temp;
+    out[4] = out[0] + out[1] + out[2] + out[3];
+    return 0;
+}
+
 /* ======================================================================
  * 5. The step.
  * ====================================================================== */
