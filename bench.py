@@ -37,6 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "shard AdamW-step elements/s; achieved HBM GB/s vs GB300 roofline"
+NOMINAL_HBM_GBS = 8000.0      # HBM3e, nominal
 
 
 def log(*a):
@@ -576,10 +577,12 @@ WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_al
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def time_oracle(W, wl_fn, n_per_shard, steps):
+def time_oracle(sample, n_per_shard, steps):
+    """The oracle as it stands, in this process: each step's wall time."""
     import numpy as np
     import oracle
-    nd, grads, flat, h = wl_fn(n_per_shard)
+    nd, grads, flat, h = sample
+    flat = flat.copy()
     shards = [dict(numel=n_per_shard, grad_off=r * n_per_shard, param_off=r * n_per_shard,
                    master=oracle.widen_16(flat[r * n_per_shard:(r + 1) * n_per_shard], 2),
                    m=np.zeros(n_per_shard, np.float32), v=np.zeros(n_per_shard, np.float32)) for r in range(nd)]
@@ -590,6 +593,85 @@ def time_oracle(W, wl_fn, n_per_shard, steps):
         oracle.zero_step(grads, 2, shards, flat, 2, hh, t, 1.0)
         times.append(time.perf_counter() - t0)
     return nd * n_per_shard, times
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+_BARRIER = None
+
+
+def _oracle_worker_init(barrier):
+    global _BARRIER
+    _BARRIER = barrier
+
+
+def _oracle_chunk(task):
+    """One process's share of the all-cores oracle timing: the oracle's step on
+    elements [lo, hi) of every shard, repacked as a problem of its own (the
+    elements' updates are independent without clipping).  Every step starts
+    behind a barrier across the processes; returns each step's (start, end)
+    and, if asked, the parameters after the last step."""
+    import numpy as np
+    import oracle
+    nd, c, grads, flat, hyper, steps, want_params = task
+    shards = [dict(numel=c, grad_off=r * c, param_off=r * c, master=oracle.widen_16(flat[r * c:(r + 1) * c], 2),
+                   m=np.zeros(c, np.float32), v=np.zeros(c, np.float32)) for r in range(nd)]
+    hh = dict(hyper, max_grad_norm=0.0)
+    marks = []
+    for t in range(1, steps + 1):
+        _BARRIER.wait(timeout=600)
+        t0 = time.perf_counter()
+        oracle.zero_step(grads, 2, shards, flat, 2, hh, t, 1.0)
+        marks.append((t0, time.perf_counter()))
+    return marks, (flat if want_params else None)
+
+
+def time_oracle_parallel(sample, n_per_shard, steps, procs, want_params=False):
+    """The oracle as it stands, run by `procs` spawned processes at once, each
+    on an equal share of every shard's elements.  Returns the elements per step,
+    each step's wall time (last end minus first start over the processes) and,
+    if asked, the parameters after the last step reassembled in flat order."""
+    import multiprocessing as mp
+    import numpy as np
+    nd, grads, flat, h = sample
+    n = n_per_shard
+    bounds = [n * w // procs for w in range(procs + 1)]
+    tasks = []
+    for w in range(procs):
+        lo, hi = bounds[w], bounds[w + 1]
+        pick = lambda a: np.concatenate([a[r * n + lo:r * n + hi] for r in range(nd)])
+        tasks.append((nd, hi - lo, [pick(g) for g in grads], pick(flat), h, steps, want_params))
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    with ctx.Pool(procs, initializer=_oracle_worker_init, initargs=(barrier,)) as pool:
+        res = pool.map(_oracle_chunk, tasks, chunksize=1)
+    walls = [max(r[0][s][1] for r in res) - min(r[0][s][0] for r in res) for s in range(steps)]
+    params = None
+    if want_params:
+        params = np.empty_like(flat)
+        for w, (_, fw) in enumerate(res):
+            lo, hi = bounds[w], bounds[w + 1]
+            c = hi - lo
+            for r in range(nd):
+                params[r * n + lo:r * n + hi] = fw[r * c:(r + 1) * c]
+    return nd * n, walls, params
 
 
 # ------------------------------------------------------------------ multi-rank timing and the output line
@@ -710,13 +792,14 @@ def main():
                 "frac": dk["achieved_gbs"] / peak, "traffic": ncu_traffic(wl["name"], dom),
                 "peak_source": peak_src, "kernel": f"{dom} [{wl['config']['update_kernel']}]",
                 "kernel_ms_per_launch": dk["ms_per_launch"],
-                "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"]}
+                "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"],
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": dk["achieved_gbs"] / NOMINAL_HBM_GBS}
+    if roofline["traffic"] is not None:
+        dram = roofline["traffic"] / (dk["ms_per_launch"] / 1e3) / 1e9
+        roofline.update(dram_gbs=dram, dram_frac=dram / peak, dram_frac_of_nominal=dram / NOMINAL_HBM_GBS)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and wl["sample_for_cpu"]:
-        n, times = time_oracle(W, wl["sample_for_cpu"], 1 << 22, 2)
-        cpu = {"value": n / statistics.mean(times), "unit": "elements/s", "cores": 1, "kind": "oracle",
-               "sample": f"the first {1 << 22} elements of each of the {wl['nd']} shards "
-                         f"({n} elements), 2 steps, single-threaded plain C oracle"}
+        cpu = cpu_baseline(wl)
     if rank == 0:
         line = build_line(world, args.steps, max(3, args.warmup), ms, wl["elements"], wl["nd"], wl["config"],
                           roofline, per_kernel, cpu, e2e, clocks, wl["launches_per_step"] * args.steps,
@@ -726,25 +809,47 @@ def main():
         dist.destroy_process_group()
 
 
+def cpu_baseline(wl):
+    """The oracle timed on the host cores on a bounded sample of the workload:
+    the first 2^22 elements of each shard, 3 steps, run by one process per
+    host core (each on an equal share of every shard's elements); the value is
+    the mean of steps 2 and 3.  The single-threaded figure on the same sample
+    (2 steps) is given beside it."""
+    n_per = 1 << 22
+    sample = wl["sample_for_cpu"](n_per)
+    n, times = time_oracle(sample, n_per, 2)
+    procs = host_cores()
+    n, walls, _ = time_oracle_parallel(sample, n_per, 3, procs)
+    return {"value": n / statistics.mean(walls[1:]), "unit": "elements/s", "cores": procs, "kind": "oracle",
+            "sample": f"the first {n_per} elements of each of the {wl['nd']} shards ({n} elements), 3 steps, "
+                      f"{procs} processes each on an equal share of every shard; mean of steps 2-3",
+            "cpu_model": cpu_model(),
+            "single_thread": {"value": n / statistics.mean(times), "cores": 1,
+                              "sample": "the same elements, 2 steps, one process"}}
+
+
 def reference_arm(args, rank, world, W):
-    """The CPU oracle on the host cores: each step one oracle step over a
-    bounded sample of the workload (the first 2^20 elements of each shard)."""
+    """The CPU oracle on the host cores: one process per core, each on an equal
+    share of a bounded sample of the workload (the first 2^22 elements of each
+    of the GPT-2 group's 8 shards); every step starts behind a barrier and its
+    time is the last process's end minus the first one's start."""
     if rank != 0:
         return
-    n_per = 1 << 20
-    wl_fn = cpu_sample_gpt2
-    _, times = time_oracle(W, lambda n: wl_fn(W, n), n_per, args.steps + args.warmup)
-    times = times[args.warmup:]
-    n = 8 * n_per
-    ms = 1e3 * statistics.mean(times)
+    n_per = 1 << 22
+    procs = host_cores()
+    n, walls, _ = time_oracle_parallel(cpu_sample_gpt2(W, n_per), n_per, args.steps + args.warmup, procs)
+    walls = walls[args.warmup:]
+    ms = 1e3 * statistics.mean(walls)
     value = n / (ms / 1e3)
     line = {"metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
             "config": {"workload": "gpt2-1.5b-nd8: GPT-2 1.5B-shaped group, N_d=8, all ranks",
                        "sample_elements_per_step": n},
-            "cpu_baseline": {"value": value, "unit": "elements/s", "cores": 1, "kind": "oracle",
-                             "sample": f"the first {n_per} elements of each of the 8 shards per step"},
+            "cpu_baseline": {"value": value, "unit": "elements/s", "cores": procs, "kind": "oracle",
+                             "sample": f"the first {n_per} elements of each of the 8 shards per step, "
+                                       f"{procs} processes each on an equal share",
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

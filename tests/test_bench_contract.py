@@ -76,3 +76,26 @@ def test_every_input_helper_bench_and_tests_use_exists():
                 if not hasattr(W, node.attr):
                     missing.add(f"{os.path.basename(f)}: W.{node.attr}")
     assert not missing, sorted(missing)
+
+
+@pytest.mark.timeout(300)
+def test_all_cores_oracle_timing_splits_the_work_exactly():
+    """The all-cores CPU baseline runs the oracle on an equal share of every
+    shard in each process; reassembled, the parameters after three steps equal
+    one process's run over the whole sample."""
+    import numpy as np
+    import bench
+    import oracle
+    import workloads as W
+    n = 1001
+    sample = bench.cpu_sample_gpt2(W, n)
+    nd, grads, flat, h = sample
+    ne, walls, got = bench.time_oracle_parallel(sample, n, 3, 3, want_params=True)
+    assert ne == nd * n and len(walls) == 3 and all(w > 0 for w in walls)
+    ref = flat.copy()
+    shards = [dict(numel=n, grad_off=r * n, param_off=r * n, master=oracle.widen_16(ref[r * n:(r + 1) * n], 2),
+                   m=np.zeros(n, np.float32), v=np.zeros(n, np.float32)) for r in range(nd)]
+    for t in (1, 2, 3):
+        oracle.zero_step(grads, 2, shards, ref, 2, dict(h, max_grad_norm=0.0), t, 1.0)
+    assert not np.array_equal(ref, flat)
+    assert np.array_equal(got, ref)
