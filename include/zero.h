@@ -111,6 +111,33 @@ int zero_plan_intersections(const int64_t* tensor_offsets, const int64_t* numels
 int zero_mem_model(double psi, double K, int n_d, int stage, double* bytes_out);
 
 /* ------------------------------------------------------------------------
+ * Plan-exact model states of one rank, with temporaries.  Host only.
+ * Source: ZeRO paper (Chinese translation), 5.1-5.3 (which model states each
+ * stage partitions), 3.2 and 6.2 (fused fp32 flat buffers: 6 GB for 1.5B
+ * parameters, 12 GB for 3B).  zero_mem_model takes a rank's share as
+ * psi / n_d; this takes the plan's own sizes, so padding and the remainder
+ * ranks are counted:
+ *   flat_numel   elements of a 16-bit flat buffer the stage keeps whole: the
+ *                plan's padded total (zero_plan), or psi for stage 0
+ *   shard_numel  this rank's shard (zero_plan's rank_numels[r]; for ZeRO-3 the
+ *                sum of the rank's part of every unit)
+ *   K            optimizer-state bytes per parameter (12 for mixed-precision Adam)
+ *   state_sets   copies of the optimizer state held: 1 when updated in place,
+ *                2 for the double-buffered state of the fused single pass
+ *   fp32_temp_numel, b16_temp_numel  elements of fp32 and 16-bit temporaries
+ *                (a fused flat buffer, a ZeRO-3 layer buffer, a bucket), or 0
+ * bytes_out[5] = parameters, gradients, optimizer states, temporaries, total:
+ *   parameters  2 flat_numel for stages 0-2, 2 shard_numel for stage 3
+ *   gradients   2 flat_numel for stages 0-1, 2 shard_numel for stages 2-3
+ *   states      K state_sets flat_numel for stage 0, K state_sets shard_numel otherwise
+ *   temporaries 4 fp32_temp_numel + 2 b16_temp_numel
+ * Returns ZERO_OK or ZERO_EINVAL (a negative size, stage outside 0..3,
+ * state_sets < 1, K < 0, bytes_out null).
+ * ------------------------------------------------------------------------ */
+int zero_mem_model_plan(int64_t flat_numel, int64_t shard_numel, double K, int stage, int state_sets,
+                        int64_t fp32_temp_numel, int64_t b16_temp_numel, double* bytes_out);
+
+/* ------------------------------------------------------------------------
  * Communication volume per rank and step, in elements.  Host only.
  * Source: ZeRO paper (Chinese translation), 7.1 (a reduce-scatter or an
  * all-gather of Psi elements moves Psi; data parallelism's all-reduce is one

@@ -90,6 +90,26 @@ def test_mem_model_equals_oracle(Z, orc):
         Z.zero_mem_model(1e9, 12, 0, 1)
 
 
+def test_mem_model_plan_equals_oracle(Z, orc):
+    units = W.llama_units(W.llama_group())
+    cases = []
+    for numels, nd, mode in ((W.numels(W.tiny_group()), 3, 0), (W.numels(W.tiny_group()), 3, 1),
+                             (W.numels(W.gpt2_group()), 8, 0), (W.numels(W.llama_group()), 4, 0),
+                             (W.numels(W.gpt2_group(52, 3456, 50257, 1024)), 64, 0)):
+        p = Z.zero_plan(numels, nd, mode)
+        cases += [(p["padded_total"], n) for n in set(p["rank_numels"])]
+    cases.append((sum(units), sum(u // 4 for u in units)))          # ZeRO-3 rank: its part of every unit
+    for F, n in cases:
+        for st in range(4):
+            for sets, f32, b16 in ((1, 0, 0), (2, 0, 0), (1, F, 0), (2, 0, max(units))):
+                assert Z.zero_mem_model_plan(F, n, 12, st, sets, f32, b16) == \
+                    orc.mem_model_plan(F, n, 12, st, sets, f32, b16)
+    for bad in ((-1, 0, 12, 1, 1, 0, 0), (8, 2, 12, 4, 1, 0, 0), (8, 2, 12, 1, 0, 0, 0), (8, 2, -1.0, 1, 1, 0, 0),
+                (8, 2, 12, 1, 1, -5, 0), (8, -2, 12, 1, 1, 0, 0)):
+        with pytest.raises(Z.ZeroError):
+            Z.zero_mem_model_plan(*bad)
+
+
 def test_argument_errors_before_any_device_work(Z):
     fake = 0x10000   # never dereferenced: every case below fails validation first
     ws = Z.zero_workspace_bytes()

@@ -64,6 +64,7 @@ _SIGS = {
     "zero_plan": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "zero_plan_intersections": (_I, [_P, _P, _I, _I64, _I64, _P]),
     "zero_mem_model": (_I, [ctypes.c_double, ctypes.c_double, _I, _I, _P]),
+    "zero_mem_model_plan": (_I, [_I64, _I64, ctypes.c_double, _I, _I, _I64, _I64, _P]),
     "zero_comm_volume": (_I, [ctypes.c_double, _I, _I, _I, _P]),
     "zero_plan_round_robin": (_I, [_I, _I, _P]),
     "zero_workspace_bytes": (ctypes.c_size_t, []),
@@ -147,6 +148,14 @@ def zero_mem_model(psi, K, n_d, stage):
     b = ctypes.c_double()
     _check(lib.zero_mem_model(psi, K, n_d, stage, ctypes.byref(b)))
     return b.value
+
+
+def zero_mem_model_plan(flat_numel, shard_numel, K, stage, state_sets=1, fp32_temp_numel=0, b16_temp_numel=0):
+    """Plan-exact bytes of one rank: dict of params, grads, states, temp, total."""
+    out = (ctypes.c_double * 5)()
+    _check(lib.zero_mem_model_plan(flat_numel, shard_numel, K, stage, state_sets, fp32_temp_numel, b16_temp_numel,
+                                   out))
+    return dict(zip(("params", "grads", "states", "temp", "total"), list(out)))
 
 
 def zero_comm_volume(psi, n_d, stage, ring=False):

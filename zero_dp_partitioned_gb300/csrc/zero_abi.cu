@@ -333,6 +333,21 @@ int zero_mem_model(double psi, double K, int n_d, int stage, double* bytes_out) 
     return ZERO_OK;
 }
 
+int zero_mem_model_plan(int64_t flat_numel, int64_t shard_numel, double K, int stage, int state_sets,
+                        int64_t fp32_temp_numel, int64_t b16_temp_numel, double* bytes_out) {
+    if (!bytes_out || flat_numel < 0 || shard_numel < 0 || !(K >= 0.0) || stage < 0 || stage > 3 ||
+        state_sets < 1 || fp32_temp_numel < 0 || b16_temp_numel < 0)
+        return fail(ZERO_EINVAL, "zero_mem_model_plan: bad argument");
+    const double F = (double)flat_numel, n = (double)shard_numel;
+    // P_os partitions the optimizer states, P_os+g the gradients too, P_os+g+p the parameters too
+    bytes_out[0] = 2.0 * (stage == 3 ? n : F);
+    bytes_out[1] = 2.0 * (stage >= 2 ? n : F);
+    bytes_out[2] = K * (double)state_sets * (stage == 0 ? F : n);
+    bytes_out[3] = 4.0 * (double)fp32_temp_numel + 2.0 * (double)b16_temp_numel;
+    bytes_out[4] = bytes_out[0] + bytes_out[1] + bytes_out[2] + bytes_out[3];
+    return ZERO_OK;
+}
+
 int zero_comm_volume(double psi, int n_d, int stage, int ring, double* elements_out) {
     if (!elements_out || n_d < 1 || stage < 0 || stage > 3 || !(psi >= 0.0))
         return fail(ZERO_EINVAL, "zero_comm_volume: bad argument");
