@@ -420,6 +420,15 @@ def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None):
                 sample_for_cpu=None)
 
 
+def _gather_status_check(gstatus):
+    """After the timed steps: the bulk gathers' sticky status word must be clear."""
+    def check(steps):
+        if int(gstatus.item()) != 0:
+            raise RuntimeError("zero3_gather_bulk reported a timed-out wait")
+        return {}
+    return check
+
+
 def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
     """ZeRO-3 per-layer path, Llama-3-8B group as 34 units, N_d = 4, rank 1:
     per step 34 forward gathers, 34 backward gathers (reverse order), 34 bucket
@@ -456,10 +465,12 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
     st = dict(cur=0, t=1, S=wl.loss_scale)
     part_ptrs = [[rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)] for u in range(len(units))]
 
+    gstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+
     def step(from_host=False):
         for u in list(range(len(units))) + list(reversed(range(len(units)))):
-            with timer("k_gather"):
-                Z.zero3_gather_layer(part_ptrs[u], units[u], Z.ZERO_BF16, layer)
+            with timer("k_gather_bulk"):
+                Z.zero3_gather_bulk(part_ptrs[u], [parts[u]] * nd, Z.ZERO_BF16, layer, 0, gstatus)
         for k, (u, row) in enumerate(buckets):
             with timer("k_reduce"):
                 Z.zero3_reduce_bucket(row, me, units[u], Z.ZERO_BF16, gshard[uoff[u]:uoff[u] + parts[u]], k > 0,
@@ -471,12 +482,12 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
 
     total_units = sum(units)
     return dict(name=wl.name, step=step, state=st, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
-                kernel_bytes={"k_gather": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
-                dominant_label=None, h2d=None, d2h=48, e2e_ok=False,
+                kernel_bytes={"k_gather_bulk": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=_gather_status_check(gstatus),
                 formula_bytes=2 * 4 * total_units + (2 * nd + 2) * L + 28 * L,
                 config={"workload": "zero3-llama3-8b: Llama-3-8B group as 34 ZeRO-3 units, N_d=4, rank 1",
                         "units": len(units), "shard_elements": L, "psi": total_units,
-                        "path": "per unit: gather x2, bucket reduce; then apply",
+                        "path": "per unit: gather x2 (zero3_gather_bulk on every SM), bucket reduce; then apply",
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
 
@@ -526,10 +537,12 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
     reduces = [(buckets[u], [Z.shard(ln, u0, 0, None, None, None, grad_shard=gseg[s0:s0 + ln])])
                for u in mine for r, u0, s0, ln in pieces[u] if r == me]
 
+    gstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+
     def step(from_host=False):
         for u in list(range(len(units))) + list(reversed(range(len(units)))):
-            with timer("k_gather"):
-                Z.zero3_gather_segments(gathers[u][0], gathers[u][1], Z.ZERO_BF16, layer)
+            with timer("k_gather_bulk"):
+                Z.zero3_gather_bulk(gathers[u][0], gathers[u][1], Z.ZERO_BF16, layer, 0, gstatus)
         for k, (bk, sh) in enumerate(reduces):
             with timer("k_reduce"):
                 Z.zero_shard_reduce(bk, Z.ZERO_BF16, sh, k > 0, stats, ws, ws.numel())
@@ -541,13 +554,151 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
     total = sum(units)
     return dict(name=name, step=step, state=st, elements=L, nd=nd,
                 launches_per_step=2 * len(units) + len(reduces) + 1,
-                kernel_bytes={"k_gather": 2 * 4 * total, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
-                dominant_label=None, h2d=None, d2h=48, e2e_ok=False,
+                kernel_bytes={"k_gather_bulk": 2 * 4 * total, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=_gather_status_check(gstatus),
                 formula_bytes=2 * 4 * total + (2 * nd + 2) * L + 28 * L,
                 config={"workload": f"{name}: Llama-3-8B group as {len(units)} ZeRO-3 units, owner broadcast "
                                     "from contiguous rank segments, N_d=4, rank 1",
                         "units": len(units), "segment_elements": L, "psi": total,
-                        "path": "per unit: gather of the owners' pieces x2, reduce of rank 1's pieces; then apply",
+                        "path": "per unit: gather of the owners' pieces x2 (zero3_gather_bulk on every SM), reduce "
+                                "of rank 1's pieces; then apply",
+                        "l2": "inputs larger than L2, no flush"},
+                sample_for_cpu=None)
+
+
+def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, tokens=1024, gather_ctas=32):
+    """ZeRO-3 on the Llama-3-8B group (N_d = 4, rank 1) with the parameter
+    gather of the next unit prefetched on a side stream while the current unit
+    computes.  The units' computation is a stand-in: per unit a bf16 GEMM of
+    the gathered parameters, viewed as [unit/4096, 4096], with `tokens`
+    activations (twice in the backward).  The gathers go to two alternating
+    layer buffers through zero3_gather_bulk on `gather_ctas` CTAs; each
+    backward unit's bucket reduce and the final shard update run on the main
+    stream.  The same step is also timed in order on one stream (each gather
+    by zero3_gather_bulk on every SM) and with the stand-in GEMMs alone."""
+    wl = W.workload("zero3-llama3-8b")
+    if layers:
+        wl.specs = W.llama_group(L=layers)
+    name = "zero3-prefetch-llama3-8b" if not layers else f"zero3-prefetch-llama3-{layers}layers"
+    nd, me, cols = wl.nd, 1, 4096
+    units = W.llama_units(wl.specs, L=layers or 32)
+    assert all(u % cols == 0 for u in units)
+    parts = [u // nd for u in units]
+    starts = [sum(units[:i]) for i in range(len(units))]
+    uoff = [sum(parts[:i]) for i in range(len(parts))]
+    L = sum(parts)
+    log(f"[bench] {name}: {len(units)} units, rank shard {L}, stand-in GEMMs with {tokens} tokens; generating inputs")
+    flat = W.flat_params(wl.specs, sum(units), torch.bfloat16, wl.param_seed, dev)
+    rshards = [torch.cat([flat[s + r * p: s + (r + 1) * p] for s, p in zip(starts, parts)]) for r in range(nd)]
+    del flat
+    torch.cuda.empty_cache()
+    gs = W.GradStream([5 + r for r in range(nd)], dev)
+    buckets = {}
+    for u in reversed(range(len(units))):
+        buckets[u] = gs.draw_plain([torch.empty(units[u], dtype=torch.bfloat16, device=dev) for _ in range(nd)],
+                                   wl.grad_std)
+    bufs = [torch.empty(max(units), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    X = W.fill_normal_(torch.empty(tokens * cols, dtype=torch.bfloat16, device=dev), 1.0,
+                       W.generator(77, dev)).view(tokens, cols)
+    Y = torch.empty(max(units) // cols, tokens, dtype=torch.bfloat16, device=dev)
+    master, m, v = rshards[me].float(), torch.zeros(L, device=dev), torch.zeros(L, device=dev)
+    gshard = torch.empty(L, dtype=torch.bfloat16, device=dev)
+    sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    stats = torch.zeros(16, dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    gstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+    part_ptrs = [[rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)] for u in range(len(units))]
+    n_units = len(units)
+    order = [(u, 1) for u in range(n_units)] + [(u, 2) for u in reversed(range(n_units))]   # (unit, GEMMs)
+    side = torch.cuda.Stream(device=dev)
+    gathered = [torch.cuda.Event() for _ in order]
+    consumed = [torch.cuda.Event() for _ in order]
+
+    def consume(buf, u, k):
+        w = buf[:units[u]].view(-1, cols)
+        for _ in range(k):
+            torch.matmul(w, X.t(), out=Y[:w.shape[0]])
+
+    def backward_reduce(i, u):
+        if i >= n_units:
+            with timer("k_reduce"):
+                Z.zero3_reduce_bucket(buckets[u], me, units[u], Z.ZERO_BF16, gshard[uoff[u]:uoff[u] + parts[u]],
+                                      i > n_units, stats, ws, ws.numel())
+
+    def finish():
+        with timer("k_apply"):
+            Z.zero_shard_apply(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"],
+                               stats, 0.0, 0, ws, ws.numel(), res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    def step(from_host=False):
+        main = torch.cuda.current_stream()
+
+        def gather(i):
+            if i >= 2:
+                side.wait_event(consumed[i - 2])
+            u = order[i][0]
+            Z.zero3_gather_bulk(part_ptrs[u], [parts[u]] * nd, Z.ZERO_BF16, bufs[i % 2], gather_ctas, gstatus,
+                                stream=side)
+            gathered[i].record(side)
+
+        side.wait_stream(main)          # the last step's update of rank 1's parameters comes first
+        gather(0)
+        for i, (u, k) in enumerate(order):
+            if i + 1 < len(order):
+                gather(i + 1)
+            main.wait_event(gathered[i])
+            consume(bufs[i % 2], u, k)
+            consumed[i].record(main)
+            backward_reduce(i, u)
+        finish()
+
+    def step_serial():
+        for i, (u, k) in enumerate(order):
+            Z.zero3_gather_bulk(part_ptrs[u], [parts[u]] * nd, Z.ZERO_BF16, bufs[0], 0, gstatus)
+            consume(bufs[0], u, k)
+            backward_reduce(i, u)
+        finish()
+
+    def step_consumers_only():
+        for u, k in order:
+            consume(bufs[0], u, k)
+
+    def extra(steps):
+        """The serial schedule and the stand-in GEMMs alone, timed like the step."""
+        out = {}
+        for key, fn in (("serial_ms_per_step", step_serial), ("consumer_ms_per_step", step_consumers_only)):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            out[key] = a.elapsed_time(b) / steps
+        if int(gstatus.item()) != 0:
+            raise RuntimeError("zero3_gather_bulk reported a timed-out wait")
+        return out
+
+    total = sum(units)
+    return dict(name=name, step=step, state=st, elements=L, nd=nd,
+                launches_per_step=len(order) + n_units + 1,
+                kernel_bytes={"k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=extra,
+                formula_bytes=2 * 4 * total + (2 * nd + 2) * L + 28 * L,
+                config={"workload": f"{name}: Llama-3-8B group as {n_units} ZeRO-3 units, N_d=4, rank 1; the next "
+                                    "unit's gather prefetched on a side stream beside a stand-in compute",
+                        "units": n_units, "shard_elements": L, "psi": total, "tokens": tokens,
+                        "gather_ctas": gather_ctas,
+                        "consumer": f"stand-in per unit: bf16 GEMM [unit/{cols}, {cols}] x [{cols}, {tokens}] "
+                                    "(torch.matmul), once forward and twice backward",
+                        "path": "side stream: zero3_gather_bulk into two alternating layer buffers; main stream: "
+                                "stand-in GEMMs, bucket reduce after each backward unit, then apply",
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
 
@@ -573,7 +724,7 @@ def cpu_sample_gpt2(W, n_per_shard):
 WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_allreduce,
              "llama3-8b-nd4-r1": llama_rank_local,
              "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama,
-             "zero3-bcast-llama3-8b": zero3_broadcast}
+             "zero3-bcast-llama3-8b": zero3_broadcast, "zero3-prefetch-llama3-8b": zero3_prefetch}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -714,6 +865,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--tokens", type=int, default=1024,
+                    help="zero3-prefetch-llama3-8b: activations of the stand-in GEMM per unit")
+    ap.add_argument("--gather-ctas", type=int, default=32,
+                    help="zero3-prefetch-llama3-8b: CTAs the prefetched gather may use")
     args = ap.parse_args()
     rank, world, local = dist_env()
     import workloads as W
@@ -734,7 +889,8 @@ def main():
             dist.barrier()
 
     timer = KernelTimer(torch)
-    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, layers=args.layers)
+    kw = dict(tokens=args.tokens, gather_ctas=args.gather_ctas) if args.workload == "zero3-prefetch-llama3-8b" else {}
+    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, layers=args.layers, **kw)
     step = wl["step"]
     sampler = ClockSampler(local)
     for _ in range(max(3, args.warmup)):
@@ -757,6 +913,8 @@ def main():
     clocks = sampler.stop()
     ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, dev)
     kinds = timer.per_kind(args.steps)
+    if wl.get("extra"):
+        wl["config"].update(wl["extra"](args.steps))
 
     e2e = None
     if wl["e2e_ok"]:

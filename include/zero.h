@@ -343,6 +343,25 @@ int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t uni
 int zero3_gather_segments(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments,
                           int dtype, void* layer_out, void* stream);
 
+/* The same materialisation for a pipelined schedule: the gather of the next
+ * unit runs on a side stream while the current unit computes.
+ * Source: flycode100 ZeRO tutorial, section 4 (DeepSpeed prefetches the next
+ * layer's parameters so that the all-gather overlaps with computation).
+ * layer_out = segment 0 | segment 1 | ... exactly as zero3_gather_segments
+ * (and, with world_size equal segments, as zero3_gather_layer).  The copy runs
+ * on at most n_ctas CTAs (0 = one per SM), leaving the other SMs to whatever
+ * else the GPU runs.  When every segment's source and its slot in layer_out
+ * agree modulo 16 bytes, the bytes are moved by the TMA unit (bulk copies
+ * through shared memory, one thread per CTA issuing them, about 100 GB/s per
+ * CTA); otherwise the register-staged gather runs on at most n_ctas blocks.
+ * status: device int32 the caller zero-fills; a CTA whose bounded wait for a
+ * copy runs out sets bit 0 and stops, and layer_out is then incomplete.
+ * Errors (before any work): ZERO_EINVAL (NULL, negative sizes or n_ctas,
+ * unknown dtype, status not 4-byte aligned), ZERO_EALIGN, ZERO_ELIMIT,
+ * ZERO_ECUDA. */
+int zero3_gather_bulk(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments, int dtype,
+                      void* layer_out, int n_ctas, int32_t* status, void* stream);
+
 /* The owner's share of the unit's gradient reduce-scatter:
  * grad_part[j] = round16(sum_r fp32(bucket_r[owner * P + j]) / world_size),
  * and the part's sum of squares / overflow added to *stats (accumulate as for

@@ -230,3 +230,132 @@ def test_owner_broadcast_pipeline_three_steps(Z):
         assert np.array_equal(t2u16(segs[me]), o_param)
         assert np.array_equal(master.cpu().numpy().view(np.uint32), o_master.view(np.uint32))
         assert np.array_equal(m.cpu().numpy().view(np.uint32), o_m.view(np.uint32))
+
+
+def _aligned_view(host_u16, shift, L):
+    """A device view of L elements starting `shift` elements past a 256-byte aligned allocation."""
+    base = dev16(host_u16, 2)
+    assert base.data_ptr() % 256 == 0
+    return base[shift:shift + L]
+
+
+@pytest.mark.parametrize("n_ctas", [0, 1, 3, 32])
+def test_gather_bulk_is_exact(Z, n_ctas):
+    """Segments that agree with their slot modulo 16 bytes (the TMA path, with
+    unaligned heads and ragged tails) and segments that do not (the
+    register-staged fallback), on a bounded CTA count."""
+    rng = np.random.default_rng(40 + n_ctas)
+    for trial in range(10):
+        n = int(rng.integers(1, 7))
+        lens = [int(x) for x in rng.choice([0, 1, 7, 8, 9, 1000, 4097, 54528, 300001], n)]
+        out_shift = int(rng.integers(0, 8))
+        congruent = trial % 3 != 2
+        offs = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(int)
+        shifts = [((out_shift + int(o)) % 8) if congruent else int(rng.integers(0, 8)) for o in offs]
+        host = [rng.integers(0, 1 << 16, L + 8, dtype=np.uint64).astype(np.uint16) for L in lens]
+        dev = [_aligned_view(h, s, L) for h, s, L in zip(host, shifts, lens)]
+        out_base = torch.zeros(sum(lens) + 16, dtype=torch.bfloat16, device=DEV)
+        out = out_base[out_shift:out_shift + max(1, sum(lens))]
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        Z.zero3_gather_bulk(dev, lens, Z.ZERO_BF16, out, n_ctas, status)
+        torch.cuda.synchronize()
+        ref = orc.gather_segments([h[s:s + L].copy() for h, s, L in zip(host, shifts, lens)])
+        got = t2u16(out_base)
+        assert np.array_equal(got[out_shift:out_shift + sum(lens)], ref), (lens, shifts, out_shift)
+        assert not got[:out_shift].any() and not got[out_shift + sum(lens):].any()     # nothing outside the slot
+        assert int(status.item()) == 0
+
+
+def test_gather_bulk_equals_gather_layer_on_llama_parts(Z):
+    """World-size-4 parts of a Llama-3-8B-shaped block unit cut to 1/64
+    (3,408,000 elements): the TMA gather on 8 CTAs equals zero3_gather_layer."""
+    U, nd = 3_408_000, 4
+    rng = np.random.default_rng(3)
+    parts = [dev16(rng.integers(0, 1 << 16, U // nd, dtype=np.uint64).astype(np.uint16), 2) for _ in range(nd)]
+    a = torch.empty(U, dtype=torch.bfloat16, device=DEV)
+    b = torch.empty(U, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Z.zero3_gather_layer(parts, U, Z.ZERO_BF16, a)
+    Z.zero3_gather_bulk(parts, [U // nd] * nd, Z.ZERO_BF16, b, 8, status)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and int(status.item()) == 0
+
+
+def test_gather_bulk_wait_timeout_is_reported_and_harmless(Z, monkeypatch):
+    """With the wait limit at zero tries every CTA gives up on its first load:
+    status bit 0 is set, the CTAs drain what they started and return, and the
+    next call (default limit) is exact."""
+    L = 200_000
+    rng = np.random.default_rng(5)
+    host = rng.integers(0, 1 << 16, L, dtype=np.uint64).astype(np.uint16)
+    src = dev16(host, 2)
+    out = torch.zeros(L, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    monkeypatch.setenv("ZERO_GB300_SPIN_LIMIT", "0")
+    Z.zero3_gather_bulk([src], [L], Z.ZERO_BF16, out, 4, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1
+    monkeypatch.delenv("ZERO_GB300_SPIN_LIMIT")
+    status.zero_()
+    Z.zero3_gather_bulk([src], [L], Z.ZERO_BF16, out, 4, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and np.array_equal(t2u16(out), host)
+
+
+def test_gather_bulk_argument_errors(Z):
+    src = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(2, dtype=torch.int32, device=DEV)
+    for args, code in (((([src], [64], 7, out, 0, status)), Z.ZERO_EINVAL),
+                       ((([src], [64], Z.ZERO_BF16, out, -1, status)), Z.ZERO_EINVAL),
+                       ((([src], [-1], Z.ZERO_BF16, out, 0, status)), Z.ZERO_EINVAL),
+                       ((([src] * 65, [1] * 65, Z.ZERO_BF16, out, 0, status)), Z.ZERO_ELIMIT),
+                       ((([src], [64], Z.ZERO_BF16, out, 0, status.view(torch.uint8)[1:])), Z.ZERO_EINVAL),
+                       ((([src.view(torch.uint8)[1:]], [8], Z.ZERO_BF16, out, 0, status)), Z.ZERO_EALIGN)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero3_gather_bulk(*args)
+        assert e.value.code == code
+
+
+def test_prefetch_schedule_gives_every_consumer_its_own_unit(Z):
+    """The pipelined schedule: unit u+1 is gathered on a side stream (TMA, 8
+    CTAs) into the other of two layer buffers while the consumer of unit u
+    runs on the main stream; forward then backward (reverse order).  Each
+    consumer snapshots the buffer it was given; every snapshot equals the
+    oracle's gather of its unit, so no gather overwrote a buffer in use and no
+    consumer ran ahead of its gather."""
+    rng = np.random.default_rng(9)
+    nd = 4
+    units = [int(x) * 8 * nd for x in rng.integers(2000, 40000, 7)]
+    host = [[rng.integers(0, 1 << 16, u // nd, dtype=np.uint64).astype(np.uint16) for _ in range(nd)] for u in units]
+    parts = [[dev16(h, 2) for h in hu] for hu in host]
+    bufs = [torch.empty(max(units), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    order = list(range(len(units))) + list(reversed(range(len(units))))
+    gathered = [torch.cuda.Event() for _ in order]
+    consumed = [torch.cuda.Event() for _ in order]
+    snaps = []
+    x = torch.randn(256, 256, device=DEV)
+
+    def gather(i):
+        if i >= 2:
+            side.wait_event(consumed[i - 2])          # its buffer's previous consumer is done
+        u = order[i]
+        Z.zero3_gather_bulk(parts[u], [units[u] // nd] * nd, Z.ZERO_BF16, bufs[i % 2], 8, status, stream=side)
+        gathered[i].record(side)
+
+    side.wait_stream(main)
+    gather(0)
+    for i, u in enumerate(order):
+        if i + 1 < len(order):
+            gather(i + 1)                             # prefetch the next unit
+        main.wait_event(gathered[i])
+        for _ in range(3):                            # a stand-in consumer that takes some time
+            x = torch.tanh(x @ x)
+        snaps.append(bufs[i % 2][:units[u]].clone())
+        consumed[i].record(main)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for i, u in enumerate(order):
+        assert np.array_equal(t2u16(snaps[i]), orc.gather_segments([h.copy() for h in host[u]])), (i, u)

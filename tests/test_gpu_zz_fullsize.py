@@ -278,6 +278,8 @@ def test_zero3_llama3_8b_rank1(Z):
     del flat
     torch.cuda.empty_cache()
     layer = torch.empty(max(units), dtype=torch.bfloat16, device=DEV)
+    layer2 = torch.empty(max(units), dtype=torch.bfloat16, device=DEV)
+    gstatus = torch.zeros(1, dtype=torch.int32, device=DEV)
     buckets = [torch.empty(max(units), dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
     gs = W.GradStream([5 + r for r in range(nd)], DEV)
     master = rshards[me].float()
@@ -297,6 +299,10 @@ def test_zero3_llama3_8b_rank1(Z):
             Z.zero3_gather_layer(ptrs, units[u], dt, layer)
             if u in (0, 1, len(units) - 1):
                 assert torch.equal(layer[:units[u]], torch.cat(ptrs))     # gather = inverse of the partition
+            if t == 1:      # the TMA gather, on every SM and on 32 CTAs, equals it unit by unit
+                for n_ctas in (0, 32):
+                    Z.zero3_gather_bulk(ptrs, [parts[u]] * nd, dt, layer2, n_ctas, gstatus)
+                    assert torch.equal(layer2[:units[u]].view(torch.int16), layer[:units[u]].view(torch.int16))
         acc = orc.ExactAccumulator()
         a_samp = np.empty(idx.size, np.uint16)
         for k_u, u in enumerate(reversed(range(len(units)))):
@@ -321,3 +327,4 @@ def test_zero3_llama3_8b_rank1(Z):
         assert np.array_equal(u16(gshard[ti]), a_samp)
         orc.apply(a_samp, dt, samp.master, samp.m, samp.v, samp.param, dt, k, scalars(h, t))
         check_state(samp, master, m, v, rshards[me], exact=True)
+    assert int(gstatus.item()) == 0

@@ -75,6 +75,7 @@ _SIGS = {
                               _P, _P]),
     "zero3_gather_layer": (_I, [_P, _I, _I64, _I, _P, _P]),
     "zero3_gather_segments": (_I, [_P, _P, _I, _I, _P, _P]),
+    "zero3_gather_bulk": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
     "zero3_reduce_bucket": (_I, [_P, _I, _I, _I64, _I, _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "zero_shard_step_noalloc": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
@@ -230,6 +231,16 @@ def zero3_gather_segments(segment_ptrs, segment_numels, dtype, layer_out, stream
     n = len(segment_ptrs)
     lens = (ctypes.c_int64 * max(1, n))(*segment_numels)
     _check(lib.zero3_gather_segments(_ptrs(segment_ptrs), lens, n, dtype, _ptr(layer_out), _stream(stream)))
+
+
+def zero3_gather_bulk(segment_ptrs, segment_numels, dtype, layer_out, n_ctas, status, stream=None):
+    """The gather on at most n_ctas CTAs (0 = one per SM), moved by the TMA unit
+    when every segment agrees with its slot modulo 16 bytes; status: device
+    int32 (zero-filled by the caller), bit 0 set if a wait ran out."""
+    n = len(segment_ptrs)
+    lens = (ctypes.c_int64 * max(1, n))(*segment_numels)
+    _check(lib.zero3_gather_bulk(_ptrs(segment_ptrs), lens, n, dtype, _ptr(layer_out), int(n_ctas), _ptr(status),
+                                 _stream(stream)))
 
 
 def zero3_reduce_bucket(bucket_ptrs, owner, unit_numel, grad_dtype, grad_part, accumulate, stats, workspace,

@@ -497,7 +497,7 @@ static int gather_segments(const void* const* src, const int64_t* len, int n, in
     }
     if (off == 0) return ZERO_OK;
     const int vec = v8 ? 8 : 1;
-    const int64_t tile = (int64_t)TILE_THREADS * vec * 2;
+    const int64_t tile = (int64_t)TILE_THREADS * vec * (vec == 8 ? GATHER_UNROLL : 2);
     int64_t t = 0;
     for (int p = 0; p < n; ++p) {
         g.tile_begin[p] = t;
@@ -524,6 +524,88 @@ int zero3_gather_layer(const void* const* part_ptrs, int world_size, int64_t uni
 int zero3_gather_segments(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments,
                           int dtype, void* layer_out, void* stream) {
     return gather_segments(segment_ptrs, segment_numels, n_segments, dtype, layer_out, stream);
+}
+
+int zero3_gather_bulk(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments, int dtype,
+                      void* layer_out, int n_ctas, int32_t* status, void* stream) {
+    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "zero3_gather_bulk: unknown dtype");
+    if (n_segments < 1) return fail(ZERO_EINVAL, "zero3_gather_bulk: no segments");
+    if (n_segments > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "zero3_gather_bulk: more than ZERO_MAX_SLICES segments");
+    if (!segment_ptrs || !segment_numels || !layer_out || !status)
+        return fail(ZERO_EINVAL, "zero3_gather_bulk: NULL pointer");
+    if (n_ctas < 0) return fail(ZERO_EINVAL, "zero3_gather_bulk: negative n_ctas");
+    if (!aligned(status, 4)) return fail(ZERO_EINVAL, "zero3_gather_bulk: status not 4-byte aligned");
+    if (!aligned(layer_out, 2)) return fail(ZERO_EALIGN, "zero3_gather_bulk: layer_out not 2-byte aligned");
+    BulkGatherArgs b;
+    std::memset(&b, 0, sizeof b);
+    b.n = n_segments;
+    b.out = static_cast<uint8_t*>(layer_out);
+    b.status = status;
+    bool congruent = true;
+    int64_t off = 0;
+    for (int p = 0; p < n_segments; ++p) {
+        const int64_t L = segment_numels[p];
+        if (L < 0) return fail(ZERO_EINVAL, "zero3_gather_bulk: negative segment length");
+        if (L > 0 && !segment_ptrs[p]) return fail(ZERO_EINVAL, "zero3_gather_bulk: a segment pointer is NULL");
+        if (!aligned(segment_ptrs[p], 2)) return fail(ZERO_EALIGN, "zero3_gather_bulk: segment pointer not 2-byte aligned");
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(segment_ptrs[p]);
+        const uintptr_t da = reinterpret_cast<uintptr_t>(layer_out) + 2 * (uintptr_t)off;
+        if (L > 0 && (sa - da) % 16 != 0) congruent = false;
+        b.src[p] = static_cast<const uint8_t*>(segment_ptrs[p]);
+        b.bytes[p] = 2 * L;
+        b.dst_off[p] = 2 * off;
+        const int64_t h = (int64_t)((16 - sa % 16) % 16);
+        b.head[p] = h < b.bytes[p] ? h : b.bytes[p];
+        b.mid[p] = (b.bytes[p] - b.head[p]) / 16 * 16;
+        off += L;
+    }
+    if (off == 0) return ZERO_OK;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "zero3_gather_bulk: device query");
+    int ctas = n_ctas == 0 ? sms : n_ctas;
+    if (!congruent) {
+        // no bulk copies possible: the register-staged gather on at most `ctas` blocks
+        GatherArgs g;
+        std::memset(&g, 0, sizeof g);
+        g.n = n_segments;
+        g.out = layer_out;
+        bool v8 = aligned(layer_out, 16);
+        int64_t o = 0;
+        for (int p = 0; p < n_segments; ++p) {
+            g.src[p] = segment_ptrs[p];
+            g.len[p] = segment_numels[p];
+            g.dst_off[p] = o;
+            v8 = v8 && aligned(segment_ptrs[p], 16) && (o % 8 == 0);
+            o += segment_numels[p];
+        }
+        const int vec = v8 ? 8 : 1;
+        const int64_t tile = (int64_t)TILE_THREADS * vec * (vec == 8 ? GATHER_UNROLL : 2);
+        int64_t t = 0;
+        for (int p = 0; p < n_segments; ++p) {
+            g.tile_begin[p] = t;
+            t += (g.len[p] + tile - 1) / tile;
+        }
+        g.tile_begin[n_segments] = t;
+        return launch_gather(g, vec, static_cast<cudaStream_t>(stream), ctas);
+    }
+    // A CTA with an SM of its own gets the deeper pipeline; many CTAs share the
+    // bandwidth with smaller ones.
+    const bool few = 2 * (int64_t)ctas <= sms;
+    b.chunk = few ? 32768 : 16384;
+    b.stages = few ? 6 : 4;
+    int64_t c = 0;
+    for (int p = 0; p < n_segments; ++p) {
+        b.chunk_begin[p] = c;
+        c += (b.mid[p] + b.chunk - 1) / b.chunk;
+    }
+    b.chunk_begin[n_segments] = c;
+    if (ctas > c) ctas = (int)(c > 0 ? c : 1);
+    if (ctas > MAX_BLOCKS) ctas = MAX_BLOCKS;
+    b.spin_limit = spin_limit();
+    b.drain_limit = SPIN_LIMIT;
+    return launch_gather_bulk(b, ctas, static_cast<cudaStream_t>(stream));
 }
 
 int zero3_reduce_bucket(const void* const* bucket_ptrs, int world_size, int owner, int64_t unit_numel, int grad_dtype,

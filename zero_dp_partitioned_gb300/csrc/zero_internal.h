@@ -43,7 +43,25 @@ int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStr
 int launch_recover(const StepArgs& a, int pdt, cudaStream_t s);
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s);
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s);
-int launch_gather(const GatherArgs& a, int vec, cudaStream_t s);
+int launch_gather(const GatherArgs& a, int vec, cudaStream_t s, int max_grid = 0);
+
+// The TMA-moved gather (zero_gather_bulk.cu).  Offsets and sizes in bytes;
+// piece p is head[p] unaligned bytes, mid[p] bytes moved in chunks (a
+// multiple of 16, starting 16-byte aligned at both ends), then the rest.
+struct BulkGatherArgs {
+    const uint8_t* src[ZERO_MAX_SLICES];
+    int64_t bytes[ZERO_MAX_SLICES];
+    int64_t dst_off[ZERO_MAX_SLICES];
+    int64_t head[ZERO_MAX_SLICES];
+    int64_t mid[ZERO_MAX_SLICES];
+    int64_t chunk_begin[ZERO_MAX_SLICES + 1];   // first chunk of each piece's middle; [n] = chunk count
+    uint8_t* out;
+    int32_t* status;                            // bit 0 set by a CTA whose wait ran out
+    int n, chunk, stages;
+    unsigned spin_limit, drain_limit;
+};
+size_t gather_bulk_smem(int chunk, int stages);
+int launch_gather_bulk(const BulkGatherArgs& a, int grid, cudaStream_t s);
 
 // The shared-memory-staged passes (zero_stream.cu): selected only by
 // ZERO_GB300_PATH=stream; on GB300 they are slower than the register-staged

@@ -611,9 +611,14 @@ struct GatherArgs {
     void* out;
 };
 
+// Each thread moves GATHER_UNROLL vectors per tile, all loads issued before
+// the first store, so that a block keeps GATHER_UNROLL * 256 vectors in flight.
+constexpr int GATHER_UNROLL = 8;
+
 template <int VEC>
 __global__ void __launch_bounds__(TILE_THREADS) k_gather(const __grid_constant__ GatherArgs a) {
-    constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC * 2;   // two vectors per thread per tile
+    constexpr int U = VEC == 8 ? GATHER_UNROLL : 2;
+    constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC * U;
     const int64_t n_tiles = a.tile_begin[a.n];
     uint16_t* O = static_cast<uint16_t*>(a.out);
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -624,19 +629,25 @@ __global__ void __launch_bounds__(TILE_THREADS) k_gather(const __grid_constant__
         const uint16_t* src = static_cast<const uint16_t*>(a.src[p]);
         uint16_t* dst = O + a.dst_off[p];
         const int64_t j0 = t * TILE + (int64_t)threadIdx.x * VEC;
-        const int64_t j1 = j0 + (int64_t)TILE_THREADS * VEC;
         if (VEC == 8) {
-            const bool f0 = j0 + 8 <= L, f1 = j1 + 8 <= L;
-            uint4 w0, w1;
-            if (f0) w0 = ld_stream(src + j0);
-            if (f1) w1 = ld_stream(src + j1);
-            if (f0) __stcs(reinterpret_cast<uint4*>(dst + j0), w0);
-            else for (int64_t i = j0; i < L; ++i) dst[i] = src[i];
-            if (f1) __stcs(reinterpret_cast<uint4*>(dst + j1), w1);
-            else for (int64_t i = j1; i < L; ++i) dst[i] = src[i];
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t j = j0 + (int64_t)u * TILE_THREADS * VEC;
+                if (j + 8 <= L) w[u] = ld_stream(src + j);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t j = j0 + (int64_t)u * TILE_THREADS * VEC;
+                if (j + 8 <= L) __stcs(reinterpret_cast<uint4*>(dst + j), w[u]);
+                else for (int64_t i = j; i < L; ++i) dst[i] = src[i];
+            }
         } else {
-            if (j0 < L) dst[j0] = src[j0];
-            if (j1 < L) dst[j1] = src[j1];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t j = j0 + (int64_t)u * TILE_THREADS;
+                if (j < L) dst[j] = src[j];
+            }
         }
     }
 }

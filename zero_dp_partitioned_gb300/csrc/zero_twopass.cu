@@ -47,9 +47,10 @@ int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s) {
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "apply launch");
 }
 
-int launch_gather(const GatherArgs& a, int vec, cudaStream_t s) {
+int launch_gather(const GatherArgs& a, int vec, cudaStream_t s, int max_grid) {
     const void* f = vec == 8 ? (const void*)k_gather<8> : (const void*)k_gather<1>;
-    const int grid = grid_for(f, a.tile_begin[a.n], BPS_GATHER);
+    int grid = grid_for(f, a.tile_begin[a.n], BPS_GATHER);
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
     void* args[] = {const_cast<GatherArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "gather launch");
 }
