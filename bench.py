@@ -283,6 +283,54 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                 formula_bytes=bytes_step, sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
 
 
+def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None):
+    """The small fp16 group (Psi = 70,282, N_d = 3, all ranks, S = 1024): a
+    launch-bound step.  Its 2.3 MB of inputs fit in L2, so every step first
+    writes a 256 MB buffer (an L2 flush); the flush is inside the step time,
+    and the library call alone is timed by events around it."""
+    wl = W.workload("tiny-nd3")
+    nd = wl.nd
+    numels = W.numels(wl.specs)
+    plan = Z.zero_plan(numels, nd)
+    P = plan["padded_total"]
+    flat = W.flat_params(wl.specs, P, torch.float16, wl.param_seed, dev)
+    grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
+        [torch.empty(P, dtype=torch.float16, device=dev) for _ in range(nd)], wl.specs, lambda s: wl.grad_std,
+        wl.loss_scale)
+    sets = [[flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)],
+            [torch.empty(P, device=dev) for _ in range(3)]]
+
+    def shards(cur):
+        i, o = sets[cur], sets[1 - cur]
+        return [Z.shard(n, off, off, i[0][off:off + n], i[1][off:off + n], i[2][off:off + n],
+                        o[0][off:off + n], o[1][off:off + n], o[2][off:off + n])
+                for off, n in zip(plan["rank_offsets"], plan["rank_numels"])]
+
+    variants = [shards(0), shards(1)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
+    res = torch.zeros(48, dtype=torch.uint8, device=dev)
+    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    st = dict(cur=0, t=1, S=wl.loss_scale)
+
+    def step(from_host=False):
+        flush.fill_(st["t"] & 0xFF)
+        with timer("fused pass+k_recover"):
+            Z.zero_shard_step(grads, Z.ZERO_F16, variants[st["cur"]], flat, Z.ZERO_F16, _hyper(Z, wl.hyper, st["t"]),
+                              st["S"], 0.0, 0, ws, ws.numel(), res)
+        _finish_step(Z, torch, res, res_h, st)
+
+    bytes_step = (2 * nd + 26) * P
+    return dict(name="tiny-nd3", step=step, state=st, elements=P, nd=nd, launches_per_step=2,
+                kernel_bytes={"fused pass+k_recover": bytes_step}, dominant_label=None, h2d=None, d2h=48,
+                e2e_ok=False, formula_bytes=bytes_step, sample_for_cpu=None,
+                config={"workload": "tiny-nd3: three tensors [257,129], [129], [1000,37] (Psi = 70,282), N_d=3, "
+                                    "all ranks, fp16, S = 1024",
+                        "psi": sum(numels), "padded": P, "n_d": nd, "path": "fused single pass",
+                        "l2": "inputs fit in L2: a 256 MB write before every step flushes it (inside the step "
+                              "time); the kernels' own time is in kernels.*.ms_per_launch"})
+
+
 def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None):
     """The GPT-2 1.5B group with stage 1's full all-reduce: the reduce pass
     writes the whole averaged gradient (the all-reduce result every rank
@@ -721,7 +769,7 @@ def cpu_sample_gpt2(W, n_per_shard):
     return nd, grads, flat.view(torch.int16).numpy().view(np.uint16).copy(), wl.hyper
 
 
-WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_allreduce,
+WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_allreduce, "tiny-nd3": tiny_nd3,
              "llama3-8b-nd4-r1": llama_rank_local,
              "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama,
              "zero3-bcast-llama3-8b": zero3_broadcast, "zero3-prefetch-llama3-8b": zero3_prefetch}

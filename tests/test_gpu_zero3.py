@@ -267,18 +267,21 @@ def test_gather_bulk_is_exact(Z, n_ctas):
 
 
 def test_gather_bulk_equals_gather_layer_on_llama_parts(Z):
-    """World-size-4 parts of a Llama-3-8B-shaped block unit cut to 1/64
-    (3,408,000 elements): the TMA gather on 8 CTAs equals zero3_gather_layer."""
-    U, nd = 3_408_000, 4
+    """One Llama-3-8B block unit (218,112,000 elements, world-size-4 parts of
+    54,528,000; 436 MB, larger than L2): the TMA gather on every SM and on 32
+    CTAs equals zero3_gather_layer."""
+    U, nd = 218_112_000, 4
     rng = np.random.default_rng(3)
-    parts = [dev16(rng.integers(0, 1 << 16, U // nd, dtype=np.uint64).astype(np.uint16), 2) for _ in range(nd)]
+    parts = [dev16(rng.integers(0, 1 << 16, U // nd, dtype=np.uint16), 2) for _ in range(nd)]
     a = torch.empty(U, dtype=torch.bfloat16, device=DEV)
     b = torch.empty(U, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     Z.zero3_gather_layer(parts, U, Z.ZERO_BF16, a)
-    Z.zero3_gather_bulk(parts, [U // nd] * nd, Z.ZERO_BF16, b, 8, status)
-    torch.cuda.synchronize()
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and int(status.item()) == 0
+    for n_ctas in (0, 32):
+        b.zero_()
+        Z.zero3_gather_bulk(parts, [U // nd] * nd, Z.ZERO_BF16, b, n_ctas, status)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and int(status.item()) == 0
 
 
 def test_gather_bulk_wait_timeout_is_reported_and_harmless(Z, monkeypatch):
