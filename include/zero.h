@@ -211,7 +211,9 @@ typedef struct {
  * path       which kernels ran the update: 1 = fused single pass (register
  *            staged), 2 = apply pass (register staged), 3 = fused single pass
  *            through shared-memory stages fed by bulk asynchronous (TMA)
- *            copies, 4 = apply pass through such stages
+ *            copies, 4 = apply pass through such stages, 5 = fused single
+ *            pass with a producer warp issuing TMA copies into stages that
+ *            consumer warps work from
  * status     0, or ZERO_ETIMEOUT when a device-side wait gave up: the step is
  *            then reported as not applied, the parameters are restored, and
  *            the *_out state is indeterminate (for an in-place update that is
@@ -235,10 +237,12 @@ typedef struct {
  * on the device.
  *
  * Environment (read at each call; meant for tests and measurements):
- *   ZERO_GB300_PATH=stream            run the fused and apply passes through
- *       shared-memory stages fed by bulk asynchronous copies where the
- *       alignment rules below allow it (default: the register-staged
- *       kernels, which measure faster on GB300)
+ *   ZERO_GB300_PATH=register          the register-staged kernels only
+ *   ZERO_GB300_PATH=stream            the fused and apply passes through
+ *       shared-memory stages with a block-wide cycle per chunk, where the
+ *       alignment rules below allow it (slower on GB300; kept for comparison)
+ *   ZERO_GB300_PATH=ws                the producer/consumer fused pass where
+ *       allowed (what the default picks too)
  *   ZERO_GB300_SPIN_LIMIT=n           tries per device-side wait of the
  *       shared-memory-staged kernels (default 4194304); 0 makes every first
  *       wait give up, which exercises the ZERO_ETIMEOUT path without hanging
@@ -277,10 +281,14 @@ size_t zero_workspace_bytes(void);
  * state and the parameters once; if the step is not applied a second, short
  * kernel restores the parameters from master_in (parameters always equal
  * round16(master)).  Otherwise two passes: reduce into grad_shard (required
- * then), then apply.  With ZERO_GB300_PATH=stream the fused and apply
- * passes run through shared-memory stages fed by bulk asynchronous copies
- * when there are at most 8 slices and every slice address (+ grad_offset),
- * state pointer and grad_shard is 16-byte aligned.
+ * then), then apply.  The fused pass runs as a producer warp issuing bulk
+ * asynchronous (TMA) copies into shared-memory stages for consumer warps
+ * (path 5) when there are at most 8 slices and every slice address
+ * (+ grad_offset) and state pointer is 16-byte aligned; otherwise (and with
+ * ZERO_GB300_PATH=register) register-staged (path 1).  With
+ * ZERO_GB300_PATH=stream the fused and apply passes run through stages with a
+ * block-wide cycle per chunk under the same alignment rules (grad_shard
+ * 16-byte aligned too).
  * Errors: ZERO_EINVAL, ZERO_EALIGN (16-bit pointers must be 2-byte aligned,
  * fp32 pointers 4-byte aligned), ZERO_EWORKSPACE, ZERO_ELIMIT, ZERO_ECUDA. */
 int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype,

@@ -29,14 +29,15 @@ def Z():
     return Z
 
 
-@pytest.fixture(params=["register", "stream"])
+@pytest.fixture(params=["default", "register", "stream"])
 def kernel_path(request, monkeypatch):
-    """Run a test on the default (register-staged) kernels and again with the
-    shared-memory-staged ones selected wherever the alignment allows them."""
-    if request.param == "stream":
-        monkeypatch.setenv("ZERO_GB300_PATH", "stream")
-    else:
+    """Run a test on the default kernels (the producer/consumer fused pass
+    wherever the alignment allows it), on the register-staged kernels only,
+    and on the shared-memory-staged passes with a block-wide cycle."""
+    if request.param == "default":
         monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+    else:
+        monkeypatch.setenv("ZERO_GB300_PATH", request.param)
     return request.param
 
 
@@ -350,24 +351,37 @@ def test_staged_kernels_ragged_and_unaligned_params(Z, dt, numel, param_off, mon
     assert set(_staged_rank_local(Z, numel, 8, dt, param_off, 0.05, S=S)) == {4}      # two-pass, staged apply
 
 
-def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch):
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("numel,param_off,nd", [(896, 0, 8), (1792 * 7 + 5, 8, 8), (123457, 3, 4), (5000, 6, 1),
+                                               (7, 0, 2), (2049, 2, 8), (300001, 0, 3)])
+def test_producer_consumer_fused_pass_ragged_and_unaligned(Z, dt, numel, param_off, nd, monkeypatch):
+    """The producer/consumer fused pass over 896-element chunks: exact chunk
+    multiples, ragged tails, shards shorter than one bulk unit, parameter slots
+    at every alignment, 1-8 slices; bit-exact against the oracle."""
+    monkeypatch.setenv("ZERO_GB300_PATH", "ws")
+    S = 256.0 if dt == 1 else 1.0
+    assert set(_staged_rank_local(Z, numel, nd, dt, param_off, 0.0, S=S)) == {5}
+
+
+@pytest.mark.parametrize("path", ["stream", "ws"])
+def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch, path):
     """With the wait limit at 0 every first mbarrier wait of the staged
     kernels gives up: the step must come back as not applied with status
     ZERO_ETIMEOUT, the parameters and the *_in state unchanged, and the next
     call (limit restored) must be correct -- the context stays usable."""
-    monkeypatch.setenv("ZERO_GB300_PATH", "stream")
+    monkeypatch.setenv("ZERO_GB300_PATH", path)
     numel, nd, dt = 200000, 4, 2
     p = {"rank_offsets": np.array([0]), "rank_numels": np.array([numel])}
     flat = t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 0.02, W.generator(5, "cpu")))
     staged = [t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 1e-3, W.generator(6 + j, "cpu")))
               for j in range(nd)]
-    for clip in (0.0, 0.5):                      # fused pass, then the apply pass
+    for clip in ((0.0, 0.5) if path == "stream" else (0.0,)):      # fused pass, then the apply pass
         run = DeviceRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
         h = hyper32(max_grad_norm=clip)
         before = [x.clone() for x in run.state[0]["A"]]
         monkeypatch.setenv("ZERO_GB300_SPIN_LIMIT", "0")
         r = run.step(staged, h, 1, 1.0, grad_offsets=[0])
-        assert r.status == Z.ZERO_ETIMEOUT and r.applied == 0 and r.path in (3, 4)
+        assert r.status == Z.ZERO_ETIMEOUT and r.applied == 0 and r.path in ((3, 4) if path == "stream" else (5,))
         assert np.array_equal(t2u16(run.flat), flat)
         for x, y in zip(run.state[0]["A"], before):
             assert torch.equal(x, y)
@@ -383,11 +397,14 @@ def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch):
 
 
 @pytest.mark.parametrize("dt", [1, 2])
-def test_register_path_reports_register_kernels(Z, dt, monkeypatch):
-    monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+def test_each_path_reports_its_kernels(Z, dt, monkeypatch):
     S = 256.0 if dt == 1 else 1.0
+    monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {5}       # producer/consumer fused
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}      # register apply
+    assert set(_staged_rank_local(Z, 50001, 12, dt, 8, 0.0, S=S, steps=2)) == {1}      # > 8 slices: register
+    monkeypatch.setenv("ZERO_GB300_PATH", "register")
     assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {1}
-    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}
 
 
 def test_stage1_full_allreduce_then_shard_update(Z):
@@ -419,14 +436,19 @@ def test_stage1_full_allreduce_then_shard_update(Z):
         compare(run, osh, oflat, Z.read_result(run.res), ro, True)
 
 
+@pytest.mark.parametrize("path", ["register", "default"])
 @pytest.mark.parametrize("dt", [1, 2])
 @pytest.mark.parametrize("total,nd", [(48, 2), (80, 2), (4096 + 48, 2), (3 * 8 * 1000 + 24, 3), (64 * 1024 + 16, 4)])
-def test_unaligned_shard_heads(Z, dt, total, nd, monkeypatch):
-    """Shards that start 16 bytes past a 128-byte line take a head of up to 63
-    elements one by one so the vector loop starts aligned; heads shorter
-    than, equal to and longer than the shard, on the fused and the two-pass
-    path, must not change a bit."""
-    monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
+def test_unaligned_shard_heads(Z, dt, total, nd, path, monkeypatch):
+    """Shards that start 16 bytes past a 128-byte line: the register passes
+    take a head of up to 63 elements one by one so the vector loop starts
+    aligned; heads shorter than, equal to and longer than the shard, on the
+    fused and the two-pass path, must not change a bit.  The default fused
+    pass (producer/consumer) runs the same shards."""
+    if path == "register":
+        monkeypatch.setenv("ZERO_GB300_PATH", "register")
+    else:
+        monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
     S = 512.0 if dt == 1 else 1.0
     run_both(Z, [total], nd, dt, 0, total + nd, hyper32(), S, True, steps=2)
     run_both(Z, [total], nd, dt, 0, total + nd, hyper32(max_grad_norm=0.01), S, False, steps=2, grad_std=1e-2)

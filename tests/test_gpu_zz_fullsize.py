@@ -156,7 +156,7 @@ def test_gpt2_1p5b_all_ranks(Z):
         acc, ovf = oracle_stats(grads, dt, 0, P)
         r_gpu = Z.read_result(res)
         k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
-        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (1, 3)
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (1, 3, 5)
         assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
         cur ^= 1
         for s in samp:

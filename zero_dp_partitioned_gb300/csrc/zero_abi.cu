@@ -58,10 +58,14 @@ int grid_for(const void* func, int64_t n_tiles, int max_per_sm) {
 }
 
 // Implementation choice and wait limit, from the environment (tests and measurements).
-static int path_choice() {          // 1 register (default), 2 staged
+// 0 default (the producer/consumer fused pass where allowed, else register),
+// 1 register only, 2 staged with a block-wide cycle, 3 producer/consumer.
+static int path_choice() {
     const char* e = std::getenv("ZERO_GB300_PATH");
+    if (e && !std::strcmp(e, "register")) return 1;
     if (e && !std::strcmp(e, "stream")) return 2;
-    return 1;
+    if (e && !std::strcmp(e, "ws")) return 3;
+    return 0;
 }
 
 static unsigned spin_limit() {
@@ -236,6 +240,31 @@ static int run_stream(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s)
     return launch_stream(sa, gdt, pdt, fused, s);
 }
 
+// Chunks of `chunk` elements numbered shard after shard (no head).
+static void number_chunks(StepArgs& a, int64_t chunk) {
+    int64_t t = 0;
+    for (int i = 0; i < a.n_shards; ++i) {
+        ShardDev& d = a.shards[i];
+        d.head = 0;
+        d.tile_begin = t;
+        t += (d.numel + chunk - 1) / chunk;
+    }
+    a.n_tiles = t;
+}
+
+static bool ws_ok(const StepArgs& a) { return stream_ok(a, true) && ws_stages(a.n_slices) >= 2; }
+
+static int run_fused_ws(StepArgs& a, int gdt, int pdt, cudaStream_t s) {
+    StreamArgs sa;
+    std::memset(&sa, 0, sizeof sa);
+    number_chunks(a, ws_chunk());
+    sa.a = a;
+    sa.stages = ws_stages(a.n_slices);
+    sa.spin_limit = spin_limit();
+    sa.drain_limit = SPIN_LIMIT;
+    return launch_fused_ws(sa, gdt, pdt, s);
+}
+
 static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
     if (!ws) return fail(ZERO_EWORKSPACE, "workspace is NULL");
     if (ws_bytes < WS_BYTES) return fail(ZERO_EWORKSPACE, "workspace smaller than zero_workspace_bytes()");
@@ -403,6 +432,8 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
         a.k = (float)(1.0 / (double)loss_scale);
         if (choice == 2 && stream_ok(a, true)) {
             if ((rc = run_stream(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
+        } else if ((choice == 0 || choice == 3) && ws_ok(a)) {
+            if ((rc = run_fused_ws(a, grad_dtype, param_dtype, s)) != ZERO_OK) return rc;
         } else {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
             number_tiles(a, vec, HEAD_GRADS);
@@ -473,29 +504,21 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
 }
 
 // Copy n segments end to end into out (the layer buffer).
-static int gather_segments(const void* const* src, const int64_t* len, int n, int dtype, void* out, void* stream) {
-    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "unknown dtype");
-    if (n < 1) return fail(ZERO_EINVAL, "no segments");
-    if (n > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "more than ZERO_MAX_SLICES segments");
-    if (!src || !len || !out) return fail(ZERO_EINVAL, "NULL pointer");
-    if (!aligned(out, 2)) return fail(ZERO_EALIGN, "layer_out not 2-byte aligned");
-    GatherArgs g;
+// The register-staged gather's arguments for n pieces laid end to end in out
+// (pointers and lengths already validated); returns the vector width.
+static int gather_args(const void* const* src, const int64_t* len, int n, void* out, GatherArgs& g) {
     std::memset(&g, 0, sizeof g);
     g.n = n;
     g.out = out;
     int64_t off = 0;
     bool v8 = aligned(out, 16);
     for (int p = 0; p < n; ++p) {
-        if (len[p] < 0) return fail(ZERO_EINVAL, "negative segment length");
-        if (len[p] > 0 && !src[p]) return fail(ZERO_EINVAL, "a segment pointer is NULL");
-        if (!aligned(src[p], 2)) return fail(ZERO_EALIGN, "segment pointer not 2-byte aligned");
         g.src[p] = src[p];
         g.len[p] = len[p];
         g.dst_off[p] = off;
         v8 = v8 && aligned(src[p], 16) && (off % 8 == 0);
         off += len[p];
     }
-    if (off == 0) return ZERO_OK;
     const int vec = v8 ? 8 : 1;
     const int64_t tile = (int64_t)TILE_THREADS * vec * (vec == 8 ? GATHER_UNROLL : 2);
     int64_t t = 0;
@@ -504,6 +527,35 @@ static int gather_segments(const void* const* src, const int64_t* len, int n, in
         t += (g.len[p] + tile - 1) / tile;
     }
     g.tile_begin[n] = t;
+    return vec;
+}
+
+// Checks shared by the gathers; returns ZERO_OK and the total length in *total.
+static int check_pieces(const char* who, const void* const* src, const int64_t* len, int n, int dtype, void* out,
+                        int64_t* total) {
+    std::string w(who);
+    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, (w + ": unknown dtype").c_str());
+    if (n < 1) return fail(ZERO_EINVAL, (w + ": no segments").c_str());
+    if (n > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, (w + ": more than ZERO_MAX_SLICES segments").c_str());
+    if (!src || !len || !out) return fail(ZERO_EINVAL, (w + ": NULL pointer").c_str());
+    if (!aligned(out, 2)) return fail(ZERO_EALIGN, (w + ": layer_out not 2-byte aligned").c_str());
+    int64_t off = 0;
+    for (int p = 0; p < n; ++p) {
+        if (len[p] < 0) return fail(ZERO_EINVAL, (w + ": negative segment length").c_str());
+        if (len[p] > 0 && !src[p]) return fail(ZERO_EINVAL, (w + ": a segment pointer is NULL").c_str());
+        if (!aligned(src[p], 2)) return fail(ZERO_EALIGN, (w + ": segment pointer not 2-byte aligned").c_str());
+        off += len[p];
+    }
+    *total = off;
+    return ZERO_OK;
+}
+
+static int gather_segments(const void* const* src, const int64_t* len, int n, int dtype, void* out, void* stream) {
+    int64_t total = 0;
+    int rc = check_pieces("zero3_gather", src, len, n, dtype, out, &total);
+    if (rc != ZERO_OK || total == 0) return rc;
+    GatherArgs g;
+    const int vec = gather_args(src, len, n, out, g);
     return launch_gather(g, vec, static_cast<cudaStream_t>(stream));
 }
 
@@ -528,14 +580,18 @@ int zero3_gather_segments(const void* const* segment_ptrs, const int64_t* segmen
 
 int zero3_gather_bulk(const void* const* segment_ptrs, const int64_t* segment_numels, int n_segments, int dtype,
                       void* layer_out, int n_ctas, int32_t* status, void* stream) {
-    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "zero3_gather_bulk: unknown dtype");
-    if (n_segments < 1) return fail(ZERO_EINVAL, "zero3_gather_bulk: no segments");
-    if (n_segments > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "zero3_gather_bulk: more than ZERO_MAX_SLICES segments");
-    if (!segment_ptrs || !segment_numels || !layer_out || !status)
-        return fail(ZERO_EINVAL, "zero3_gather_bulk: NULL pointer");
+    if (!status) return fail(ZERO_EINVAL, "zero3_gather_bulk: NULL status");
     if (n_ctas < 0) return fail(ZERO_EINVAL, "zero3_gather_bulk: negative n_ctas");
     if (!aligned(status, 4)) return fail(ZERO_EINVAL, "zero3_gather_bulk: status not 4-byte aligned");
-    if (!aligned(layer_out, 2)) return fail(ZERO_EALIGN, "zero3_gather_bulk: layer_out not 2-byte aligned");
+    int64_t total = 0;
+    int rc = check_pieces("zero3_gather_bulk", segment_ptrs, segment_numels, n_segments, dtype, layer_out, &total);
+    if (rc != ZERO_OK || total == 0) return rc;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "zero3_gather_bulk: device query");
+    int ctas = n_ctas == 0 ? sms : n_ctas;
+
     BulkGatherArgs b;
     std::memset(&b, 0, sizeof b);
     b.n = n_segments;
@@ -545,9 +601,6 @@ int zero3_gather_bulk(const void* const* segment_ptrs, const int64_t* segment_nu
     int64_t off = 0;
     for (int p = 0; p < n_segments; ++p) {
         const int64_t L = segment_numels[p];
-        if (L < 0) return fail(ZERO_EINVAL, "zero3_gather_bulk: negative segment length");
-        if (L > 0 && !segment_ptrs[p]) return fail(ZERO_EINVAL, "zero3_gather_bulk: a segment pointer is NULL");
-        if (!aligned(segment_ptrs[p], 2)) return fail(ZERO_EALIGN, "zero3_gather_bulk: segment pointer not 2-byte aligned");
         const uintptr_t sa = reinterpret_cast<uintptr_t>(segment_ptrs[p]);
         const uintptr_t da = reinterpret_cast<uintptr_t>(layer_out) + 2 * (uintptr_t)off;
         if (L > 0 && (sa - da) % 16 != 0) congruent = false;
@@ -559,35 +612,10 @@ int zero3_gather_bulk(const void* const* segment_ptrs, const int64_t* segment_nu
         b.mid[p] = (b.bytes[p] - b.head[p]) / 16 * 16;
         off += L;
     }
-    if (off == 0) return ZERO_OK;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "zero3_gather_bulk: device query");
-    int ctas = n_ctas == 0 ? sms : n_ctas;
     if (!congruent) {
         // no bulk copies possible: the register-staged gather on at most `ctas` blocks
         GatherArgs g;
-        std::memset(&g, 0, sizeof g);
-        g.n = n_segments;
-        g.out = layer_out;
-        bool v8 = aligned(layer_out, 16);
-        int64_t o = 0;
-        for (int p = 0; p < n_segments; ++p) {
-            g.src[p] = segment_ptrs[p];
-            g.len[p] = segment_numels[p];
-            g.dst_off[p] = o;
-            v8 = v8 && aligned(segment_ptrs[p], 16) && (o % 8 == 0);
-            o += segment_numels[p];
-        }
-        const int vec = v8 ? 8 : 1;
-        const int64_t tile = (int64_t)TILE_THREADS * vec * (vec == 8 ? GATHER_UNROLL : 2);
-        int64_t t = 0;
-        for (int p = 0; p < n_segments; ++p) {
-            g.tile_begin[p] = t;
-            t += (g.len[p] + tile - 1) / tile;
-        }
-        g.tile_begin[n_segments] = t;
+        const int vec = gather_args(segment_ptrs, segment_numels, n_segments, layer_out, g);
         return launch_gather(g, vec, static_cast<cudaStream_t>(stream), ctas);
     }
     // A CTA with an SM of its own gets the deeper pipeline; many CTAs share the

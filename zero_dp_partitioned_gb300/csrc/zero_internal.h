@@ -71,6 +71,12 @@ struct StreamArgs;
 int stream_stages(int n_grad_arrays);
 int launch_stream(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
 
+// The fused pass with a producer warp and consumer warps (zero_ws.cu):
+// chunks of ws_chunk() elements, ws_stages(n) shared-memory stages.
+int ws_chunk();
+int ws_stages(int n_slices);
+int launch_fused_ws(const StreamArgs& sa, int gdt, int pdt, cudaStream_t s);
+
 // Kernel addresses, for the occupancy query.
 const void* fused_kernel(int gdt, int pdt, int vec, int ns);
 const void* reduce_kernel(int gdt, int vec, int ns);
