@@ -240,14 +240,18 @@ static int run_stream(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s)
     return launch_stream(sa, gdt, pdt, fused, s);
 }
 
-// Chunks of `chunk` elements numbered shard after shard (no head).
+// Chunks of `chunk` elements numbered shard after shard, after each shard's
+// head (the elements before its gradient slices reach a 128-byte boundary);
+// a shard that is all head still gets one chunk, whose block does the head.
 static void number_chunks(StepArgs& a, int64_t chunk) {
     int64_t t = 0;
     for (int i = 0; i < a.n_shards; ++i) {
         ShardDev& d = a.shards[i];
-        d.head = 0;
+        d.head = shard_head(a, d, HEAD_GRADS);
+        if (d.head > d.numel) d.head = d.numel;
         d.tile_begin = t;
-        t += (d.numel + chunk - 1) / chunk;
+        const int64_t rest = d.numel - d.head;
+        t += d.numel == 0 ? 0 : (rest > 0 ? (rest + chunk - 1) / chunk : 1);
     }
     a.n_tiles = t;
 }

@@ -17,9 +17,12 @@
 // No block-wide barrier inside the loop: each consumer warp runs as far ahead
 // as the loaded stages let it, and the producer keeps every free stage busy.
 //
-// Chunks are numbered shard after shard; a chunk's bulk part is its length
-// rounded down to 8 elements, and a shard's last (fewer than 8) elements are
-// loaded and stored with plain accesses.  Every wait is bounded; a wait that
+// Chunks are numbered shard after shard.  A shard's first d.head elements
+// (fewer than 64) are done one by one, so that its chunks start where the
+// gradient slices sit on a 128-byte boundary (a copy that starts mid-line
+// fetches one line more); a chunk's bulk part is its length rounded down to
+// 8 elements, and a shard's last (fewer than 8) elements are loaded and
+// stored with plain accesses.  Every wait is bounded; a wait that
 // runs out marks the block's flags and the step is reported as not applied.
 // Before the block finishes, the producer waits (bounded again) for the last
 // loads it issued, whether or not a consumer took them.
@@ -66,6 +69,23 @@ __device__ __forceinline__ void ws_issue(const StepArgs& a, const ShardDev& d, i
     bulk_load(stage + so + 2 * WS_CHUNK * 4, d.vi + c0, blen * 4u, bar);
 }
 
+// One element by plain loads and stores (a shard's head and last few elements).
+template <int GDT, int PDT>
+__device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, SumSq& sumsq,
+                                        int& flags) {
+    uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+    const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
+    if (Half16<GDT>::nonfinite(h)) flags |= FLAG_OVERFLOW;
+    const float af = Half16<GDT>::widen(h);
+    sumsq.add_fp64(af);
+    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
+    adamw1(th, mm, vv, af, k, a.sc);
+    d.mo[i] = th;
+    d.mmo[i] = mm;
+    d.vo[i] = vv;
+    P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
+}
+
 template <int GDT, int PDT>
 __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(const __grid_constant__ StreamArgs sa) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -105,10 +125,10 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
                 const int64_t chunk = blockIdx.x + j * G;
                 while (si + 1 < a.n_shards && a.shards[si + 1].tile_begin <= chunk) ++si;
                 const ShardDev& d = a.shards[si];
-                const int64_t c0 = (chunk - d.tile_begin) * WS_CHUNK;
+                const int64_t c0 = d.head + (chunk - d.tile_begin) * WS_CHUNK;
                 const int64_t rem = d.numel - c0;
-                ws_issue(a, d, c0, rem < WS_CHUNK ? rem : WS_CHUNK, stage0 + (uint32_t)st * stage_bytes,
-                         full0 + 8 * st);
+                ws_issue(a, d, c0, rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK,
+                         stage0 + (uint32_t)st * stage_bytes, full0 + 8 * st);
                 if (++st == S) {        // the uses of round r >= 1 wait for the consumption of round r - 1
                     st = 0;
                     if (j >= S) phase ^= 1u;
@@ -134,11 +154,13 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
             const int64_t chunk = blockIdx.x + j * G;
             while (si + 1 < a.n_shards && a.shards[si + 1].tile_begin <= chunk) ++si;
             const ShardDev& d = a.shards[si];
-            const int64_t c0 = (chunk - d.tile_begin) * WS_CHUNK;
+            const int64_t it = chunk - d.tile_begin;
+            const int64_t c0 = d.head + it * WS_CHUNK;
             const int64_t rem = d.numel - c0;
-            const int64_t len = rem < WS_CHUNK ? rem : WS_CHUNK;
+            const int64_t len = rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK;
             const int64_t blen = len & ~int64_t(7);
             const uint8_t* in = smem + WS_HEADER + (size_t)st * stage_bytes;
+            if (it == 0 && e0 / V < d.head) ws_elem<GDT, PDT>(a, d, e0 / V, k, sumsq, flags);   // the shard's head
             if (e0 + V <= blen) {
                 float sv[V];
 #pragma unroll
@@ -198,19 +220,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
             } else if (e0 < len) {
                 // the shard's last (fewer than 8) elements: plain loads and stores
                 const int64_t end = (e0 + V < len) ? e0 + V : len;
-                for (int64_t e = (e0 > blen ? e0 : blen); e < end; ++e) {
-                    const int64_t i = c0 + e;
-                    const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
-                    if (Half16<GDT>::nonfinite(h)) flags |= FLAG_OVERFLOW;
-                    const float af = Half16<GDT>::widen(h);
-                    sumsq.add_fp64(af);
-                    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
-                    adamw1(th, mm, vv, af, k, a.sc);
-                    d.mo[i] = th;
-                    d.mmo[i] = mm;
-                    d.vo[i] = vv;
-                    P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
-                }
+                for (int64_t e = (e0 > blen ? e0 : blen); e < end; ++e) ws_elem<GDT, PDT>(a, d, c0 + e, k, sumsq, flags);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
