@@ -185,7 +185,8 @@ def _hyper(Z, h, t, clip=0.0):
 
 PATH_NAMES = {1: "k_step_fused (register-staged)", 2: "k_apply (register-staged)",
               3: "k_stream<fused> (TMA bulk-copy staged)", 4: "k_stream<apply> (TMA bulk-copy staged)",
-              5: "k_fused_ws (producer warp, TMA stages, consumer warps)"}
+              5: "k_ws<fused> (producer warp, TMA stages, consumer warps)",
+              6: "k_ws<apply> (producer warp, TMA stages, consumer warps)"}
 
 
 def _finish_step(Z, torch, res, res_h, st):

@@ -213,7 +213,7 @@ typedef struct {
  *            through shared-memory stages fed by bulk asynchronous (TMA)
  *            copies, 4 = apply pass through such stages, 5 = fused single
  *            pass with a producer warp issuing TMA copies into stages that
- *            consumer warps work from
+ *            consumer warps work from, 6 = apply pass built the same way
  * status     0, or ZERO_ETIMEOUT when a device-side wait gave up: the step is
  *            then reported as not applied, the parameters are restored, and
  *            the *_out state is indeterminate (for an in-place update that is
@@ -241,8 +241,9 @@ typedef struct {
  *   ZERO_GB300_PATH=stream            the fused and apply passes through
  *       shared-memory stages with a block-wide cycle per chunk, where the
  *       alignment rules below allow it (slower on GB300; kept for comparison)
- *   ZERO_GB300_PATH=ws                the producer/consumer fused pass where
- *       allowed (what the default picks too)
+ *   ZERO_GB300_PATH=ws                the producer/consumer fused and apply
+ *       passes where allowed (the default picks the fused one; its apply
+ *       pass is slower than the register one on GB300)
  *   ZERO_GB300_SPIN_LIMIT=n           tries per device-side wait of the
  *       shared-memory-staged kernels (default 4194304); 0 makes every first
  *       wait give up, which exercises the ZERO_ETIMEOUT path without hanging
@@ -285,7 +286,9 @@ size_t zero_workspace_bytes(void);
  * asynchronous (TMA) copies into shared-memory stages for consumer warps
  * (path 5) when there are at most 8 slices and every slice address
  * (+ grad_offset) and state pointer is 16-byte aligned; otherwise (and with
- * ZERO_GB300_PATH=register) register-staged (path 1).  With
+ * ZERO_GB300_PATH=register) register-staged (path 1).  The apply pass is
+ * register-staged (path 2); ZERO_GB300_PATH=ws runs it the producer/consumer
+ * way (path 6) when every state pointer and grad_shard is aligned.  With
  * ZERO_GB300_PATH=stream the fused and apply passes run through stages with a
  * block-wide cycle per chunk under the same alignment rules (grad_shard
  * 16-byte aligned too).

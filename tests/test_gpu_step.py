@@ -29,11 +29,12 @@ def Z():
     return Z
 
 
-@pytest.fixture(params=["default", "register", "stream"])
+@pytest.fixture(params=["default", "register", "stream", "ws"])
 def kernel_path(request, monkeypatch):
     """Run a test on the default kernels (the producer/consumer fused pass
     wherever the alignment allows it), on the register-staged kernels only,
-    and on the shared-memory-staged passes with a block-wide cycle."""
+    on the shared-memory-staged passes with a block-wide cycle, and on both
+    producer/consumer passes."""
     if request.param == "default":
         monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
     else:
@@ -352,15 +353,18 @@ def test_staged_kernels_ragged_and_unaligned_params(Z, dt, numel, param_off, mon
 
 
 @pytest.mark.parametrize("dt", [1, 2])
-@pytest.mark.parametrize("numel,param_off,nd", [(896, 0, 8), (1792 * 7 + 5, 8, 8), (123457, 3, 4), (5000, 6, 1),
+@pytest.mark.parametrize("numel,param_off,nd", [(1792, 0, 8), (1792 * 7 + 5, 8, 8), (123457, 3, 4), (5000, 6, 1),
                                                (7, 0, 2), (2049, 2, 8), (300001, 0, 3)])
-def test_producer_consumer_fused_pass_ragged_and_unaligned(Z, dt, numel, param_off, nd, monkeypatch):
-    """The producer/consumer fused pass over 896-element chunks: exact chunk
-    multiples, ragged tails, shards shorter than one bulk unit, parameter slots
-    at every alignment, 1-8 slices; bit-exact against the oracle."""
+def test_producer_consumer_passes_ragged_and_unaligned(Z, dt, numel, param_off, nd, monkeypatch):
+    """The producer/consumer fused and apply passes over 1792-element chunks:
+    exact chunk multiples, ragged tails, shards shorter than one bulk unit,
+    parameter slots at every alignment, 1-8 slices; the fused pass bit-exact
+    against the oracle, the apply pass (after clipping) within the step's
+    tolerances."""
     monkeypatch.setenv("ZERO_GB300_PATH", "ws")
     S = 256.0 if dt == 1 else 1.0
     assert set(_staged_rank_local(Z, numel, nd, dt, param_off, 0.0, S=S)) == {5}
+    assert set(_staged_rank_local(Z, numel, nd, dt, param_off, 0.05, S=S)) == {6}
 
 
 @pytest.mark.parametrize("path", ["stream", "ws"])
@@ -375,13 +379,13 @@ def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch, path):
     flat = t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 0.02, W.generator(5, "cpu")))
     staged = [t2u16(W.fill_normal_(torch.zeros(numel, dtype=torch.bfloat16), 1e-3, W.generator(6 + j, "cpu")))
               for j in range(nd)]
-    for clip in ((0.0, 0.5) if path == "stream" else (0.0,)):      # fused pass, then the apply pass
+    for clip in (0.0, 0.5):                      # fused pass, then the apply pass
         run = DeviceRun(Z, p, flat, dt, [0], pingpong=(clip == 0.0))
         h = hyper32(max_grad_norm=clip)
         before = [x.clone() for x in run.state[0]["A"]]
         monkeypatch.setenv("ZERO_GB300_SPIN_LIMIT", "0")
         r = run.step(staged, h, 1, 1.0, grad_offsets=[0])
-        assert r.status == Z.ZERO_ETIMEOUT and r.applied == 0 and r.path in ((3, 4) if path == "stream" else (5,))
+        assert r.status == Z.ZERO_ETIMEOUT and r.applied == 0 and r.path in ((3, 4) if path == "stream" else (5, 6))
         assert np.array_equal(t2u16(run.flat), flat)
         for x, y in zip(run.state[0]["A"], before):
             assert torch.equal(x, y)
@@ -405,6 +409,7 @@ def test_each_path_reports_its_kernels(Z, dt, monkeypatch):
     assert set(_staged_rank_local(Z, 50001, 12, dt, 8, 0.0, S=S, steps=2)) == {1}      # > 8 slices: register
     monkeypatch.setenv("ZERO_GB300_PATH", "register")
     assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {1}
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}
 
 
 def test_stage1_full_allreduce_then_shard_update(Z):

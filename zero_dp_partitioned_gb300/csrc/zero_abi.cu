@@ -58,8 +58,11 @@ int grid_for(const void* func, int64_t n_tiles, int max_per_sm) {
 }
 
 // Implementation choice and wait limit, from the environment (tests and measurements).
-// 0 default (the producer/consumer fused pass where allowed, else register),
-// 1 register only, 2 staged with a block-wide cycle, 3 producer/consumer.
+// 0 default (the producer/consumer fused pass where allowed, else register;
+// the register apply pass), 1 register only, 2 staged with a block-wide
+// cycle, 3 producer/consumer fused and apply passes.  The producer/consumer
+// apply pass measured slower than the register one on GB300 (the Llama-3-8B
+// shard: 9.52 ms against 8.56 ms), so only ZERO_GB300_PATH=ws selects it.
 static int path_choice() {
     const char* e = std::getenv("ZERO_GB300_PATH");
     if (e && !std::strcmp(e, "register")) return 1;
@@ -241,13 +244,14 @@ static int run_stream(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s)
 }
 
 // Chunks of `chunk` elements numbered shard after shard, after each shard's
-// head (the elements before its gradient slices reach a 128-byte boundary);
-// a shard that is all head still gets one chunk, whose block does the head.
-static void number_chunks(StepArgs& a, int64_t chunk) {
+// head (the elements before its dominant stream reaches a 128-byte
+// boundary); a shard that is all head still gets one chunk, whose block does
+// the head.
+static void number_chunks(StepArgs& a, int64_t chunk, int kind) {
     int64_t t = 0;
     for (int i = 0; i < a.n_shards; ++i) {
         ShardDev& d = a.shards[i];
-        d.head = shard_head(a, d, HEAD_GRADS);
+        d.head = shard_head(a, d, kind);
         if (d.head > d.numel) d.head = d.numel;
         d.tile_begin = t;
         const int64_t rest = d.numel - d.head;
@@ -256,17 +260,21 @@ static void number_chunks(StepArgs& a, int64_t chunk) {
     a.n_tiles = t;
 }
 
-static bool ws_ok(const StepArgs& a) { return stream_ok(a, true) && ws_stages(a.n_slices) >= 2; }
+// The producer/consumer passes need what the staged ones need (16-byte
+// aligned bulk-copy addresses, at most 8 slices) and two stages.
+static bool ws_ok(const StepArgs& a, bool fused) {
+    return stream_ok(a, fused) && ws_stages(fused ? a.n_slices : 1) >= 2;
+}
 
-static int run_fused_ws(StepArgs& a, int gdt, int pdt, cudaStream_t s) {
+static int run_ws(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s) {
     StreamArgs sa;
     std::memset(&sa, 0, sizeof sa);
-    number_chunks(a, ws_chunk());
+    number_chunks(a, ws_chunk(), fused ? HEAD_GRADS : HEAD_STATE);
     sa.a = a;
-    sa.stages = ws_stages(a.n_slices);
+    sa.stages = ws_stages(fused ? a.n_slices : 1);
     sa.spin_limit = spin_limit();
     sa.drain_limit = SPIN_LIMIT;
-    return launch_fused_ws(sa, gdt, pdt, s);
+    return launch_ws(sa, gdt, pdt, fused, s);
 }
 
 static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
@@ -436,8 +444,8 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
         a.k = (float)(1.0 / (double)loss_scale);
         if (choice == 2 && stream_ok(a, true)) {
             if ((rc = run_stream(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
-        } else if ((choice == 0 || choice == 3) && ws_ok(a)) {
-            if ((rc = run_fused_ws(a, grad_dtype, param_dtype, s)) != ZERO_OK) return rc;
+        } else if ((choice == 0 || choice == 3) && ws_ok(a, true)) {
+            if ((rc = run_ws(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
         } else {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
             number_tiles(a, vec, HEAD_GRADS);
@@ -454,6 +462,7 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
     number_tiles(a, vec, HEAD_GRADS);
     if ((rc = launch_reduce(a, grad_dtype, vec, s)) != ZERO_OK) return rc;
     if (choice == 2 && stream_ok(a, false)) return run_stream(a, grad_dtype, param_dtype, false, s);
+    if (choice == 3 && ws_ok(a, false)) return run_ws(a, grad_dtype, param_dtype, false, s);
     vec = vec8_ok(a, 3) ? 8 : 1;
     number_tiles(a, vec, HEAD_STATE);
     return launch_apply(a, grad_dtype, param_dtype, vec, s);
@@ -500,14 +509,16 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
     a.stats = const_cast<zero_stats*>(stats);
     a.result = result;
     if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
-    if (path_choice() == 2 && stream_ok(a, false))
+    const int choice = path_choice();
+    if (choice == 2 && stream_ok(a, false))
         return run_stream(a, grad_dtype, param_dtype, false, static_cast<cudaStream_t>(stream));
+    if (choice == 3 && ws_ok(a, false))
+        return run_ws(a, grad_dtype, param_dtype, false, static_cast<cudaStream_t>(stream));
     const int vec = vec8_ok(a, 3) ? 8 : 1;
     number_tiles(a, vec, HEAD_STATE);
     return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));
 }
 
-// Copy n segments end to end into out (the layer buffer).
 // The register-staged gather's arguments for n pieces laid end to end in out
 // (pointers and lengths already validated); returns the vector width.
 static int gather_args(const void* const* src, const int64_t* len, int n, void* out, GatherArgs& g) {

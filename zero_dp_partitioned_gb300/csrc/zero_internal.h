@@ -71,11 +71,12 @@ struct StreamArgs;
 int stream_stages(int n_grad_arrays);
 int launch_stream(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
 
-// The fused pass with a producer warp and consumer warps (zero_ws.cu):
-// chunks of ws_chunk() elements, ws_stages(n) shared-memory stages.
+// The fused and apply passes with a producer warp and consumer warps
+// (zero_ws.cu): chunks of ws_chunk() elements, ws_stages(ng) shared-memory
+// stages for ng 16-bit arrays (the slices, or the reduced gradient).
 int ws_chunk();
-int ws_stages(int n_slices);
-int launch_fused_ws(const StreamArgs& sa, int gdt, int pdt, cudaStream_t s);
+int ws_stages(int ng);
+int launch_ws(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
 
 // Kernel addresses, for the occupancy query.
 const void* fused_kernel(int gdt, int pdt, int vec, int ns);

@@ -49,35 +49,60 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__host__ __device__ inline uint32_t ws_stage_bytes(int n_slices) {
-    return (uint32_t)(2 * n_slices + 12) * WS_CHUNK;
+// Stage bytes for ng 16-bit arrays (the slices, or the reduced gradient) and
+// the three fp32 state arrays.
+__host__ __device__ inline uint32_t ws_stage_bytes(int ng) {
+    return (uint32_t)(2 * ng + 12) * WS_CHUNK;
 }
 
-// Loads of chunk `chunk` (of shard d, elements [c0, c0 + len)) into the stage at
-// smem offset `stage`: slices first (2 * WS_CHUNK bytes each), then master, m, v.
+// Loads of elements [c0, c0 + len) of shard d into the stage at smem offset
+// `stage`: the 16-bit arrays first (2 * WS_CHUNK bytes each: FUSED, every
+// slice at the shard's gradient offset; otherwise the reduced gradient), then
+// master, m, v.
+template <bool FUSED>
 __device__ __forceinline__ void ws_issue(const StepArgs& a, const ShardDev& d, int64_t c0, int64_t len,
                                          uint32_t stage, uint32_t bar) {
+    const int ng = FUSED ? a.n_slices : 1;
     const uint32_t blen = (uint32_t)(len & ~int64_t(7));
-    mbar_expect_tx(bar, blen * (2u * a.n_slices + 12u));
+    mbar_expect_tx(bar, blen * (2u * ng + 12u));
     if (blen == 0) return;
-    for (int r = 0; r < a.n_slices; ++r)
-        bulk_load(stage + (uint32_t)r * WS_CHUNK * 2, static_cast<const uint16_t*>(a.slices[r]) + d.grad_off + c0,
-                  blen * 2u, bar);
-    const uint32_t so = (uint32_t)a.n_slices * WS_CHUNK * 2;
+    for (int r = 0; r < ng; ++r) {
+        const uint16_t* src = FUSED ? static_cast<const uint16_t*>(a.slices[r]) + d.grad_off + c0
+                                    : static_cast<const uint16_t*>(d.gshard) + c0;
+        bulk_load(stage + (uint32_t)r * WS_CHUNK * 2, src, blen * 2u, bar);
+    }
+    const uint32_t so = (uint32_t)ng * WS_CHUNK * 2;
     bulk_load(stage + so, d.mi + c0, blen * 4u, bar);
     bulk_load(stage + so + WS_CHUNK * 4, d.mmi + c0, blen * 4u, bar);
     bulk_load(stage + so + 2 * WS_CHUNK * 4, d.vi + c0, blen * 4u, bar);
 }
 
+// V 16-bit values from shared memory as V/2 words.
+template <int V>
+__device__ __forceinline__ void load_halves(const uint8_t* p, uint32_t (&u)[V / 2]) {
+    if constexpr (V == 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        u[0] = w.x; u[1] = w.y;
+    }
+}
+
 // One element by plain loads and stores (a shard's head and last few elements).
-template <int GDT, int PDT>
+template <int GDT, int PDT, bool FUSED>
 __device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, SumSq& sumsq,
                                         int& flags) {
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
-    const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
-    if (Half16<GDT>::nonfinite(h)) flags |= FLAG_OVERFLOW;
+    uint32_t h;
+    if (FUSED) {
+        h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
+        if (Half16<GDT>::nonfinite(h)) flags |= FLAG_OVERFLOW;
+    } else {
+        h = static_cast<const uint16_t*>(d.gshard)[i];
+    }
     const float af = Half16<GDT>::widen(h);
-    sumsq.add_fp64(af);
+    if (FUSED) sumsq.add_fp64(af);
     float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
     adamw1(th, mm, vv, af, k, a.sc);
     d.mo[i] = th;
@@ -86,19 +111,36 @@ __device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, in
     P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
 }
 
-template <int GDT, int PDT>
-__global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(const __grid_constant__ StreamArgs sa) {
+// FUSED: reduce the slices, statistics, AdamW with multiplier a.k, and (last
+// block) the result.  Otherwise the apply pass: AdamW from the reduced
+// gradient with the decision every block derives from the statistics; on
+// overflow nothing is loaded or written.  Either way every block publishes
+// its flags and the last block to finish writes the result, so a timeout
+// anywhere is reported.
+template <int GDT, int PDT, bool FUSED>
+__global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __grid_constant__ StreamArgs sa) {
     extern __shared__ __align__(128) uint8_t smem[];
     const StepArgs& a = sa.a;
     const int S = sa.stages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ng = FUSED ? a.n_slices : 1;
     const uint32_t full0 = smem_addr(smem), empty0 = full0 + 8 * WS_MAX_STAGES;
     const uint32_t stage0 = full0 + WS_HEADER;
-    const uint32_t stage_bytes = ws_stage_bytes(a.n_slices);
+    const uint32_t stage_bytes = ws_stage_bytes(ng);
     const int64_t G = gridDim.x;
-    const int64_t n_local = a.n_tiles > (int64_t)blockIdx.x ? (a.n_tiles - 1 - blockIdx.x) / G + 1 : 0;
-    const float k = a.k;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
+
+    float k = a.k;
+    int overflow_in = 0;
+    double st_sumsq = 0.0, norm = 0.0, clip = 1.0;
+    if (!FUSED) {
+        const zero_stats st = *a.stats;
+        overflow_in = (st.overflow | a.extra_overflow) ? 1 : 0;
+        st_sumsq = st.sumsq + a.extra_sumsq;
+        k = grad_multiplier(st_sumsq, a.loss_scale, a.max_norm, norm, clip);
+    }
+    const int64_t n_local =
+        (!overflow_in && a.n_tiles > (int64_t)blockIdx.x) ? (a.n_tiles - 1 - blockIdx.x) / G + 1 : 0;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -127,8 +169,8 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
                 const ShardDev& d = a.shards[si];
                 const int64_t c0 = d.head + (chunk - d.tile_begin) * WS_CHUNK;
                 const int64_t rem = d.numel - c0;
-                ws_issue(a, d, c0, rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK,
-                         stage0 + (uint32_t)st * stage_bytes, full0 + 8 * st);
+                ws_issue<FUSED>(a, d, c0, rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK,
+                                stage0 + (uint32_t)st * stage_bytes, full0 + 8 * st);
                 if (++st == S) {        // the uses of round r >= 1 wait for the consumption of round r - 1
                     st = 0;
                     if (j >= S) phase ^= 1u;
@@ -160,27 +202,37 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
             const int64_t len = rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK;
             const int64_t blen = len & ~int64_t(7);
             const uint8_t* in = smem + WS_HEADER + (size_t)st * stage_bytes;
-            if (it == 0 && e0 / V < d.head) ws_elem<GDT, PDT>(a, d, e0 / V, k, sumsq, flags);   // the shard's head
+            if (it == 0 && e0 / V < d.head) ws_elem<GDT, PDT, FUSED>(a, d, e0 / V, k, sumsq, flags);   // the head
             if (e0 + V <= blen) {
-                float sv[V];
+                uint32_t hg[V];                   // the averaged (FUSED) or reduced 16-bit gradient
+                if (FUSED) {
+                    float sv[V];
 #pragma unroll
-                for (int e = 0; e < V; ++e) sv[e] = 0.0f;
-                for (int r = 0; r < a.n_slices; ++r) {
-                    uint32_t u[V / 2];
-                    if constexpr (V == 8) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(in + (size_t)r * WS_CHUNK * 2 + e0 * 2);
-                        u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w;
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2*>(in + (size_t)r * WS_CHUNK * 2 + e0 * 2);
-                        u[0] = w.x; u[1] = w.y;
+                    for (int e = 0; e < V; ++e) sv[e] = 0.0f;
+                    for (int r = 0; r < ng; ++r) {
+                        uint32_t u[V / 2];
+                        load_halves<V>(in + (size_t)r * WS_CHUNK * 2 + e0 * 2, u);
+#pragma unroll
+                        for (int q = 0; q < V / 2; ++q) {
+                            sv[2 * q] = __fadd_rn(sv[2 * q], Half16<GDT>::widen(u[q] & 0xFFFFu));
+                            sv[2 * q + 1] = __fadd_rn(sv[2 * q + 1], Half16<GDT>::widen(u[q] >> 16));
+                        }
                     }
+#pragma unroll
+                    for (int e = 0; e < V; ++e) {
+                        hg[e] = average16<GDT>(sv[e], a.divisor);
+                        if (Half16<GDT>::nonfinite(hg[e])) flags |= FLAG_OVERFLOW;
+                    }
+                } else {
+                    uint32_t u[V / 2];
+                    load_halves<V>(in + e0 * 2, u);
 #pragma unroll
                     for (int q = 0; q < V / 2; ++q) {
-                        sv[2 * q] = __fadd_rn(sv[2 * q], Half16<GDT>::widen(u[q] & 0xFFFFu));
-                        sv[2 * q + 1] = __fadd_rn(sv[2 * q + 1], Half16<GDT>::widen(u[q] >> 16));
+                        hg[2 * q] = u[q] & 0xFFFFu;
+                        hg[2 * q + 1] = u[q] >> 16;
                     }
                 }
-                const uint8_t* sin = in + (size_t)a.n_slices * WS_CHUNK * 2;
+                const uint8_t* sin = in + (size_t)ng * WS_CHUNK * 2;
                 float th[V], mm[V], vv[V];
 #pragma unroll
                 for (int q = 0; q < V / 4; ++q) {
@@ -195,9 +247,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
                 uint32_t hp[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
-                    const uint32_t h = average16<GDT>(sv[e], a.divisor);
-                    if (Half16<GDT>::nonfinite(h)) flags |= FLAG_OVERFLOW;
-                    af[e] = Half16<GDT>::widen(h);
+                    af[e] = Half16<GDT>::widen(hg[e]);
                     adamw1(th[e], mm[e], vv[e], af[e], k, a.sc);
                 }
 #pragma unroll
@@ -206,8 +256,10 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
                     hp[e] = w & 0xFFFFu;
                     hp[e + 1] = w >> 16;
                 }
-                if constexpr (V == 8) sumsq.add8(*reinterpret_cast<const float(*)[8]>(af));
-                else sumsq.add4(*reinterpret_cast<const float(*)[4]>(af));
+                if (FUSED) {
+                    if constexpr (V == 8) sumsq.add8(*reinterpret_cast<const float(*)[8]>(af));
+                    else sumsq.add4(*reinterpret_cast<const float(*)[4]>(af));
+                }
 #pragma unroll
                 for (int q = 0; q < V / 4; ++q) {
                     const int e = 4 * q;
@@ -220,7 +272,8 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
             } else if (e0 < len) {
                 // the shard's last (fewer than 8) elements: plain loads and stores
                 const int64_t end = (e0 + V < len) ? e0 + V : len;
-                for (int64_t e = (e0 > blen ? e0 : blen); e < end; ++e) ws_elem<GDT, PDT>(a, d, c0 + e, k, sumsq, flags);
+                for (int64_t e = (e0 > blen ? e0 : blen); e < end; ++e)
+                    ws_elem<GDT, PDT, FUSED>(a, d, c0 + e, k, sumsq, flags);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -231,7 +284,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
         }
     }
 
-    double acc = sumsq.total();
+    double acc = FUSED ? sumsq.total() : 0.0;
     block_reduce(acc, flags);
     if (!publish_partial(a, acc, flags)) return;
     double sum;
@@ -239,40 +292,50 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_fused_ws(con
     combine_partials(a, sum, flag);
     if (threadIdx.x == 0) {
         zero_result r;
-        r.overflow = ((flag & FLAG_OVERFLOW) || a.extra_overflow) ? 1 : 0;
-        r.sumsq = sum + a.extra_sumsq;
-        r.grad_norm = sqrt(r.sumsq) / a.loss_scale;
-        r.clip_coef = 1.0;
-        r.grad_mult = a.k;
+        if (FUSED) {
+            r.overflow = ((flag & FLAG_OVERFLOW) || a.extra_overflow) ? 1 : 0;
+            r.sumsq = sum + a.extra_sumsq;
+            r.grad_norm = sqrt(r.sumsq) / a.loss_scale;
+            r.clip_coef = 1.0;
+            r.grad_mult = a.k;
+        } else {
+            r.overflow = overflow_in;
+            r.sumsq = st_sumsq;
+            r.grad_norm = norm;
+            r.clip_coef = clip;
+            r.grad_mult = k;
+        }
         r.status = (flag & FLAG_TIMEOUT) ? ZERO_ETIMEOUT : 0;
         r.applied = (r.overflow || r.status) ? 0 : 1;
-        r.path = 5;
+        r.path = FUSED ? 5 : 6;
         r.reserved = 0.0f;
         *a.result = r;
     }
 }
 
 template <int G, int P>
-static const void* ws_ptr() {
-    return (const void*)k_fused_ws<G, P>;
+static const void* ws_ptr(bool fused) {
+    return fused ? (const void*)k_ws<G, P, true> : (const void*)k_ws<G, P, false>;
 }
 
-static const void* ws_kernel(int gdt, int pdt) {
-    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? ws_ptr<ZERO_BF16, ZERO_BF16>() : ws_ptr<ZERO_BF16, ZERO_F16>();
-    return pdt == ZERO_BF16 ? ws_ptr<ZERO_F16, ZERO_BF16>() : ws_ptr<ZERO_F16, ZERO_F16>();
+static const void* ws_kernel(int gdt, int pdt, bool fused) {
+    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? ws_ptr<ZERO_BF16, ZERO_BF16>(fused)
+                                                  : ws_ptr<ZERO_BF16, ZERO_F16>(fused);
+    return pdt == ZERO_BF16 ? ws_ptr<ZERO_F16, ZERO_BF16>(fused) : ws_ptr<ZERO_F16, ZERO_F16>(fused);
 }
 
 int ws_chunk() { return WS_CHUNK; }
 
-// Stages of a block: as many as fit 110 KB (two blocks share an SM), at most 8.
-int ws_stages(int n_slices) {
-    const int s = (int)((110 * 1024 - WS_HEADER) / ws_stage_bytes(n_slices));
+// Stages of a block for ng 16-bit arrays: as many as fit 110 KB (two blocks
+// share an SM), at most 8.
+int ws_stages(int ng) {
+    const int s = (int)((110 * 1024 - WS_HEADER) / ws_stage_bytes(ng));
     return s > WS_MAX_STAGES ? WS_MAX_STAGES : s;
 }
 
-int launch_fused_ws(const StreamArgs& sa, int gdt, int pdt, cudaStream_t s) {
-    const void* f = ws_kernel(gdt, pdt);
-    const size_t smem = WS_HEADER + (size_t)sa.stages * ws_stage_bytes(sa.a.n_slices);
+int launch_ws(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s) {
+    const void* f = ws_kernel(gdt, pdt, fused);
+    const size_t smem = WS_HEADER + (size_t)sa.stages * ws_stage_bytes(fused ? sa.a.n_slices : 1);
     static std::mutex mu;
     static std::unordered_map<const void*, size_t> configured[16];
     int dev = 0;
@@ -282,7 +345,7 @@ int launch_fused_ws(const StreamArgs& sa, int gdt, int pdt, cudaStream_t s) {
         size_t& have = configured[dev & 15][f];
         if (have < smem) {
             int rc = cuda_fail(cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                               "raising the shared-memory limit of the producer/consumer fused kernel");
+                               "raising the shared-memory limit of the producer/consumer kernel");
             if (rc != ZERO_OK) return rc;
             have = smem;
         }
@@ -290,7 +353,7 @@ int launch_fused_ws(const StreamArgs& sa, int gdt, int pdt, cudaStream_t s) {
     const int grid = grid_for_smem(f, sa.a.n_tiles, smem, WS_BLOCKS_PER_SM);
     void* args[] = {const_cast<StreamArgs*>(&sa)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, smem, s),
-                     "producer/consumer fused kernel launch");
+                     "producer/consumer kernel launch");
 }
 
 }  // namespace zdp
