@@ -168,13 +168,16 @@ class KernelTimer:
         return _Ctx()
 
     def per_kind(self, steps):
-        out = {}
+        out, each = {}, {}
         for kind, a, b in self.events:
             d = out.setdefault(kind, {"ms_total": 0.0, "launches": 0})
-            d["ms_total"] += a.elapsed_time(b)
+            ms = a.elapsed_time(b)
+            d["ms_total"] += ms
             d["launches"] += 1
-        for d in out.values():
+            each.setdefault(kind, []).append(ms)
+        for kind, d in out.items():
             d["ms_per_launch"] = d["ms_total"] / d["launches"]
+            d["ms_median"] = statistics.median(each[kind])
             d["ms_per_step"] = d["ms_total"] / steps
         return out
 
@@ -999,7 +1002,7 @@ def main():
     roofline = {"bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dk["achieved_gbs"] / peak, "traffic": ncu_traffic(wl["name"], dom),
                 "peak_source": peak_src, "kernel": f"{dom} [{wl['config']['update_kernel']}]",
-                "kernel_ms_per_launch": dk["ms_per_launch"],
+                "kernel_ms_per_launch": dk["ms_per_launch"], "kernel_ms_median": dk["ms_median"],
                 "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"],
                 "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": dk["achieved_gbs"] / NOMINAL_HBM_GBS}
     if roofline["traffic"] is not None:
