@@ -63,10 +63,10 @@ struct BulkGatherArgs {
 size_t gather_bulk_smem(int chunk, int stages);
 int launch_gather_bulk(const BulkGatherArgs& a, int grid, cudaStream_t s);
 
-// The shared-memory-staged passes (zero_stream.cu): selected only by
-// ZERO_GB300_PATH=stream; on GB300 they are slower than the register-staged
-// passes (14.1 ms vs 10.8 ms for the fused GPT-2 step), so the default is the
-// register path.
+// The shared-memory-staged passes with a block-wide cycle per chunk
+// (zero_stream.cu): selected only by ZERO_GB300_PATH=stream; on GB300 they
+// are slower than the register-staged passes (14.1 ms vs 10.8 ms for the
+// fused GPT-2 step at the time) and than the producer/consumer fused pass.
 struct StreamArgs;
 int stream_stages(int n_grad_arrays);
 int launch_stream(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);

@@ -1,5 +1,9 @@
 // zero_stream.cuh -- TMA-pipelined versions of the two write-heavy passes
-// (the fused single pass for up to 8 gradient slices, and the apply pass).
+// (the fused single pass for up to 8 gradient slices, and the apply pass),
+// with one block-wide cycle per chunk; opt-in (ZERO_GB300_PATH=stream).  The
+// producer/consumer passes in zero_ws.cu split the same work between a
+// producer lane and consumer warps without that cycle.  This file also holds
+// the PTX wrappers (mbarrier, bulk copies) the TMA kernels share.
 //
 // Why: the register-staged kernels keep at most ~4 blocks of 256 threads per
 // SM (64 / 50 registers), so the bytes they keep in flight, and with them the
