@@ -72,10 +72,17 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and blank lines are left
+    out, so that a capture stays valid across edits that change no code."""
+    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "zero_dp_partitioned_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        h.update(open(os.path.join(d, f), "rb").read())
+        text = open(os.path.join(d, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(f.encode() + b"\0" + code.encode() + b"\0")
     return h.hexdigest()[:16]
 
 
