@@ -217,7 +217,9 @@ typedef struct {
  * status     0, or ZERO_ETIMEOUT when a device-side wait gave up: the step is
  *            then reported as not applied, the parameters are restored, and
  *            the *_out state is indeterminate (for an in-place update that is
- *            the state itself: treat the state as lost)
+ *            the state itself: treat the state as lost); ZERO_ELIMIT for a
+ *            chained step whose t lies outside its scalar table (nothing is
+ *            updated)
  * sumsq      sum of squares of the scaled reduced gradient plus extra_sumsq
  * grad_norm  sqrt(sumsq) / loss_scale
  * clip_coef  max_grad_norm / (grad_norm + 1e-6) when that is below 1, else 1
@@ -413,6 +415,65 @@ int zero_shard_step_noalloc(const void* const* grad_slices, int n_slices, int gr
                             void* flat_param, int param_dtype,
                             const zero_hyper* hyper, float loss_scale,
                             double extra_sumsq, int extra_overflow,
+                            zero_result* result, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Steps chained on the device.  zero_shard_step leaves the bookkeeping of a
+ * step to the caller: it reads zero_result, swaps the state sets, advances
+ * t or lowers S (DeepSpeed ZeRO stages 1-2 walkthrough, 6 step 1: on
+ * overflow the optimizer is not called and the loss scale is lowered) -- one
+ * device-to-host round trip per step.
+ * Here that bookkeeping lives in device memory, so that any number of steps
+ * can be enqueued (or captured in a CUDA graph and replayed) without the host
+ * waiting on one.
+ * ------------------------------------------------------------------------ */
+
+/* Device-resident state of a chain of steps, owned by the caller.
+ * cur         the current state set: 0 = every shard's *_in pointers, 1 = its
+ *             *_out pointers; the step reads set cur and writes set 1 - cur
+ * step        t of the next step (1-based)
+ * loss_scale  S of the next step
+ * applied, skipped, failed   steps applied, skipped on overflow, and ended
+ *             with a nonzero status
+ * After each step: applied -> step += 1 and cur ^= 1; overflow -> loss_scale
+ * halves (no hysteresis, as zero_shard_step's callers do); a nonzero status
+ * (timeout, or step outside the scalar table) changes nothing but `failed`. */
+typedef struct {
+    int32_t cur, reserved;
+    int64_t step;
+    double loss_scale;
+    int64_t applied, skipped, failed;
+} zero_chain;
+
+/* The two step-dependent AdamW scalars for steps t0 .. t0 + n - 1, computed
+ * on the host as zero_shard_step computes them (fp64, each rounded once to
+ * fp32): table_out[2 i] = lr / (1 - beta1^t), table_out[2 i + 1] =
+ * 1 / sqrt(1 - beta2^t) with t = t0 + i.  table_out: host, 2 n floats.  Copy
+ * it to the device for zero_shard_step_chained.  Returns ZERO_OK or
+ * ZERO_EINVAL (t0 < 1, n < 0, NULL pointers, hyper-parameters as
+ * zero_shard_step checks them). */
+int zero_adam_scalar_table(const zero_hyper* hyper, int64_t t0, int64_t n, float* table_out);
+
+/* One step with its bookkeeping on the device: what zero_shard_step computes
+ * for t = chain->step and S = chain->loss_scale, with the shards' two state
+ * sets used by turns (chain->cur), then the chain updated as zero_chain
+ * describes.  hyper->step is ignored.  Each shard's *_in and *_out must be
+ * two distinct sets (no in-place update: the set read must survive a
+ * skipped step).  Clipping (max_grad_norm > 0) takes the reduce and apply
+ * passes and needs grad_shard; otherwise the fused pass.
+ * scalar_table: device, 2 n_table floats from zero_adam_scalar_table for
+ * steps table_t0 .. table_t0 + n_table - 1; a step outside it is not
+ * applied and reports status ZERO_ELIMIT.  chain: device.  No host
+ * synchronisation; the calls of a chain must run in stream order.
+ * Errors as zero_shard_step, and ZERO_EINVAL for a NULL chain or table or a
+ * shard updated in place. */
+int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int grad_dtype,
+                            const zero_shard* shards, int n_shards,
+                            void* flat_param, int param_dtype,
+                            const zero_hyper* hyper, const float* scalar_table, int64_t table_t0,
+                            int64_t n_table, zero_chain* chain,
+                            double extra_sumsq, int extra_overflow,
+                            void* workspace, size_t workspace_bytes,
                             zero_result* result, void* stream);
 
 /* Message of the last error on this thread ("" if none). */

@@ -110,6 +110,18 @@ def test_mem_model_plan_equals_oracle(Z, orc):
             Z.zero_mem_model_plan(*bad)
 
 
+def test_adam_scalar_table_equals_oracle(Z, orc):
+    for lr, b1, b2, wd in ((1e-3, 0.9, 0.999, 0.01), (3e-4, 0.95, 0.98, 0.1), (1.0, 0.5, 0.5, 0.0)):
+        h = Z.hyper(lr=lr, beta1=b1, beta2=b2, weight_decay=wd, step=1)
+        tab = Z.zero_adam_scalar_table(h, 7, 50)
+        for i in range(50):
+            sc = orc.make_scalars(np.float32(lr), np.float32(b1), np.float32(b2), np.float32(1e-8), np.float32(wd),
+                                  7 + i)
+            assert tab[2 * i] == np.float32(sc.ss) and tab[2 * i + 1] == np.float32(sc.rb2)
+    with pytest.raises(Z.ZeroError):
+        Z.zero_adam_scalar_table(Z.hyper(), 0, 4)
+
+
 def test_argument_errors_before_any_device_work(Z):
     fake = 0x10000   # never dereferenced: every case below fails validation first
     ws = Z.zero_workspace_bytes()

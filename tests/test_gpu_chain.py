@@ -1,0 +1,195 @@
+"""GPU parity of chained steps: the step's bookkeeping (t, the loss scale, the
+state set in use) kept on the device by zero_shard_step_chained, against the
+CPU oracle driven with the same bookkeeping on the host (an overflowing step
+is skipped: t is not advanced and S halves), eagerly and replayed from a
+CUDA graph.  Unclipped steps are bit-exact; clipped ones follow the step's
+tolerances (the multiplier depends on an fp64 norm)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from helpers import hyper32, make_problem, t2u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+TDT = {1: torch.float16, 2: torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def Z():
+    import zero_dp_partitioned_gb300 as Z
+    return Z
+
+
+def dev16(a, dt):
+    return torch.from_numpy(a.view(np.int16).copy()).view(TDT[dt]).to(DEV)
+
+
+def chain_tensor(Z, step, S):
+    c = Z.chain(step=step, loss_scale=S)
+    return torch.frombuffer(bytearray(bytes(c)), dtype=torch.uint8).to(DEV)
+
+
+class ChainRun:
+    """Device copy of a problem with two state sets and a device chain."""
+
+    def __init__(self, Z, p, flat, dt, h, S, n_table=16):
+        self.Z, self.p, self.dt, self.h = Z, p, dt, h
+        P = flat.size
+        self.flat = dev16(flat, dt)
+        self.sets = [[self.flat.float(), torch.zeros(P, device=DEV), torch.zeros(P, device=DEV)],
+                     [torch.empty(P, device=DEV) for _ in range(3)]]
+        self.gshard = torch.empty(P, dtype=TDT[dt], device=DEV)
+        self.chain = chain_tensor(Z, 1, S)
+        self.hyper = Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], h["max_grad_norm"], 1)
+        self.table = torch.from_numpy(Z.zero_adam_scalar_table(self.hyper, 1, n_table)).to(DEV)
+        self.n_table = n_table
+        self.ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+        self.res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+        A, B = self.sets
+        self.shards = [Z.shard(int(n), int(o), int(o), *(x[int(o):int(o) + int(n)] for x in A),
+                               *(x[int(o):int(o) + int(n)] for x in B), self.gshard[int(o):int(o) + int(n)])
+                       for o, n in zip(p["rank_offsets"], p["rank_numels"])]
+
+    def step(self, slices_dev, stream=None):
+        self.Z.zero_shard_step_chained(slices_dev, self.dt, self.shards, self.flat, self.dt, self.hyper, self.table, 1,
+                                       self.n_table, self.chain, 0.0, 0, self.ws, self.ws.numel(), self.res,
+                                       stream=stream)
+
+    def state(self):
+        c = self.Z.read_chain(self.chain)
+        return c, [x.cpu().numpy() for x in self.sets[c.cur]]
+
+
+def oracle_run(p, flat, dt, h, S, grads):
+    """The oracle over the same steps with the host bookkeeping."""
+    osh = [dict(numel=int(n), grad_off=int(o), param_off=int(o), master=orc.widen_16(flat[int(o):int(o) + int(n)], dt),
+                m=np.zeros(int(n), np.float32), v=np.zeros(int(n), np.float32))
+           for o, n in zip(p["rank_offsets"], p["rank_numels"])]
+    oflat = flat.copy()
+    t, results = 1, []
+    for g in grads:
+        r, _ = orc.zero_step(g, dt, osh, oflat, dt, h, t, np.float32(S))
+        results.append(r)
+        if r.applied:
+            t += 1
+        else:
+            S /= 2
+    return osh, oflat, t, S, results
+
+
+def check(run, p, osh, oflat, exact):
+    c, (th, m, v) = run.state()
+    got_flat = t2u16(run.flat)
+    if exact:
+        assert np.array_equal(got_flat, oflat)
+    else:
+        assert np.abs(got_flat.astype(np.int32) - oflat.astype(np.int32)).max() <= 1
+    for o, n, os_ in zip(p["rank_offsets"], p["rank_numels"], osh):
+        o, n = int(o), int(n)
+        for got, ref in ((th[o:o + n], os_["master"]), (m[o:o + n], os_["m"]), (v[o:o + n], os_["v"])):
+            if exact:
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+            else:
+                # the clipped multiplier may differ by an ulp in a step (fp64 norm, summed in another order):
+                # 1e-5 relative, with a floor of 1e-3 of the array's largest value where the update cancels
+                ref64 = ref.astype(np.float64)
+                floor = 1e-3 * np.abs(ref64).max()
+                assert np.all(np.abs(got.astype(np.float64) - ref64) <= 1e-5 * np.maximum(np.abs(ref64), floor))
+    return c
+
+
+@pytest.mark.parametrize("numels,nd,dt", [([20000, 4096, 992], 4, 2), ([20000, 555], 3, 1), ([3000, 5000], 8, 2)])
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_chained_steps_match_the_oracle(Z, numels, nd, dt, clip):
+    """Five chained steps, the second with a NaN in one slice (skipped: t stays,
+    S halves), no host synchronisation in between."""
+    S = 256.0 if dt == 1 else 1.0
+    p, flat, grads = make_problem(numels, nd, dt, 0, 61, loss_scale=S, grad_std=1e-2, steps=5)
+    grads[1][0] = grads[1][0].copy()
+    grads[1][0][7] = 0x7E00 if dt == 1 else 0x7FC0
+    h = hyper32(max_grad_norm=clip)
+    run = ChainRun(Z, p, flat, dt, h, S)
+    slices = [[dev16(g, dt) for g in step] for step in grads]
+    for k in range(5):
+        run.step(slices[k])
+    torch.cuda.synchronize()
+    osh, oflat, t, So, results = oracle_run(p, flat, dt, h, S, grads)
+    assert [r.applied for r in results] == [1, 0, 1, 1, 1]
+    c = check(run, p, osh, oflat, clip <= 0.0)
+    assert (c.step, c.loss_scale, c.applied, c.skipped, c.failed) == (t, So, 4, 1, 0)
+    r = Z.read_result(run.res)
+    assert r.applied == 1 and r.status == 0
+
+
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_chained_steps_replayed_from_a_cuda_graph(Z, clip):
+    """Three chained steps captured in one CUDA graph and replayed twice equal
+    six eager chained steps from the same start, bit for bit."""
+    numels, nd, dt = [20000, 4096, 992], 4, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 62, grad_std=1e-2, steps=3)
+    h = hyper32(max_grad_norm=clip)
+    slices = [[dev16(g, dt) for g in step] for step in grads]
+    eager = ChainRun(Z, p, flat, dt, h, 1.0)
+    for _ in range(2):
+        for k in range(3):
+            eager.step(slices[k])
+    graphed = ChainRun(Z, p, flat, dt, h, 1.0)
+    warm = ChainRun(Z, p, flat, dt, h, 1.0)          # the library's one-time set-up, outside the capture
+    warm.step(slices[0])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        for k in range(3):
+            graphed.step(slices[k])
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    ce, se = eager.state()
+    cg, sg = graphed.state()
+    assert ce.as_dict() == cg.as_dict() and ce.step == 7
+    assert torch.equal(eager.flat.view(torch.int16), graphed.flat.view(torch.int16))
+    for a, b in zip(se, sg):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_chained_step_outside_its_table_changes_nothing(Z):
+    numels, nd, dt = [20000, 4096, 992], 4, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 63, grad_std=1e-2, steps=3)
+    h = hyper32()
+    run = ChainRun(Z, p, flat, dt, h, 1.0, n_table=2)
+    slices = [[dev16(g, dt) for g in step] for step in grads]
+    run.step(slices[0])
+    run.step(slices[1])
+    torch.cuda.synchronize()
+    c2, s2 = run.state()
+    f2 = t2u16(run.flat)
+    run.step(slices[2])
+    torch.cuda.synchronize()
+    c3, s3 = run.state()
+    r = Z.read_result(run.res)
+    assert r.applied == 0 and r.status == Z.ZERO_ELIMIT
+    assert (c3.step, c3.cur, c3.applied, c3.failed) == (3, c2.cur, 2, 1)
+    assert np.array_equal(t2u16(run.flat), f2)
+    for a, b in zip(s2, s3):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_chained_step_argument_errors(Z):
+    numels, nd, dt = [4096], 2, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 64, steps=1)
+    run = ChainRun(Z, p, flat, dt, hyper32(), 1.0)
+    slices = [dev16(g, dt) for g in grads[0]]
+    inplace = [Z.shard(s.numel, s.grad_offset, s.param_offset, s.master_in, s.m_in, s.v_in, s.master_in, s.m_in,
+                       s.v_in) for s in run.shards]
+    for kw, code in ((dict(shards=inplace), Z.ZERO_EINVAL), (dict(chain_dev=0), Z.ZERO_EINVAL),
+                     (dict(n_table=0), Z.ZERO_EINVAL), (dict(table=0), Z.ZERO_EINVAL)):
+        args = dict(shards=run.shards, chain_dev=run.chain, n_table=run.n_table, table=run.table)
+        args.update(kw)
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_step_chained(slices, dt, args["shards"], run.flat, dt, run.hyper, args["table"], 1,
+                                      args["n_table"], args["chain_dev"], 0.0, 0, run.ws, run.ws.numel(), run.res)
+        assert e.value.code == code

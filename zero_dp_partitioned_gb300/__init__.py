@@ -47,6 +47,15 @@ class zero_stats(ctypes.Structure):
     _fields_ = [("sumsq", ctypes.c_double), ("overflow", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class zero_chain(ctypes.Structure):
+    _fields_ = [("cur", ctypes.c_int32), ("reserved", ctypes.c_int32), ("step", ctypes.c_int64),
+                ("loss_scale", ctypes.c_double), ("applied", ctypes.c_int64), ("skipped", ctypes.c_int64),
+                ("failed", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if not k.startswith("reserved")}
+
+
 class zero_result(ctypes.Structure):
     _fields_ = [("overflow", ctypes.c_int32), ("applied", ctypes.c_int32), ("path", ctypes.c_int32),
                 ("status", ctypes.c_int32), ("sumsq", ctypes.c_double), ("grad_norm", ctypes.c_double),
@@ -78,6 +87,9 @@ _SIGS = {
     "zero3_gather_bulk": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
     "zero3_reduce_bucket": (_I, [_P, _I, _I, _I64, _I, _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "zero_shard_step_noalloc": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P, _P]),
+    "zero_adam_scalar_table": (_I, [_P, _I64, _I64, _P]),
+    "zero_shard_step_chained": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _P, _I64, _I64, _P, ctypes.c_double, _I, _P,
+                                     ctypes.c_size_t, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 # every symbol include/zero.h declares
@@ -248,6 +260,39 @@ def zero3_reduce_bucket(bucket_ptrs, owner, unit_numel, grad_dtype, grad_part, a
     _check(lib.zero3_reduce_bucket(_ptrs(bucket_ptrs), len(bucket_ptrs), owner, unit_numel, grad_dtype,
                                    _ptr(grad_part), int(accumulate), _ptr(stats), _ptr(workspace), workspace_bytes,
                                    _stream(stream)))
+
+
+def zero_adam_scalar_table(hyper, t0, n):
+    """The step-dependent AdamW scalars (lr / (1 - b1^t), 1 / sqrt(1 - b2^t)) for
+    t = t0 .. t0 + n - 1, as a host float32 array of 2 n values."""
+    import numpy as np
+    out = np.zeros(2 * int(n), np.float32)
+    _check(lib.zero_adam_scalar_table(ctypes.byref(hyper), int(t0), int(n), out.ctypes.data))
+    return out
+
+
+def chain(step=1, loss_scale=1.0, cur=0):
+    """A zero_chain to copy to the device (48 bytes) as the start of a chain."""
+    return zero_chain(cur, 0, step, loss_scale, 0, 0, 0)
+
+
+def read_chain(t) -> zero_chain:
+    """A zero_chain from a 48-byte tensor (device or host)."""
+    b = bytes(t.detach().cpu().view(-1).numpy().tobytes()) if hasattr(t, "detach") else bytes(t)
+    return zero_chain.from_buffer_copy(b[:ctypes.sizeof(zero_chain)])
+
+
+def zero_shard_step_chained(grad_slices, grad_dtype, shards, flat_param, param_dtype, hyper, scalar_table, table_t0,
+                            n_table, chain_dev, extra_sumsq, extra_overflow, workspace, workspace_bytes, result,
+                            stream=None):
+    """One step with its bookkeeping (t, S, the state set in use) in the device
+    zero_chain chain_dev; scalar_table: device float32, 2 n_table values."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_step_chained(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards),
+                                       _ptr(flat_param), param_dtype, ctypes.byref(hyper), _ptr(scalar_table),
+                                       int(table_t0), int(n_table), _ptr(chain_dev), extra_sumsq,
+                                       int(extra_overflow), _ptr(workspace), workspace_bytes, _ptr(result),
+                                       _stream(stream)))
 
 
 def read_result(t) -> zero_result:

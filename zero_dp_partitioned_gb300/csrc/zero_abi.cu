@@ -468,6 +468,83 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
     return launch_apply(a, grad_dtype, param_dtype, vec, s);
 }
 
+int zero_adam_scalar_table(const zero_hyper* hyper, int64_t t0, int64_t n, float* table_out) {
+    if (!hyper || t0 < 1 || n < 0 || (n > 0 && !table_out)) return fail(ZERO_EINVAL, "zero_adam_scalar_table: bad argument");
+    zero_hyper h = *hyper;
+    for (int64_t i = 0; i < n; ++i) {
+        h.step = t0 + i;
+        const AdamScalars c = adam_scalars(h);
+        table_out[2 * i] = c.ss;
+        table_out[2 * i + 1] = c.rb2;
+    }
+    return ZERO_OK;
+}
+
+int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
+                            int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper,
+                            const float* scalar_table, int64_t table_t0, int64_t n_table, zero_chain* chain,
+                            double extra_sumsq, int extra_overflow, void* workspace, size_t workspace_bytes,
+                            zero_result* result, void* stream) {
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (!hyper) return fail(ZERO_EINVAL, "hyper is NULL");
+    if (!chain || !aligned(chain, 8)) return fail(ZERO_EINVAL, "chain is NULL or not 8-byte aligned");
+    if (!scalar_table || !aligned(scalar_table, 4) || n_table < 1 || table_t0 < 1)
+        return fail(ZERO_EINVAL, "scalar_table is NULL or misaligned, or n_table / table_t0 < 1");
+    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
+    int rc;
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    if ((rc = pack_slices(a, grad_slices, n_slices)) != ZERO_OK) return rc;
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+    for (int i = 0; i < n_shards && shards; ++i)
+        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
+                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
+            return fail(ZERO_EINVAL, "zero_shard_step_chained: a shard updates its state in place; give two sets");
+    const bool fused = hyper->max_grad_norm <= 0.0f;
+    if ((rc = pack_shards(a, shards, n_shards, fused ? 1 : 2)) != ZERO_OK) return rc;
+    if (!fused && (rc = pack_shards(a, shards, n_shards, 3)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = flat_param;
+    zero_hyper h1 = *hyper;
+    h1.step = 1;
+    a.sc = adam_scalars(h1);              // t-independent scalars; ss and rb2 come from the table
+    a.max_norm = (double)hyper->max_grad_norm;
+    a.extra_sumsq = extra_sumsq;
+    a.extra_overflow = extra_overflow ? 1 : 0;
+    a.result = result;
+    a.chain = chain;
+    a.sc_table = scalar_table;
+    a.t0 = table_t0;
+    a.n_table = n_table;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (fused) {
+        // the fused pass derives k = fp32(1/S) from chain->loss_scale on the device
+        if (ws_ok(a, true) && path_choice() != 1) {
+            if ((rc = run_ws(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
+        } else {
+            const int vec = vec8_ok(a, 1) ? 8 : 1;
+            number_tiles(a, vec, HEAD_GRADS);
+            const int grid =
+                grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles,
+                         n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+            if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
+        }
+        if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
+    } else {
+        a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
+        a.accumulate = 0;
+        int vec = vec8_ok(a, 2) ? 8 : 1;
+        number_tiles(a, vec, HEAD_GRADS);
+        if ((rc = launch_reduce(a, grad_dtype, vec, s)) != ZERO_OK) return rc;
+        vec = vec8_ok(a, 3) ? 8 : 1;
+        number_tiles(a, vec, HEAD_STATE);
+        if ((rc = launch_apply(a, grad_dtype, param_dtype, vec, s)) != ZERO_OK) return rc;
+    }
+    return launch_chain_update(chain, result, s);
+}
+
 int zero_shard_reduce(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
                       int n_shards, int accumulate, zero_stats* stats, void* workspace, size_t workspace_bytes,
                       void* stream) {

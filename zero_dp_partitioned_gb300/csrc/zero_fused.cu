@@ -43,4 +43,27 @@ int launch_recover(const StepArgs& a, int pdt, cudaStream_t s) {
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "recover launch");
 }
 
+// ---------------------------------------------------------------- chained steps: the bookkeeping
+// After a chained step's kernels: applied -> next t, the other state set;
+// overflow -> half the loss scale; another failure -> counted only.
+__global__ void k_chain_update(zero_chain* chain, const zero_result* result) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const zero_result r = *result;
+    if (r.applied) {
+        chain->step += 1;
+        chain->cur ^= 1;
+        chain->applied += 1;
+    } else if (r.overflow && r.status == 0) {
+        chain->loss_scale *= 0.5;
+        chain->skipped += 1;
+    } else {
+        chain->failed += 1;
+    }
+}
+
+int launch_chain_update(zero_chain* chain, const zero_result* result, cudaStream_t s) {
+    k_chain_update<<<1, 32, 0, s>>>(chain, result);
+    return cuda_fail(cudaGetLastError(), "chain update launch");
+}
+
 }  // namespace zdp

@@ -80,6 +80,11 @@ struct StepArgs {
     unsigned* counter;
     zero_stats* stats;
     zero_result* result;
+    // chained steps (NULL chain otherwise): t, S and the state set in use come
+    // from *chain; the step-dependent scalars from sc_table (2 per step, from t0)
+    zero_chain* chain;
+    const float* sc_table;
+    int64_t t0, n_table;
 };
 
 // ---------------------------------------------------------------- 16-bit conversions
@@ -349,23 +354,71 @@ __device__ __forceinline__ float reduce1(const StepArgs& a, int64_t off) {
     return s;
 }
 
+// ---------------------------------------------------------------- per-step control
+// What a kernel needs of the step that is not in its arguments for a chained
+// step: the scalars, the multiplier, S, and which state set is read.
+struct Ctl {
+    AdamScalars sc;
+    float k;            // the fused pass's gradient multiplier, fp32(1/S)
+    double S;
+    bool sw;            // the state sets are used the other way round (chain->cur == 1)
+    bool bad;           // a chained step outside its scalar table: nothing is updated
+};
+
+__device__ __forceinline__ Ctl step_ctl(const StepArgs& a) {
+    Ctl c;
+    c.sc = a.sc;
+    c.k = a.k;
+    c.S = a.loss_scale;
+    c.sw = false;
+    c.bad = false;
+    if (a.chain) {
+        const int cur = __ldcg(&a.chain->cur);
+        const int64_t t = __ldcg(&a.chain->step);
+        c.S = __ldcg(&a.chain->loss_scale);
+        c.k = (float)(1.0 / c.S);
+        c.sw = cur != 0;
+        const int64_t i = t - a.t0;
+        if (i < 0 || i >= a.n_table) {
+            c.bad = true;
+        } else {
+            c.sc.ss = __ldg(a.sc_table + 2 * i);
+            c.sc.rb2 = __ldg(a.sc_table + 2 * i + 1);
+        }
+    }
+    return c;
+}
+
+// A shard's state set read and state set written.
+struct StatePtrs {
+    const float *mi, *mmi, *vi;
+    float *mo, *mmo, *vo;
+};
+
+__device__ __forceinline__ StatePtrs state_ptrs(const ShardDev& d, bool sw) {
+    if (!sw) return StatePtrs{d.mi, d.mmi, d.vi, d.mo, d.mmo, d.vo};
+    return StatePtrs{d.mo, d.mmo, d.vo, const_cast<float*>(d.mi), const_cast<float*>(d.mmi),
+                     const_cast<float*>(d.vi)};
+}
+
 // ---------------------------------------------------------------- one element at a time
 // The per-element bodies of the passes, for the elements the vector loops do
 // not cover (a shard's unaligned head and ragged tail, or everything on the
 // scalar path).  Same arithmetic as the vector bodies.
 template <int GDT, int PDT>
-__device__ __forceinline__ void fused_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, SumSq& sumsq,
-                                           int& ovf) {
+__device__ __forceinline__ void fused_elem(const StepArgs& a, const ShardDev& d, int64_t i, const Ctl& c,
+                                           SumSq& sumsq, int& ovf) {
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     const uint32_t h = average16<GDT>(reduce1<GDT>(a, d.grad_off + i), a.divisor);
     ovf |= Half16<GDT>::nonfinite(h);
     const float af = Half16<GDT>::widen(h);
     sumsq.add_fp64(af);
-    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
-    adamw1(th, mm, vv, af, k, a.sc);
-    d.mo[i] = th;
-    d.mmo[i] = mm;
-    d.vo[i] = vv;
+    const StatePtrs p = state_ptrs(d, c.sw);
+    float th = p.mi[i], mm = p.mmi[i], vv = p.vi[i];
+    adamw1(th, mm, vv, af, c.k, c.sc);
+    p.mo[i] = th;
+    p.mmo[i] = mm;
+    p.vo[i] = vv;
     P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
 }
 
@@ -378,13 +431,14 @@ __device__ __forceinline__ void reduce_elem(const StepArgs& a, const ShardDev& d
 }
 
 template <int GDT, int PDT>
-__device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k) {
+__device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, const Ctl& c) {
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
-    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
-    adamw1(th, mm, vv, Half16<GDT>::widen(static_cast<const uint16_t*>(d.gshard)[i]), k, a.sc);
-    d.mo[i] = th;
-    d.mmo[i] = mm;
-    d.vo[i] = vv;
+    const StatePtrs p = state_ptrs(d, c.sw);
+    float th = p.mi[i], mm = p.mmi[i], vv = p.vi[i];
+    adamw1(th, mm, vv, Half16<GDT>::widen(static_cast<const uint16_t*>(d.gshard)[i]), k, c.sc);
+    p.mo[i] = th;
+    p.mmo[i] = mm;
+    p.vo[i] = vv;
     P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
 }
 
@@ -400,19 +454,21 @@ k_step_fused(const __grid_constant__ StepArgs a) {
     SumSq sumsq;
     int ovf = 0;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
-    const float k = a.k;
-    for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+    const Ctl c = step_ctl(a);
+    const float k = c.k;
+    for (int64_t tile = c.bad ? a.n_tiles : blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
         const ShardDev& d = a.shards[si];
         const int64_t it = tile - d.tile_begin;
         if (it == 0 && threadIdx.x < d.head && threadIdx.x < d.numel)
-            fused_elem<GDT, PDT>(a, d, threadIdx.x, k, sumsq, ovf);      // the shard's unaligned head
+            fused_elem<GDT, PDT>(a, d, threadIdx.x, c, sumsq, ovf);      // the shard's unaligned head
         const int64_t j = d.head + it * TILE + (int64_t)threadIdx.x * VEC;
         if (j >= d.numel) continue;
         if (VEC == 8 && j + 8 <= d.numel) {
-            const float4 t0 = ld_ro4(d.mi + j), t1 = ld_ro4(d.mi + j + 4);
-            const float4 m0 = ld_ro4(d.mmi + j), m1 = ld_ro4(d.mmi + j + 4);
-            const float4 v0 = ld_ro4(d.vi + j), v1 = ld_ro4(d.vi + j + 4);
+            const StatePtrs p = state_ptrs(d, c.sw);
+            const float4 t0 = ld_ro4(p.mi + j), t1 = ld_ro4(p.mi + j + 4);
+            const float4 m0 = ld_ro4(p.mmi + j), m1 = ld_ro4(p.mmi + j + 4);
+            const float4 v0 = ld_ro4(p.vi + j), v1 = ld_ro4(p.vi + j + 4);
             float s[8];
             reduce8<GDT, NS>(a, d.grad_off + j, s);
             float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
@@ -424,7 +480,7 @@ k_step_fused(const __grid_constant__ StepArgs a) {
                 const uint32_t h = average16n<GDT, NS>(s[e], a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h);
                 af[e] = Half16<GDT>::widen(h);
-                adamw1(th[e], mm[e], vv[e], af[e], k, a.sc);
+                adamw1(th[e], mm[e], vv[e], af[e], k, c.sc);
             }
             uint32_t hp[8];
 #pragma unroll
@@ -434,16 +490,16 @@ k_step_fused(const __grid_constant__ StepArgs a) {
                 hp[e + 1] = w >> 16;
             }
             sumsq.add8(af);
-            st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
-            st_stream4(d.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
-            st_stream4(d.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
-            st_stream4(d.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
-            st_stream4(d.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
-            st_stream4(d.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+            st_stream4(p.mo + j, make_float4(th[0], th[1], th[2], th[3]));
+            st_stream4(p.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
+            st_stream4(p.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
+            st_stream4(p.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
+            st_stream4(p.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
+            st_stream4(p.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
             store8(P, d.param_off + j, hp);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
-            for (int64_t i = j; i < end; ++i) fused_elem<GDT, PDT>(a, d, i, k, sumsq, ovf);
+            for (int64_t i = j; i < end; ++i) fused_elem<GDT, PDT>(a, d, i, c, sumsq, ovf);
         }
     }
     double acc = sumsq.total();
@@ -455,13 +511,13 @@ k_step_fused(const __grid_constant__ StepArgs a) {
     if (threadIdx.x == 0) {
         zero_result r;
         r.overflow = (flag | a.extra_overflow) ? 1 : 0;
-        r.applied = r.overflow ? 0 : 1;
+        r.status = c.bad ? ZERO_ELIMIT : 0;
+        r.applied = (r.overflow || r.status) ? 0 : 1;
         r.path = 1;
-        r.status = 0;
         r.sumsq = sum + a.extra_sumsq;
-        r.grad_norm = sqrt(r.sumsq) / a.loss_scale;
+        r.grad_norm = sqrt(r.sumsq) / c.S;
         r.clip_coef = 1.0;
-        r.grad_mult = a.k;
+        r.grad_mult = c.k;
         r.reserved = 0.0f;
         *a.result = r;
     }
@@ -471,12 +527,14 @@ k_step_fused(const __grid_constant__ StepArgs a) {
 template <int PDT>
 __global__ void __launch_bounds__(TILE_THREADS) k_recover(const __grid_constant__ StepArgs a) {
     if (__ldcg(&a.result->applied)) return;
+    const bool sw = a.chain && __ldcg(&a.chain->cur) != 0;     // the set the step read (not yet flipped)
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     for (int si = 0; si < a.n_shards; ++si) {
         const ShardDev& d = a.shards[si];
+        const float* M = state_ptrs(d, sw).mi;
         for (int64_t i = (int64_t)blockIdx.x * TILE_THREADS + threadIdx.x; i < d.numel;
              i += (int64_t)gridDim.x * TILE_THREADS)
-            P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(d.mi[i]);
+            P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(M[i]);
     }
 }
 
@@ -538,13 +596,14 @@ k_apply(const __grid_constant__ StepArgs a) {
     const int overflow = (st.overflow | a.extra_overflow) ? 1 : 0;
     const double sumsq = st.sumsq + a.extra_sumsq;
     double norm, clip;
-    const float k = grad_multiplier(sumsq, a.loss_scale, a.max_norm, norm, clip);
+    const Ctl c = step_ctl(a);
+    const float k = grad_multiplier(sumsq, c.S, a.max_norm, norm, clip);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         zero_result r;
         r.overflow = overflow;
-        r.applied = overflow ? 0 : 1;
+        r.status = c.bad ? ZERO_ELIMIT : 0;
+        r.applied = (overflow || c.bad) ? 0 : 1;
         r.path = 2;
-        r.status = 0;
         r.sumsq = sumsq;
         r.grad_norm = norm;
         r.clip_coef = clip;
@@ -552,21 +611,22 @@ k_apply(const __grid_constant__ StepArgs a) {
         r.reserved = 0.0f;
         *a.result = r;
     }
-    if (overflow) return;
+    if (overflow || c.bad) return;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
         const ShardDev& d = a.shards[si];
         const int64_t it = tile - d.tile_begin;
         if (it == 0 && threadIdx.x < d.head && threadIdx.x < d.numel)
-            apply_elem<GDT, PDT>(a, d, threadIdx.x, k);                      // the shard's unaligned head
+            apply_elem<GDT, PDT>(a, d, threadIdx.x, k, c);                   // the shard's unaligned head
         const int64_t j = d.head + it * TILE + (int64_t)threadIdx.x * VEC;
         if (j >= d.numel) continue;
         const uint16_t* G = static_cast<const uint16_t*>(d.gshard);
         if (VEC == 8 && j + 8 <= d.numel) {
-            const float4 t0 = ld_stream4(d.mi + j), t1 = ld_stream4(d.mi + j + 4);
-            const float4 m0 = ld_stream4(d.mmi + j), m1 = ld_stream4(d.mmi + j + 4);
-            const float4 v0 = ld_stream4(d.vi + j), v1 = ld_stream4(d.vi + j + 4);
+            const StatePtrs p = state_ptrs(d, c.sw);
+            const float4 t0 = ld_stream4(p.mi + j), t1 = ld_stream4(p.mi + j + 4);
+            const float4 m0 = ld_stream4(p.mmi + j), m1 = ld_stream4(p.mmi + j + 4);
+            const float4 v0 = ld_stream4(p.vi + j), v1 = ld_stream4(p.vi + j + 4);
             const uint4 w = ld_stream(G + j);
             const uint32_t u[4] = {w.x, w.y, w.z, w.w};
             float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
@@ -575,7 +635,7 @@ k_apply(const __grid_constant__ StepArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t h = (e & 1) ? (u[e >> 1] >> 16) : (u[e >> 1] & 0xFFFFu);
-                adamw1(th[e], mm[e], vv[e], Half16<GDT>::widen(h), k, a.sc);
+                adamw1(th[e], mm[e], vv[e], Half16<GDT>::widen(h), k, c.sc);
             }
             uint32_t hp[8];
 #pragma unroll
@@ -584,16 +644,16 @@ k_apply(const __grid_constant__ StepArgs a) {
                 hp[e] = w & 0xFFFFu;
                 hp[e + 1] = w >> 16;
             }
-            st_stream4(d.mo + j, make_float4(th[0], th[1], th[2], th[3]));
-            st_stream4(d.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
-            st_stream4(d.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
-            st_stream4(d.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
-            st_stream4(d.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
-            st_stream4(d.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+            st_stream4(p.mo + j, make_float4(th[0], th[1], th[2], th[3]));
+            st_stream4(p.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
+            st_stream4(p.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
+            st_stream4(p.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
+            st_stream4(p.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
+            st_stream4(p.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
             store8(P, d.param_off + j, hp);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
-            for (int64_t i = j; i < end; ++i) apply_elem<GDT, PDT>(a, d, i, k);
+            for (int64_t i = j; i < end; ++i) apply_elem<GDT, PDT>(a, d, i, k, c);
         }
     }
 }

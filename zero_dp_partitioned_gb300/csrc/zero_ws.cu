@@ -60,7 +60,7 @@ __host__ __device__ inline uint32_t ws_stage_bytes(int ng) {
 // slice at the shard's gradient offset; otherwise the reduced gradient), then
 // master, m, v.
 template <bool FUSED>
-__device__ __forceinline__ void ws_issue(const StepArgs& a, const ShardDev& d, int64_t c0, int64_t len,
+__device__ __forceinline__ void ws_issue(const StepArgs& a, const ShardDev& d, bool sw, int64_t c0, int64_t len,
                                          uint32_t stage, uint32_t bar) {
     const int ng = FUSED ? a.n_slices : 1;
     const uint32_t blen = (uint32_t)(len & ~int64_t(7));
@@ -72,9 +72,10 @@ __device__ __forceinline__ void ws_issue(const StepArgs& a, const ShardDev& d, i
         bulk_load(stage + (uint32_t)r * WS_CHUNK * 2, src, blen * 2u, bar);
     }
     const uint32_t so = (uint32_t)ng * WS_CHUNK * 2;
-    bulk_load(stage + so, d.mi + c0, blen * 4u, bar);
-    bulk_load(stage + so + WS_CHUNK * 4, d.mmi + c0, blen * 4u, bar);
-    bulk_load(stage + so + 2 * WS_CHUNK * 4, d.vi + c0, blen * 4u, bar);
+    const StatePtrs p = state_ptrs(d, sw);
+    bulk_load(stage + so, p.mi + c0, blen * 4u, bar);
+    bulk_load(stage + so + WS_CHUNK * 4, p.mmi + c0, blen * 4u, bar);
+    bulk_load(stage + so + 2 * WS_CHUNK * 4, p.vi + c0, blen * 4u, bar);
 }
 
 // V 16-bit values from shared memory as V/2 words.
@@ -91,8 +92,8 @@ __device__ __forceinline__ void load_halves(const uint8_t* p, uint32_t (&u)[V / 
 
 // One element by plain loads and stores (a shard's head and last few elements).
 template <int GDT, int PDT, bool FUSED>
-__device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, SumSq& sumsq,
-                                        int& flags) {
+__device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, int64_t i, float k, const Ctl& c,
+                                        SumSq& sumsq, int& flags) {
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     uint32_t h;
     if (FUSED) {
@@ -103,11 +104,12 @@ __device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, in
     }
     const float af = Half16<GDT>::widen(h);
     if (FUSED) sumsq.add_fp64(af);
-    float th = d.mi[i], mm = d.mmi[i], vv = d.vi[i];
-    adamw1(th, mm, vv, af, k, a.sc);
-    d.mo[i] = th;
-    d.mmo[i] = mm;
-    d.vo[i] = vv;
+    const StatePtrs p = state_ptrs(d, c.sw);
+    float th = p.mi[i], mm = p.mmi[i], vv = p.vi[i];
+    adamw1(th, mm, vv, af, k, c.sc);
+    p.mo[i] = th;
+    p.mmo[i] = mm;
+    p.vo[i] = vv;
     P[d.param_off + i] = (uint16_t)Half16<PDT>::narrow(th);
 }
 
@@ -130,17 +132,18 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
     const int64_t G = gridDim.x;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
 
-    float k = a.k;
+    const Ctl c = step_ctl(a);
+    float k = c.k;
     int overflow_in = 0;
     double st_sumsq = 0.0, norm = 0.0, clip = 1.0;
     if (!FUSED) {
         const zero_stats st = *a.stats;
         overflow_in = (st.overflow | a.extra_overflow) ? 1 : 0;
         st_sumsq = st.sumsq + a.extra_sumsq;
-        k = grad_multiplier(st_sumsq, a.loss_scale, a.max_norm, norm, clip);
+        k = grad_multiplier(st_sumsq, c.S, a.max_norm, norm, clip);
     }
-    const int64_t n_local =
-        (!overflow_in && a.n_tiles > (int64_t)blockIdx.x) ? (a.n_tiles - 1 - blockIdx.x) / G + 1 : 0;
+    const int64_t n_local = (!overflow_in && !c.bad && a.n_tiles > (int64_t)blockIdx.x)
+                                ? (a.n_tiles - 1 - blockIdx.x) / G + 1 : 0;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
                 const ShardDev& d = a.shards[si];
                 const int64_t c0 = d.head + (chunk - d.tile_begin) * WS_CHUNK;
                 const int64_t rem = d.numel - c0;
-                ws_issue<FUSED>(a, d, c0, rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK,
+                ws_issue<FUSED>(a, d, c.sw, c0, rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK,
                                 stage0 + (uint32_t)st * stage_bytes, full0 + 8 * st);
                 if (++st == S) {        // the uses of round r >= 1 wait for the consumption of round r - 1
                     st = 0;
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
             const int64_t len = rem < WS_CHUNK ? (rem > 0 ? rem : 0) : WS_CHUNK;
             const int64_t blen = len & ~int64_t(7);
             const uint8_t* in = smem + WS_HEADER + (size_t)st * stage_bytes;
-            if (it == 0 && e0 / V < d.head) ws_elem<GDT, PDT, FUSED>(a, d, e0 / V, k, sumsq, flags);   // the head
+            if (it == 0 && e0 / V < d.head) ws_elem<GDT, PDT, FUSED>(a, d, e0 / V, k, c, sumsq, flags);  // the head
             if (e0 + V <= blen) {
                 uint32_t hg[V];                   // the averaged (FUSED) or reduced 16-bit gradient
                 if (FUSED) {
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     af[e] = Half16<GDT>::widen(hg[e]);
-                    adamw1(th[e], mm[e], vv[e], af[e], k, a.sc);
+                    adamw1(th[e], mm[e], vv[e], af[e], k, c.sc);
                 }
 #pragma unroll
                 for (int e = 0; e < V; e += 2) {
@@ -260,12 +263,13 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
                     if constexpr (V == 8) sumsq.add8(*reinterpret_cast<const float(*)[8]>(af));
                     else sumsq.add4(*reinterpret_cast<const float(*)[4]>(af));
                 }
+                const StatePtrs sp = state_ptrs(d, c.sw);
 #pragma unroll
                 for (int q = 0; q < V / 4; ++q) {
                     const int e = 4 * q;
-                    st_stream4(d.mo + c0 + e0 + e, make_float4(th[e], th[e + 1], th[e + 2], th[e + 3]));
-                    st_stream4(d.mmo + c0 + e0 + e, make_float4(mm[e], mm[e + 1], mm[e + 2], mm[e + 3]));
-                    st_stream4(d.vo + c0 + e0 + e, make_float4(vv[e], vv[e + 1], vv[e + 2], vv[e + 3]));
+                    st_stream4(sp.mo + c0 + e0 + e, make_float4(th[e], th[e + 1], th[e + 2], th[e + 3]));
+                    st_stream4(sp.mmo + c0 + e0 + e, make_float4(mm[e], mm[e + 1], mm[e + 2], mm[e + 3]));
+                    st_stream4(sp.vo + c0 + e0 + e, make_float4(vv[e], vv[e + 1], vv[e + 2], vv[e + 3]));
                 }
                 if constexpr (V == 8) store8(P, d.param_off + c0 + e0, *reinterpret_cast<const uint32_t(*)[8]>(hp));
                 else store4(P, d.param_off + c0 + e0, *reinterpret_cast<const uint32_t(*)[4]>(hp));
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
                 // the shard's last (fewer than 8) elements: plain loads and stores
                 const int64_t end = (e0 + V < len) ? e0 + V : len;
                 for (int64_t e = (e0 > blen ? e0 : blen); e < end; ++e)
-                    ws_elem<GDT, PDT, FUSED>(a, d, c0 + e, k, sumsq, flags);
+                    ws_elem<GDT, PDT, FUSED>(a, d, c0 + e, k, c, sumsq, flags);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
@@ -295,9 +299,9 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
         if (FUSED) {
             r.overflow = ((flag & FLAG_OVERFLOW) || a.extra_overflow) ? 1 : 0;
             r.sumsq = sum + a.extra_sumsq;
-            r.grad_norm = sqrt(r.sumsq) / a.loss_scale;
+            r.grad_norm = sqrt(r.sumsq) / c.S;
             r.clip_coef = 1.0;
-            r.grad_mult = a.k;
+            r.grad_mult = c.k;
         } else {
             r.overflow = overflow_in;
             r.sumsq = st_sumsq;
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
             r.clip_coef = clip;
             r.grad_mult = k;
         }
-        r.status = (flag & FLAG_TIMEOUT) ? ZERO_ETIMEOUT : 0;
+        r.status = (flag & FLAG_TIMEOUT) ? ZERO_ETIMEOUT : (c.bad ? ZERO_ELIMIT : 0);
         r.applied = (r.overflow || r.status) ? 0 : 1;
         r.path = FUSED ? 5 : 6;
         r.reserved = 0.0f;
