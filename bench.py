@@ -269,8 +269,23 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
-    st = dict(cur=0, t=1, S=wl.loss_scale)
+    st = dict(cur=0, t=1, S=wl.loss_scale, chained=True)
     pinned = _pin_copies(torch, grads, e2e)
+    # Device-timed steps are chained: t, S and the state set in use stay on the
+    # device, so steps follow one another with no host round trip.
+    hy = _hyper(Z, wl.hyper, 1)
+    n_table = 1 << 16
+    table = torch.from_numpy(Z.zero_adam_scalar_table(hy, 1, n_table)).to(dev)
+    chain_dev = torch.frombuffer(bytearray(bytes(Z.chain(step=1, loss_scale=wl.loss_scale))),
+                                 dtype=torch.uint8).to(dev)
+
+    def host_from_chain():
+        """The end-to-end steps keep the bookkeeping on the host: take it over."""
+        if st["chained"]:
+            c = Z.read_chain(chain_dev)
+            if c.failed:
+                raise RuntimeError(f"{c.failed} chained steps failed (status != 0)")
+            st.update(cur=c.cur, t=c.step, S=c.loss_scale, chained=False)
     # End to end, the next step's gradients cross the host link on a copy
     # stream into a second device set while this step computes.
     host = dict(sets=[grads], copy=None, copied=None, consumed=None, i=0, pending=None)
@@ -293,6 +308,12 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
 
     def step(from_host=False):
         main = torch.cuda.current_stream()
+        if not from_host and st["chained"]:
+            with timer("fused pass+k_recover"):
+                Z.zero_shard_step_chained(grads, Z.ZERO_BF16, variants[0], flat, Z.ZERO_BF16, hy, table, 1, n_table,
+                                          chain_dev, 0.0, 0, ws, ws.numel(), res)
+            return
+        host_from_chain()
         b = 0
         if from_host:
             b = host["i"] % 2
@@ -314,8 +335,12 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
         if host["pending"] is not None:
             torch.cuda.current_stream().wait_event(host["copied"][host["pending"]])
 
+    def path_of_last_step():
+        return Z.read_result(res).path
+
     bytes_step = (2 * nd + 26) * P
-    return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=2,
+    return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=3,
+                path_of_last_step=path_of_last_step,
                 kernel_bytes={"fused pass+k_recover": bytes_step},
                 dominant_label=None,
                 h2d=sum(g.numel() * 2 for g in grads) if pinned else None, d2h=48, e2e_ok=pinned is not None,
@@ -326,6 +351,8 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                                     "N_d=8, all 8 ranks simulated on one GPU",
                         "psi": P, "n_d": nd, "shard_elements": plan["rank_numels"][0], "grad_dtype": "bf16",
                         "param_dtype": "bf16", "state": "f32 master/m/v, ping-pong", "path": "fused single pass",
+                        "steps": "zero_shard_step_chained: t, S and the state set in use stay on the device "
+                                 "(3 launches a step: the pass, the parameter restore check, the bookkeeping)",
                         "bytes_per_step": bytes_step,
                         "l2": f"inputs larger than L2 ({bytes_step / 1e9:.1f} GB per step), no flush"},
                 formula_bytes=bytes_step, sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
@@ -368,10 +395,45 @@ def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None):
                               st["S"], 0.0, 0, ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
 
+    hy = _hyper(Z, wl.hyper, 1)
+    table = torch.from_numpy(Z.zero_adam_scalar_table(hy, 1, 1 << 12)).to(dev)
+
+    def extra(steps):
+        """The same steps chained on the device and replayed from one CUDA graph
+        (20 steps, each with its L2 flush), against the host-driven steps above."""
+        chain_dev = torch.frombuffer(bytearray(bytes(Z.chain(step=1, loss_scale=wl.loss_scale))),
+                                     dtype=torch.uint8).to(dev)
+
+        def chained():
+            flush.fill_(7)
+            Z.zero_shard_step_chained(grads, Z.ZERO_F16, variants[0], flat, Z.ZERO_F16, hy, table, 1, 1 << 12,
+                                      chain_dev, 0.0, 0, ws, ws.numel(), res)
+
+        chained()                               # one-time set-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+            for _ in range(20):
+                chained()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        c = Z.read_chain(chain_dev)
+        if c.failed:
+            raise RuntimeError("chained tiny steps failed")
+        return {"graph_of_chained_steps_ms_per_step": a.elapsed_time(b) / (20 * reps),
+                "graph_steps_applied": c.applied}
+
     bytes_step = (2 * nd + 26) * P
     return dict(name="tiny-nd3", step=step, state=st, elements=P, nd=nd, launches_per_step=2,
                 kernel_bytes={"fused pass+k_recover": bytes_step}, dominant_label=None, h2d=None, d2h=48,
-                e2e_ok=False, formula_bytes=bytes_step, sample_for_cpu=None,
+                e2e_ok=False, formula_bytes=bytes_step, sample_for_cpu=None, extra=extra,
                 config={"workload": "tiny-nd3: three tensors [257,129], [129], [1000,37] (Psi = 70,282), N_d=3, "
                                     "all ranks, fp16, S = 1024",
                         "psi": sum(numels), "padded": P, "n_d": nd, "path": "fused single pass",
@@ -1009,6 +1071,8 @@ def main():
     clocks = sampler.stop()
     ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, dev)
     kinds = timer.per_kind(args.steps)
+    if wl.get("path_of_last_step"):
+        wl["state"]["path"] = wl["path_of_last_step"]()
     if wl.get("extra"):
         wl["config"].update(wl["extra"](args.steps))
 
