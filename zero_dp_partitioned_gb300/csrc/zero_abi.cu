@@ -526,9 +526,8 @@ int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int gr
         } else {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
             number_tiles(a, vec, HEAD_GRADS);
-            const int grid =
-                grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles,
-                         n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+            const int grid = grid_for(fused_kernel_chain(grad_dtype, param_dtype, vec), a.n_tiles,
+                                      n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
             if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
         }
         if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;

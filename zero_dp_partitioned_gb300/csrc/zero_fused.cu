@@ -28,8 +28,22 @@ const void* fused_kernel(int gdt, int pdt, int vec, int ns) {
     return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_F16, ZERO_BF16>(vec, ns) : fused_ptr_v<ZERO_F16, ZERO_F16>(vec, ns);
 }
 
+// Chained steps take the generic slice loop (the producer/consumer pass
+// covers the common case; this one runs for more than 8 slices or misaligned
+// data).
+template <int G, int P>
+static const void* fused_chain_ptr(int vec) {
+    return vec == 8 ? (const void*)k_step_fused<G, P, 8, 0, true> : (const void*)k_step_fused<G, P, 1, 0, true>;
+}
+
+const void* fused_kernel_chain(int gdt, int pdt, int vec) {
+    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_BF16, ZERO_BF16>(vec)
+                                                  : fused_chain_ptr<ZERO_BF16, ZERO_F16>(vec);
+    return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_F16, ZERO_BF16>(vec) : fused_chain_ptr<ZERO_F16, ZERO_F16>(vec);
+}
+
 int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s) {
-    const void* f = fused_kernel(gdt, pdt, vec, ns_variant(a.n_slices));
+    const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec) : fused_kernel(gdt, pdt, vec, ns_variant(a.n_slices));
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "fused step launch");
 }

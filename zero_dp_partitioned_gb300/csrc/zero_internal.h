@@ -81,6 +81,7 @@ int launch_ws(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s
 
 // Kernel addresses, for the occupancy query.
 const void* fused_kernel(int gdt, int pdt, int vec, int ns);
+const void* fused_kernel_chain(int gdt, int pdt, int vec);
 const void* reduce_kernel(int gdt, int vec, int ns);
 const void* apply_kernel(int gdt, int pdt, int vec);
 

@@ -155,14 +155,21 @@ __device__ __forceinline__ uint32_t average16n(float s, float divisor) {
 }
 
 // AdamW on one coordinate, the operations in the order of the update rule.
-__device__ __forceinline__ void adamw1(float& th, float& m, float& v, float a, float k, const AdamScalars& c) {
+// ss and rb2 (the step-dependent scalars) come apart from the rest, so that
+// the rest can stay in the kernel's parameter space.
+__device__ __forceinline__ void adamw1(float& th, float& m, float& v, float a, float k, const AdamScalars& c,
+                                       float ss, float rb2) {
     const float g = __fmul_rn(a, k);
     th = __fmul_rn(th, c.wdf);
     m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
     const float g2 = __fmul_rn(g, g);
     v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, g2));
-    const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v), c.rb2), c.eps);
-    th = __fsub_rn(th, __fmul_rn(c.ss, __fdiv_rn(m, den)));
+    const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v), rb2), c.eps);
+    th = __fsub_rn(th, __fmul_rn(ss, __fdiv_rn(m, den)));
+}
+
+__device__ __forceinline__ void adamw1(float& th, float& m, float& v, float a, float k, const AdamScalars& c) {
+    adamw1(th, m, v, a, k, c, c.ss, c.rb2);
 }
 
 // Store 8 16-bit values at dst + q with the widest stores its address allows
@@ -358,32 +365,41 @@ __device__ __forceinline__ float reduce1(const StepArgs& a, int64_t off) {
 // What a kernel needs of the step that is not in its arguments for a chained
 // step: the scalars, the multiplier, S, and which state set is read.
 struct Ctl {
-    AdamScalars sc;
+    float ss, rb2;      // the step-dependent AdamW scalars (the others stay in a.sc)
     float k;            // the fused pass's gradient multiplier, fp32(1/S)
-    double S;
     bool sw;            // the state sets are used the other way round (chain->cur == 1)
     bool bad;           // a chained step outside its scalar table: nothing is updated
 };
 
+// S of the step (read again where it is needed, rather than kept live).
+__device__ __forceinline__ double step_S(const StepArgs& a) {
+    return a.chain ? __ldcg(&a.chain->loss_scale) : a.loss_scale;
+}
+
+__device__ __forceinline__ bool step_bad(const StepArgs& a) {
+    if (!a.chain) return false;
+    const int64_t i = __ldcg(&a.chain->step) - a.t0;
+    return i < 0 || i >= a.n_table;
+}
+
 __device__ __forceinline__ Ctl step_ctl(const StepArgs& a) {
     Ctl c;
-    c.sc = a.sc;
+    c.ss = a.sc.ss;
+    c.rb2 = a.sc.rb2;
     c.k = a.k;
-    c.S = a.loss_scale;
     c.sw = false;
     c.bad = false;
     if (a.chain) {
         const int cur = __ldcg(&a.chain->cur);
         const int64_t t = __ldcg(&a.chain->step);
-        c.S = __ldcg(&a.chain->loss_scale);
-        c.k = (float)(1.0 / c.S);
+        c.k = (float)(1.0 / __ldcg(&a.chain->loss_scale));
         c.sw = cur != 0;
         const int64_t i = t - a.t0;
         if (i < 0 || i >= a.n_table) {
             c.bad = true;
         } else {
-            c.sc.ss = __ldg(a.sc_table + 2 * i);
-            c.sc.rb2 = __ldg(a.sc_table + 2 * i + 1);
+            c.ss = __ldg(a.sc_table + 2 * i);
+            c.rb2 = __ldg(a.sc_table + 2 * i + 1);
         }
     }
     return c;
@@ -415,7 +431,7 @@ __device__ __forceinline__ void fused_elem(const StepArgs& a, const ShardDev& d,
     sumsq.add_fp64(af);
     const StatePtrs p = state_ptrs(d, c.sw);
     float th = p.mi[i], mm = p.mmi[i], vv = p.vi[i];
-    adamw1(th, mm, vv, af, c.k, c.sc);
+    adamw1(th, mm, vv, af, c.k, a.sc, c.ss, c.rb2);
     p.mo[i] = th;
     p.mmo[i] = mm;
     p.vo[i] = vv;
@@ -435,7 +451,7 @@ __device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d,
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
     const StatePtrs p = state_ptrs(d, c.sw);
     float th = p.mi[i], mm = p.mmi[i], vv = p.vi[i];
-    adamw1(th, mm, vv, Half16<GDT>::widen(static_cast<const uint16_t*>(d.gshard)[i]), k, c.sc);
+    adamw1(th, mm, vv, Half16<GDT>::widen(static_cast<const uint16_t*>(d.gshard)[i]), k, a.sc, c.ss, c.rb2);
     p.mo[i] = th;
     p.mmo[i] = mm;
     p.vo[i] = vv;
@@ -447,14 +463,16 @@ __device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d,
 // 16-bit parameters once.  Speculative: the skip decision is global, so the
 // *_out state is only committed by the caller when result->applied; the
 // parameters are restored by k_recover on overflow.
-template <int GDT, int PDT, int VEC, int NS>
-__global__ void __launch_bounds__(TILE_THREADS)
+// CHAIN: a chained step (t, S and the state set from a.chain); the other
+// instantiations take everything from their arguments.
+template <int GDT, int PDT, int VEC, int NS, bool CHAIN = false>
+__global__ void __launch_bounds__(TILE_THREADS, (NS == 0 && !CHAIN) ? 4 : 1)   // many slices: 4 blocks per SM
 k_step_fused(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
     SumSq sumsq;
     int ovf = 0;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
-    const Ctl c = step_ctl(a);
+    const Ctl c = CHAIN ? step_ctl(a) : Ctl{a.sc.ss, a.sc.rb2, a.k, false, false};
     const float k = c.k;
     for (int64_t tile = c.bad ? a.n_tiles : blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
         const int si = find_shard(a, tile);
@@ -480,7 +498,7 @@ k_step_fused(const __grid_constant__ StepArgs a) {
                 const uint32_t h = average16n<GDT, NS>(s[e], a.divisor);
                 ovf |= Half16<GDT>::nonfinite(h);
                 af[e] = Half16<GDT>::widen(h);
-                adamw1(th[e], mm[e], vv[e], af[e], k, c.sc);
+                adamw1(th[e], mm[e], vv[e], af[e], k, a.sc, c.ss, c.rb2);
             }
             uint32_t hp[8];
 #pragma unroll
@@ -511,13 +529,13 @@ k_step_fused(const __grid_constant__ StepArgs a) {
     if (threadIdx.x == 0) {
         zero_result r;
         r.overflow = (flag | a.extra_overflow) ? 1 : 0;
-        r.status = c.bad ? ZERO_ELIMIT : 0;
+        r.status = (CHAIN && step_bad(a)) ? ZERO_ELIMIT : 0;
         r.applied = (r.overflow || r.status) ? 0 : 1;
         r.path = 1;
         r.sumsq = sum + a.extra_sumsq;
-        r.grad_norm = sqrt(r.sumsq) / c.S;
+        r.grad_norm = sqrt(r.sumsq) / (CHAIN ? step_S(a) : a.loss_scale);
         r.clip_coef = 1.0;
-        r.grad_mult = c.k;
+        r.grad_mult = CHAIN ? (float)(1.0 / step_S(a)) : a.k;
         r.reserved = 0.0f;
         *a.result = r;
     }
@@ -597,7 +615,7 @@ k_apply(const __grid_constant__ StepArgs a) {
     const double sumsq = st.sumsq + a.extra_sumsq;
     double norm, clip;
     const Ctl c = step_ctl(a);
-    const float k = grad_multiplier(sumsq, c.S, a.max_norm, norm, clip);
+    const float k = grad_multiplier(sumsq, step_S(a), a.max_norm, norm, clip);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         zero_result r;
         r.overflow = overflow;
@@ -635,7 +653,7 @@ k_apply(const __grid_constant__ StepArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t h = (e & 1) ? (u[e >> 1] >> 16) : (u[e >> 1] & 0xFFFFu);
-                adamw1(th[e], mm[e], vv[e], Half16<GDT>::widen(h), k, c.sc);
+                adamw1(th[e], mm[e], vv[e], Half16<GDT>::widen(h), k, a.sc, c.ss, c.rb2);
             }
             uint32_t hp[8];
 #pragma unroll

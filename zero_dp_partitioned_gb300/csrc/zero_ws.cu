@@ -106,7 +106,7 @@ __device__ __forceinline__ void ws_elem(const StepArgs& a, const ShardDev& d, in
     if (FUSED) sumsq.add_fp64(af);
     const StatePtrs p = state_ptrs(d, c.sw);
     float th = p.mi[i], mm = p.mmi[i], vv = p.vi[i];
-    adamw1(th, mm, vv, af, k, c.sc);
+    adamw1(th, mm, vv, af, k, a.sc, c.ss, c.rb2);
     p.mo[i] = th;
     p.mmo[i] = mm;
     p.vo[i] = vv;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
         const zero_stats st = *a.stats;
         overflow_in = (st.overflow | a.extra_overflow) ? 1 : 0;
         st_sumsq = st.sumsq + a.extra_sumsq;
-        k = grad_multiplier(st_sumsq, c.S, a.max_norm, norm, clip);
+        k = grad_multiplier(st_sumsq, step_S(a), a.max_norm, norm, clip);
     }
     const int64_t n_local = (!overflow_in && !c.bad && a.n_tiles > (int64_t)blockIdx.x)
                                 ? (a.n_tiles - 1 - blockIdx.x) / G + 1 : 0;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
 #pragma unroll
                 for (int e = 0; e < V; ++e) {
                     af[e] = Half16<GDT>::widen(hg[e]);
-                    adamw1(th[e], mm[e], vv[e], af[e], k, c.sc);
+                    adamw1(th[e], mm[e], vv[e], af[e], k, a.sc, c.ss, c.rb2);
                 }
 #pragma unroll
                 for (int e = 0; e < V; e += 2) {
@@ -299,9 +299,9 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
         if (FUSED) {
             r.overflow = ((flag & FLAG_OVERFLOW) || a.extra_overflow) ? 1 : 0;
             r.sumsq = sum + a.extra_sumsq;
-            r.grad_norm = sqrt(r.sumsq) / c.S;
+            r.grad_norm = sqrt(r.sumsq) / step_S(a);
             r.clip_coef = 1.0;
-            r.grad_mult = c.k;
+            r.grad_mult = (float)(1.0 / step_S(a));
         } else {
             r.overflow = overflow_in;
             r.sumsq = st_sumsq;
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(TILE_THREADS, WS_BLOCKS_PER_SM) k_ws(const __g
             r.clip_coef = clip;
             r.grad_mult = k;
         }
-        r.status = (flag & FLAG_TIMEOUT) ? ZERO_ETIMEOUT : (c.bad ? ZERO_ELIMIT : 0);
+        r.status = (flag & FLAG_TIMEOUT) ? ZERO_ETIMEOUT : (step_bad(a) ? ZERO_ELIMIT : 0);
         r.applied = (r.overflow || r.status) ? 0 : 1;
         r.path = FUSED ? 5 : 6;
         r.reserved = 0.0f;
