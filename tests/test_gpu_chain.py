@@ -101,9 +101,12 @@ def check(run, p, osh, oflat, exact):
     return c
 
 
-@pytest.mark.parametrize("numels,nd,dt", [([20000, 4096, 992], 4, 2), ([20000, 555], 3, 1), ([3000, 5000], 8, 2)])
+# aligned, at most 8 slices: the producer/consumer pass; misaligned: the register pass one element at a time;
+# 12 slices, aligned: the register pass with 16-byte vectors
+@pytest.mark.parametrize("numels,nd,dt,fused_path", [([20000, 4096, 992], 4, 2, 5), ([20000, 555], 3, 1, 1),
+                                                     ([3000, 5000], 8, 2, 5), ([24000, 576], 12, 2, 1)])
 @pytest.mark.parametrize("clip", [0.0, 0.05])
-def test_chained_steps_match_the_oracle(Z, numels, nd, dt, clip):
+def test_chained_steps_match_the_oracle(Z, numels, nd, dt, fused_path, clip):
     """Five chained steps, the second with a NaN in one slice (skipped: t stays,
     S halves), no host synchronisation in between."""
     S = 256.0 if dt == 1 else 1.0
@@ -121,7 +124,7 @@ def test_chained_steps_match_the_oracle(Z, numels, nd, dt, clip):
     c = check(run, p, osh, oflat, clip <= 0.0)
     assert (c.step, c.loss_scale, c.applied, c.skipped, c.failed) == (t, So, 4, 1, 0)
     r = Z.read_result(run.res)
-    assert r.applied == 1 and r.status == 0
+    assert r.applied == 1 and r.status == 0 and r.path == (fused_path if clip <= 0.0 else 2)
 
 
 @pytest.mark.parametrize("clip", [0.0, 0.05])
