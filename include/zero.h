@@ -58,7 +58,9 @@ typedef enum {
     ZERO_EALIGN = -2,      /* a pointer is not aligned to its element size */
     ZERO_EWORKSPACE = -3,  /* workspace missing or smaller than zero_workspace_bytes() */
     ZERO_ECUDA = -4,       /* a CUDA runtime call or launch failed */
-    ZERO_ELIMIT = -5,      /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards */
+    ZERO_ELIMIT = -5,      /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards; a call beyond
+                              zero_shard_step_noalloc's scratch; (zero_result.status) a chained step outside
+                              its scalar table */
     ZERO_ETIMEOUT = -6     /* (zero_result.status only) a device-side wait gave up; the step was not applied */
 } zero_status;
 
