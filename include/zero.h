@@ -241,13 +241,13 @@ typedef struct {
  * on the device.
  *
  * Environment (read at each call; meant for tests and measurements):
- *   ZERO_GB300_PATH=register          the register-staged kernels only
+ *   ZERO_GB300_PATH=register          the register-staged kernels (the default)
  *   ZERO_GB300_PATH=stream            the fused and apply passes through
  *       shared-memory stages with a block-wide cycle per chunk, where the
  *       alignment rules below allow it (slower on GB300; kept for comparison)
  *   ZERO_GB300_PATH=ws                the producer/consumer fused and apply
- *       passes where allowed (the default picks the fused one; its apply
- *       pass is slower than the register one on GB300)
+ *       passes where allowed (a producer warp feeding TMA stages to consumer
+ *       warps; 1-10% slower than the register passes on GB300)
  *   ZERO_GB300_SPIN_LIMIT=n           tries per device-side wait of the
  *       shared-memory-staged kernels (default 4194304); 0 makes every first
  *       wait give up, which exercises the ZERO_ETIMEOUT path without hanging
@@ -286,13 +286,12 @@ size_t zero_workspace_bytes(void);
  * state and the parameters once; if the step is not applied a second, short
  * kernel restores the parameters from master_in (parameters always equal
  * round16(master)).  Otherwise two passes: reduce into grad_shard (required
- * then), then apply.  The fused pass runs as a producer warp issuing bulk
- * asynchronous (TMA) copies into shared-memory stages for consumer warps
- * (path 5) when there are at most 8 slices and every slice address
- * (+ grad_offset) and state pointer is 16-byte aligned; otherwise (and with
- * ZERO_GB300_PATH=register) register-staged (path 1).  The apply pass is
- * register-staged (path 2); ZERO_GB300_PATH=ws runs it the producer/consumer
- * way (path 6) when every state pointer and grad_shard is aligned.  With
+ * then), then apply.  Both passes are register-staged (paths 1 and 2), with
+ * 16-byte vectors where every slice address (+ grad_offset), state pointer
+ * and grad_shard is 16-byte aligned.  ZERO_GB300_PATH=ws runs them as a
+ * producer warp issuing bulk asynchronous (TMA) copies into shared-memory
+ * stages for consumer warps (paths 5 and 6) when there are at most 8 slices
+ * and the same addresses are aligned.  With
  * ZERO_GB300_PATH=stream the fused and apply passes run through stages with a
  * block-wide cycle per chunk under the same alignment rules (grad_shard
  * 16-byte aligned too).

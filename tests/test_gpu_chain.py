@@ -101,14 +101,21 @@ def check(run, p, osh, oflat, exact):
     return c
 
 
-# aligned, at most 8 slices: the producer/consumer pass; misaligned: the register pass one element at a time;
-# 12 slices, aligned: the register pass with 16-byte vectors
-@pytest.mark.parametrize("numels,nd,dt,fused_path", [([20000, 4096, 992], 4, 2, 5), ([20000, 555], 3, 1, 1),
-                                                     ([3000, 5000], 8, 2, 5), ([24000, 576], 12, 2, 1)])
+# aligned: 16-byte vectors; misaligned: one element at a time; 12 slices: the many-slice loop;
+# path 5: the producer/consumer pass (ZERO_GB300_PATH=ws)
+@pytest.mark.parametrize("numels,nd,dt,path_env,fused_path", [([20000, 4096, 992], 4, 2, None, 1),
+                                                              ([20000, 4096, 992], 4, 2, "ws", 5),
+                                                              ([20000, 555], 3, 1, None, 1),
+                                                              ([3000, 5000], 8, 2, "ws", 5),
+                                                              ([24000, 576], 12, 2, None, 1)])
 @pytest.mark.parametrize("clip", [0.0, 0.05])
-def test_chained_steps_match_the_oracle(Z, numels, nd, dt, fused_path, clip):
+def test_chained_steps_match_the_oracle(Z, numels, nd, dt, path_env, fused_path, clip, monkeypatch):
     """Five chained steps, the second with a NaN in one slice (skipped: t stays,
     S halves), no host synchronisation in between."""
+    if path_env:
+        monkeypatch.setenv("ZERO_GB300_PATH", path_env)
+    else:
+        monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
     S = 256.0 if dt == 1 else 1.0
     p, flat, grads = make_problem(numels, nd, dt, 0, 61, loss_scale=S, grad_std=1e-2, steps=5)
     grads[1][0] = grads[1][0].copy()

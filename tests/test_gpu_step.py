@@ -29,12 +29,11 @@ def Z():
     return Z
 
 
-@pytest.fixture(params=["default", "register", "stream", "ws"])
+@pytest.fixture(params=["default", "stream", "ws"])
 def kernel_path(request, monkeypatch):
-    """Run a test on the default kernels (the producer/consumer fused pass
-    wherever the alignment allows it), on the register-staged kernels only,
-    on the shared-memory-staged passes with a block-wide cycle, and on both
-    producer/consumer passes."""
+    """Run a test on the default (register-staged) kernels, on the
+    shared-memory-staged passes with a block-wide cycle, and on both
+    producer/consumer passes, wherever the alignment allows them."""
     if request.param == "default":
         monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
     else:
@@ -404,12 +403,13 @@ def test_wait_timeout_is_reported_and_harmless(Z, monkeypatch, path):
 def test_each_path_reports_its_kernels(Z, dt, monkeypatch):
     S = 256.0 if dt == 1 else 1.0
     monkeypatch.delenv("ZERO_GB300_PATH", raising=False)
-    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {5}       # producer/consumer fused
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {1}       # register fused
     assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}      # register apply
+    assert set(_staged_rank_local(Z, 50001, 12, dt, 8, 0.0, S=S, steps=2)) == {1}      # many slices
+    monkeypatch.setenv("ZERO_GB300_PATH", "ws")
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {5}       # producer/consumer fused
+    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {6}      # producer/consumer apply
     assert set(_staged_rank_local(Z, 50001, 12, dt, 8, 0.0, S=S, steps=2)) == {1}      # > 8 slices: register
-    monkeypatch.setenv("ZERO_GB300_PATH", "register")
-    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.0, S=S, steps=2)) == {1}
-    assert set(_staged_rank_local(Z, 50001, 4, dt, 8, 0.05, S=S, steps=2)) == {2}
 
 
 def test_stage1_full_allreduce_then_shard_update(Z):

@@ -58,11 +58,11 @@ int grid_for(const void* func, int64_t n_tiles, int max_per_sm) {
 }
 
 // Implementation choice and wait limit, from the environment (tests and measurements).
-// 0 default (the producer/consumer fused pass where allowed, else register;
-// the register apply pass), 1 register only, 2 staged with a block-wide
-// cycle, 3 producer/consumer fused and apply passes.  The producer/consumer
-// apply pass measured slower than the register one on GB300 (the Llama-3-8B
-// shard: 9.52 ms against 8.56 ms), so only ZERO_GB300_PATH=ws selects it.
+// 0 default (the register-staged passes), 1 register only (the same), 2
+// staged with a block-wide cycle, 3 producer/consumer fused and apply
+// passes.  On GB300 the register passes measure fastest: the GPT-2 fused step
+// 9.51 ms against 9.63 ms producer/consumer, the Llama-3-8B apply pass 8.56
+// ms against 9.52 ms.
 static int path_choice() {
     const char* e = std::getenv("ZERO_GB300_PATH");
     if (e && !std::strcmp(e, "register")) return 1;
@@ -444,13 +444,13 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
         a.k = (float)(1.0 / (double)loss_scale);
         if (choice == 2 && stream_ok(a, true)) {
             if ((rc = run_stream(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
-        } else if ((choice == 0 || choice == 3) && ws_ok(a, true)) {
+        } else if (choice == 3 && ws_ok(a, true)) {
             if ((rc = run_ws(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
         } else {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
             number_tiles(a, vec, HEAD_GRADS);
             const int grid =
-                grid_for(fused_kernel(grad_dtype, param_dtype, vec, ns_variant(n_slices)), a.n_tiles,
+                grid_for(fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
                          n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
             if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
         }
@@ -521,12 +521,12 @@ int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int gr
 
     if (fused) {
         // the fused pass derives k = fp32(1/S) from chain->loss_scale on the device
-        if (ws_ok(a, true) && path_choice() != 1) {
+        if (path_choice() == 3 && ws_ok(a, true)) {
             if ((rc = run_ws(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
         } else {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
             number_tiles(a, vec, HEAD_GRADS);
-            const int grid = grid_for(fused_kernel_chain(grad_dtype, param_dtype, vec), a.n_tiles,
+            const int grid = grid_for(fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
                                       n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
             if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
         }

@@ -6,15 +6,7 @@ namespace zdp {
 
 template <int G, int P, int V>
 static const void* fused_ptr(int ns) {
-    if (V == 1) return (const void*)k_step_fused<G, P, 1, 0>;
-    switch (ns) {
-    case 1: return (const void*)k_step_fused<G, P, V, 1>;
-    case 2: return (const void*)k_step_fused<G, P, V, 2>;
-    case 3: return (const void*)k_step_fused<G, P, V, 3>;
-    case 4: return (const void*)k_step_fused<G, P, V, 4>;
-    case 8: return (const void*)k_step_fused<G, P, V, 8>;
-    default: return (const void*)k_step_fused<G, P, V, 0>;
-    }
+    return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW> : (const void*)k_step_fused<G, P, V, 0>;
 }
 
 template <int G, int P>
@@ -31,19 +23,26 @@ const void* fused_kernel(int gdt, int pdt, int vec, int ns) {
 // Chained steps take the generic slice loop (the producer/consumer pass
 // covers the common case; this one runs for more than 8 slices or misaligned
 // data).
-template <int G, int P>
-static const void* fused_chain_ptr(int vec) {
-    return vec == 8 ? (const void*)k_step_fused<G, P, 8, 0, true> : (const void*)k_step_fused<G, P, 1, 0, true>;
+template <int G, int P, int V>
+static const void* fused_chain_ptr_v(int ns) {
+    return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW, true> : (const void*)k_step_fused<G, P, V, 0, true>;
 }
 
-const void* fused_kernel_chain(int gdt, int pdt, int vec) {
-    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_BF16, ZERO_BF16>(vec)
-                                                  : fused_chain_ptr<ZERO_BF16, ZERO_F16>(vec);
-    return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_F16, ZERO_BF16>(vec) : fused_chain_ptr<ZERO_F16, ZERO_F16>(vec);
+template <int G, int P>
+static const void* fused_chain_ptr(int vec, int ns) {
+    return vec == 8 ? fused_chain_ptr_v<G, P, 8>(ns) : fused_chain_ptr_v<G, P, 1>(ns);
+}
+
+const void* fused_kernel_chain(int gdt, int pdt, int vec, int ns) {
+    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_BF16, ZERO_BF16>(vec, ns)
+                                                  : fused_chain_ptr<ZERO_BF16, ZERO_F16>(vec, ns);
+    return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_F16, ZERO_BF16>(vec, ns)
+                            : fused_chain_ptr<ZERO_F16, ZERO_F16>(vec, ns);
 }
 
 int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s) {
-    const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec) : fused_kernel(gdt, pdt, vec, ns_variant(a.n_slices));
+    const int ns = fused_ns(a.n_slices);
+    const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec, ns) : fused_kernel(gdt, pdt, vec, ns);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "fused step launch");
 }

@@ -81,11 +81,17 @@ int launch_ws(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s
 
 // Kernel addresses, for the occupancy query.
 const void* fused_kernel(int gdt, int pdt, int vec, int ns);
-const void* fused_kernel_chain(int gdt, int pdt, int vec);
+const void* fused_kernel_chain(int gdt, int pdt, int vec, int ns);
 const void* reduce_kernel(int gdt, int vec, int ns);
 const void* apply_kernel(int gdt, int pdt, int vec);
 
-// The slice-count specialisation used for n slices (0 = the generic loop).
+// The slice-count specialisation of the reduce pass for n slices (0 = the
+// generic loop).
 inline int ns_variant(int n) { return (n >= 1 && n <= 4) ? n : (n == 8 ? 8 : 0); }
+
+// The fused pass's slice loop: generic, at 2 blocks per SM for at most
+// FEW_SLICES slices (NS_FEW) or at 4 for more (0).
+constexpr int NS_FEW = -1;
+inline int fused_ns(int n) { return n <= FEW_SLICES ? NS_FEW : 0; }
 
 }  // namespace zdp

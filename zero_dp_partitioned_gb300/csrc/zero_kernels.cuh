@@ -463,10 +463,16 @@ __device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d,
 // 16-bit parameters once.  Speculative: the skip decision is global, so the
 // *_out state is only committed by the caller when result->applied; the
 // parameters are restored by k_recover on overflow.
+// NS: 0 = the generic slice loop for many slices, 4 blocks per SM (at most
+// 64 registers); NS_FEW = the same loop for at most FEW_SLICES slices, 2
+// blocks per SM (up to 128 registers: every load of a vector is in flight
+// at once).  Measured on the GPT-2 step (8 slices): 9.51 ms with NS_FEW,
+// against 9.72 ms for the loop unrolled for exactly 8 slices and 10.77 ms
+// for the 64-register loop.
 // CHAIN: a chained step (t, S and the state set from a.chain); the other
 // instantiations take everything from their arguments.
 template <int GDT, int PDT, int VEC, int NS, bool CHAIN = false>
-__global__ void __launch_bounds__(TILE_THREADS, (NS == 0 && !CHAIN) ? 4 : 1)   // many slices: 4 blocks per SM
+__global__ void __launch_bounds__(TILE_THREADS, NS == 0 ? (CHAIN ? 3 : 4) : 2)   // chained: 3, so no spills
 k_step_fused(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
     SumSq sumsq;
