@@ -328,3 +328,91 @@ def test_zero3_llama3_8b_rank1(Z):
         orc.apply(a_samp, dt, samp.master, samp.m, samp.v, samp.param, dt, k, scalars(h, t))
         check_state(samp, master, m, v, rshards[me], exact=True)
     assert int(gstatus.item()) == 0
+
+
+@pytest.mark.parametrize("clip", [0.0, 1.0])
+def test_shard_past_the_int32_index_range(Z, clip):
+    """One shard of 2^31 + 4099 elements, so that element, gradient and
+    parameter indices run past 2^31 and the shard ends 3 elements after its
+    last full vector; N_d = 2 staged bf16 slices; parameter offset 8 inside a
+    flat buffer whose other slots must stay untouched.  Without clipping: the
+    fused pass out of place, 2 steps (both state-set directions); with a
+    clip that fires: the in-place two-pass path, 1 step."""
+    nd, dt, o = 2, 2, 8
+    n = (1 << 31) + 4099
+    flat = torch.empty(o + n + 8, dtype=torch.bfloat16, device=DEV)
+    W.fill_normal_(flat, 0.02, W.generator(71, DEV))
+    head, tail = flat[:o].clone(), flat[o + n:].clone()
+    slices = [torch.empty(n, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([72 + r for r in range(nd)], DEV)
+    idx = np.unique(np.concatenate([sample_idx(n, 7, 20000), np.arange((1 << 31) - 24, (1 << 31) + 24),
+                                    np.arange((1 << 31) - TILE - 8, (1 << 31) - TILE + 8)])).astype(np.int64)
+    ti = torch.from_numpy(idx).to(DEV)
+    samp = Sampled(idx, u16(flat[o + ti]), dt)
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    h = hyper32(max_grad_norm=clip)
+    hz = {k: h[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}
+    if clip <= 0.0:
+        sets = [[flat[o:o + n].float(), torch.zeros(n, device=DEV), torch.zeros(n, device=DEV)],
+                [torch.empty(n, device=DEV) for _ in range(3)]]
+        cur = 0
+        for t in (1, 2):
+            gs.draw_plain(slices, 1e-3)
+            sh = [Z.shard(n, 0, o, *sets[cur], *sets[1 - cur])]
+            Z.zero_shard_step(slices, dt, sh, flat, dt, Z.hyper(step=t, **hz), 1.0, 0.0, 0, ws, ws.numel(), res)
+            acc, ovf = oracle_stats(slices, dt, 0, n)
+            k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+            r_gpu = Z.read_result(res)
+            assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (1, 3, 5)
+            assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
+            cur ^= 1
+            samp.step([u16(s[ti]) for s in slices], dt, k, scalars(h, t))
+            check_state(samp, *sets[cur], flat[o:o + n], exact=True)
+        del sets
+    else:
+        master = flat[o:o + n].float()
+        m = torch.zeros(n, device=DEV)
+        v = torch.zeros(n, device=DEV)
+        gshard = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+        gs.draw_plain(slices, 1e-3)
+        sh = [Z.shard(n, 0, o, master, m, v, grad_shard=gshard)]
+        Z.zero_shard_step(slices, dt, sh, flat, dt, Z.hyper(step=1, **hz), 1.0, 0.0, 0, ws, ws.numel(), res)
+        acc, ovf = oracle_stats(slices, dt, 0, n)
+        k, norm, c = orc.grad_multiplier(acc.value(), 1.0, clip)
+        r_gpu = Z.read_result(res)
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (2, 4, 6)
+        assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5) and c < 1.0
+        prev = (samp.master.copy(), samp.m.copy())
+        a = samp.step([u16(s[ti]) for s in slices], dt, k, scalars(h, 1))
+        assert np.array_equal(u16(gshard[ti]), a)                       # reduced gradient: bit-exact
+        check_state(samp, master, m, v, flat[o:o + n], exact=False, prev=prev, g=orc.widen_16(a, dt) * k)
+    assert torch.equal(flat[:o], head) and torch.equal(flat[o + n:], tail)
+
+
+def test_gather_past_the_int32_index_range(Z):
+    """A 16-bit unit of 2^31 + 32 elements (4.3 GB) gathered from 4 equal
+    parts by the register gather and by the TMA gather on every SM and on 32
+    CTAs, then from 4 ragged segments (the TMA gather's fallback to register
+    copies): each equals the concatenation of its parts."""
+    nd = 4
+    p = (1 << 29) + 8
+    parts = [torch.empty(p, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([81 + r for r in range(nd)], DEV)
+    gs.draw_plain(parts, 0.02)
+    want = torch.cat(parts).view(torch.int16)
+    out = torch.empty(nd * p, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out.zero_()
+    Z.zero3_gather_layer(parts, nd * p, 2, out)
+    assert torch.equal(out.view(torch.int16), want)
+    for n_ctas in (0, 32):
+        out.zero_()
+        Z.zero3_gather_bulk(parts, [p] * nd, 2, out, n_ctas, status)
+        assert torch.equal(out.view(torch.int16), want)
+    lens = [p - 3, p, p - 1, p - 5]
+    segs = [x[:n] for x, n in zip(parts, lens)]
+    out.zero_()
+    Z.zero3_gather_bulk(segs, lens, 2, out, 32, status)
+    assert torch.equal(out[:sum(lens)].view(torch.int16), torch.cat(segs).view(torch.int16))
+    assert int(status.item()) == 0
