@@ -243,6 +243,12 @@ def _pin_copies(torch, bufs, e2e):
 
 
 # ------------------------------------------------------------------ workloads (our path)
+def gpt2_desc(name, layers=48):
+    """The GPT-2 workload's description, shared by both arms' `config`."""
+    return (f"{name}: GPT-2-shaped group ({layers} layers, d=1600, vocab 50257, ctx 1024), "
+            "N_d=8, all 8 ranks simulated on one GPU")
+
+
 def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
     """GPT-2 1.5B-shaped group, N_d = 8, all ranks on this GPU, bf16, ping-pong state (fused single pass)."""
     wl = W.workload("gpt2-1.5b-nd8")
@@ -347,8 +353,7 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                 e2e_drain=e2e_drain,
                 e2e_note="each step's gradients are copied from pinned host memory on a copy stream into one of two "
                          "device sets while the previous step computes; the timed region holds one copy per step",
-                config={"workload": f"{name}: GPT-2-shaped group ({layers} layers, d=1600, vocab 50257, ctx 1024), "
-                                    "N_d=8, all 8 ranks simulated on one GPU",
+                config={"workload": gpt2_desc(name, layers),
                         "psi": P, "n_d": nd, "shard_elements": plan["rank_numels"][0], "grad_dtype": "bf16",
                         "param_dtype": "bf16", "state": "f32 master/m/v, ping-pong", "path": "fused single pass",
                         "steps": "zero_shard_step_chained: t, S and the state set in use stay on the device "
@@ -1166,8 +1171,7 @@ def reference_arm(args, rank, world, W):
     line = {"metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "gpt2-1.5b-nd8: GPT-2 1.5B-shaped group, N_d=8, all ranks",
-                       "sample_elements_per_step": n},
+            "config": {"workload": gpt2_desc("gpt2-1.5b-nd8"), "sample_elements_per_step": n},
             "cpu_baseline": {"value": value, "unit": "elements/s", "cores": procs, "kind": "oracle",
                              "sample": f"the first {n_per} elements of each of the 8 shards per step, "
                                        f"{procs} processes each on an equal share",
