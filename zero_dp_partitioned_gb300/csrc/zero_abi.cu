@@ -5,9 +5,10 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
-#include <unordered_map>
+#include <utility>
 
 #include "zero_internal.h"
 #include "zero_stream.cuh"
@@ -26,7 +27,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int max_per_sm) {
     static std::mutex mu;
-    static std::unordered_map<const void*, int> per_sm[16];
+    static std::map<std::pair<const void*, size_t>, int> per_sm[16];    // (kernel, dynamic smem) -> blocks
     static int sms[16] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -35,12 +36,13 @@ int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int ma
     {
         std::lock_guard<std::mutex> g(mu);
         if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        auto it = per_sm[dev].find(func);
+        const auto key = std::make_pair(func, dynamic_smem);
+        auto it = per_sm[dev].find(key);
         if (it == per_sm[dev].end()) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, TILE_THREADS, dynamic_smem) != cudaSuccess ||
                 nb < 1)
                 nb = 1;
-            per_sm[dev][func] = nb;
+            per_sm[dev][key] = nb;
         } else {
             nb = it->second;
         }
