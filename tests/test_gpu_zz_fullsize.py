@@ -122,8 +122,11 @@ def scalars(h, t):
     return orc.make_scalars(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], t)
 
 
-def test_gpt2_1p5b_all_ranks(Z):
-    """GPT-2 1.5B-shaped group, N_d = 8, all ranks, bf16, fused single pass, 3 steps."""
+@pytest.mark.parametrize("chained", [False, True])
+def test_gpt2_1p5b_all_ranks(Z, chained):
+    """GPT-2 1.5B-shaped group, N_d = 8, all ranks, bf16, fused single pass, 3
+    steps: host-driven (the caller swaps the state sets and advances t), and
+    chained as the benchmark runs it (t, S and the current set on the device)."""
     wl = W.workload("gpt2-1.5b-nd8")
     nd, dt = 8, 2
     numels = W.numels(wl.specs)
@@ -144,21 +147,30 @@ def test_gpt2_1p5b_all_ranks(Z):
         idx = o + sample_idx(n, r, 8000)
         samp.append(Sampled(idx, u16(flat[torch.from_numpy(idx).to(DEV)]), dt))
     h = hyper32()
+    hz = {k: h[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}
+    if chained:
+        hy = Z.hyper(step=1, **hz)
+        table = torch.from_numpy(Z.zero_adam_scalar_table(hy, 1, 16)).to(DEV)
+        chain = torch.frombuffer(bytearray(bytes(Z.chain(step=1, loss_scale=1.0))), dtype=torch.uint8).to(DEV)
     cur = 0
     for t in (1, 2, 3):
         gs.draw_flat(grads, wl.specs, W.gpt2_grad_std())
-        A, B = sets[cur], sets[1 - cur]
+        A, B = sets[0 if chained else cur], sets[1 if chained else 1 - cur]
         sh = [Z.shard(n, o, o, A[0][o:o + n], A[1][o:o + n], A[2][o:o + n], B[0][o:o + n], B[1][o:o + n],
                       B[2][o:o + n]) for o, n in zip(plan["rank_offsets"], plan["rank_numels"])]
-        Z.zero_shard_step(grads, dt, sh, flat, dt, Z.hyper(step=t, **{k: h[k] for k in
-                          ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}), 1.0, 0.0, 0, ws,
-                          ws.numel(), res)
+        if chained:
+            Z.zero_shard_step_chained(grads, dt, sh, flat, dt, hy, table, 1, 16, chain, 0.0, 0, ws, ws.numel(), res)
+        else:
+            Z.zero_shard_step(grads, dt, sh, flat, dt, Z.hyper(step=t, **hz), 1.0, 0.0, 0, ws, ws.numel(), res)
         acc, ovf = oracle_stats(grads, dt, 0, P)
         r_gpu = Z.read_result(res)
         k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
         assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path in (1, 3, 5)
         assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
         cur ^= 1
+        if chained:
+            c = Z.read_chain(chain)
+            assert (c.step, c.cur, c.applied, c.skipped, c.failed) == (t + 1, cur, t, 0, 0)
         for s in samp:
             ti = torch.from_numpy(s.idx).to(DEV)
             s.step([u16(g[ti]) for g in grads], dt, k, scalars(h, t))
