@@ -132,7 +132,7 @@ def compare(run, osh, oflat, r_gpu, r_or, exact, prev=None, red=None):
 
 
 def run_both(Z, numels, nd, dt, mode, seed, h, S, pingpong, steps=3, inject=None, extra=(0.0, 0), ranks=None,
-             state_pad=0, param_pad=0, grad_std=1e-3):
+             state_pad=0, param_pad=0, grad_std=1e-3, t0=1):
     p, flat, grads = make_problem(numels, nd, dt, mode, seed, loss_scale=S, grad_std=grad_std, steps=steps)
     if inject:
         inject(grads)
@@ -140,7 +140,7 @@ def run_both(Z, numels, nd, dt, mode, seed, h, S, pingpong, steps=3, inject=None
     run = DeviceRun(Z, p, flat, dt, ranks, pingpong, state_pad=state_pad, param_pad=param_pad)
     osh = oracle_shards(p, flat, dt, ranks)
     oflat = flat.copy()
-    t, Sg, So = 1, S, S
+    t, Sg, So = t0, S, S
     exact = h["max_grad_norm"] <= 0
     results = []
     for k in range(steps):
@@ -228,6 +228,33 @@ def test_huge_finite_squares_use_fp64(Z):
 def test_slice_counts(Z, nd, kernel_path):
     # the loss scale crosses the C ABI as fp32: give the oracle that same value
     run_both(Z, [9000, 1234], nd, 1, 0, nd, hyper32(), float(np.float32(4096.0 / nd)), True, steps=2)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("case", ["lr 0", "wd 0", "betas 0", "t from 1e6", "eps 1", "S 2^14", "S 2^-8"])
+def test_hyperparameters_at_their_edges(Z, dt, case, kernel_path):
+    """Bit-exact steps with the hyper-parameters at the edges of their range:
+    lr = 0 (only the moments move), no weight decay, beta1 = beta2 = 0 (m = g,
+    v = g^2), t starting at 10^6 (both bias corrections round to 1 in fp32),
+    eps = 1, and loss scales of 2^14 and 2^-8 (gradients drawn scaled by S:
+    fp16 gradients of 2^-8 are mostly subnormal)."""
+    kw, S, t0 = {}, 1.0, 1
+    if case == "lr 0":
+        kw = dict(lr=0.0)
+    elif case == "wd 0":
+        kw = dict(weight_decay=0.0)
+    elif case == "betas 0":
+        kw = dict(beta1=0.0, beta2=0.0)
+    elif case == "t from 1e6":
+        t0 = 1_000_000
+    elif case == "eps 1":
+        kw = dict(eps=1.0)
+    elif case == "S 2^14":
+        S = 2.0 ** 14
+    else:
+        S = 2.0 ** -8
+    res = run_both(Z, [20000, 4096, 333], 4, dt, 0, 70, hyper32(**kw), S, True, steps=2, t0=t0)
+    assert all(g["applied"] == 1 for g, _ in res)
 
 
 def test_unaligned_pointers_take_the_scalar_path(Z):
