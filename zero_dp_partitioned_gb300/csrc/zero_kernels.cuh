@@ -464,7 +464,8 @@ __device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d,
 // *_out state is only committed by the caller when result->applied; the
 // parameters are restored by k_recover on overflow.
 // NS: 0 = the generic slice loop for many slices, 4 blocks per SM (at most
-// 64 registers); NS_FEW = the same loop for at most FEW_SLICES slices, 2
+// 64 registers; chained steps 3, at most 85); NS_FEW = the same loop for at
+// most FEW_SLICES slices, 2
 // blocks per SM (up to 128 registers: every load of a vector is in flight
 // at once).  Measured on the GPT-2 step (8 slices): 9.51 ms with NS_FEW,
 // against 9.72 ms for the loop unrolled for exactly 8 slices and 10.77 ms
