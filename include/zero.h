@@ -29,7 +29,9 @@
  * Conventions for every entry point:
  *  - Device pointers are CUDA device (or managed) addresses on the current
  *    device; host pointers are plain CPU memory.  The caller owns every
- *    buffer; the library allocates nothing and keeps no state between calls.
+ *    buffer; the library allocates nothing (zero_shard_step_noalloc's scratch
+ *    is an array compiled into it) and carries no data from one call to the
+ *    next (chained steps carry theirs in the caller's zero_chain).
  *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and is asynchronous: results land in caller memory when
  *    the stream reaches them.  No entry point synchronises.
@@ -450,9 +452,8 @@ typedef struct {
  * on the host as zero_shard_step computes them (fp64, each rounded once to
  * fp32): table_out[2 i] = lr / (1 - beta1^t), table_out[2 i + 1] =
  * 1 / sqrt(1 - beta2^t) with t = t0 + i.  table_out: host, 2 n floats.  Copy
- * it to the device for zero_shard_step_chained.  Returns ZERO_OK or
- * ZERO_EINVAL (t0 < 1, n < 0, NULL pointers, hyper-parameters as
- * zero_shard_step checks them). */
+ * it to the device for zero_shard_step_chained.  hyper->step is ignored.
+ * Returns ZERO_OK or ZERO_EINVAL (t0 < 1, n < 0, NULL pointers). */
 int zero_adam_scalar_table(const zero_hyper* hyper, int64_t t0, int64_t n, float* table_out);
 
 /* One step with its bookkeeping on the device: what zero_shard_step computes
