@@ -1001,15 +1001,24 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 
 def build_line(world, steps, warmup, ms, elements, nd, config, roofline, kernels, cpu, e2e, clocks, launches,
-               formula_bytes=None):
+               formula_bytes=None, actual_bytes=None, peak=None):
     """The JSON line rank 0 prints: value is the whole job's shard elements per
-    second (every rank runs its own copy of the workload, so scaling is weak)."""
+    second (every rank runs its own copy of the workload, so scaling is weak).
+    The step's bandwidth is given twice: by the formula's bytes ((2 N_d + 26)
+    per element, or the ZeRO-3 sum) and by the bytes the kernels of the step
+    move by design, each as a fraction of the measured and the nominal peak."""
     fb = formula_bytes if formula_bytes is not None else elements * (2 * nd + 26)
+    step_bw = None
+    if actual_bytes is not None and peak:
+        f, a = fb / (ms / 1e3) / 1e9, actual_bytes / (ms / 1e3) / 1e9
+        step_bw = {"formula_bytes": fb, "formula_gbs": f, "formula_frac": f / peak,
+                   "formula_frac_of_nominal": f / NOMINAL_HBM_GBS, "actual_bytes": actual_bytes, "actual_gbs": a,
+                   "actual_frac": a / peak, "actual_frac_of_nominal": a / NOMINAL_HBM_GBS}
     return {"metric": METRIC, "value": world * elements / (ms / 1e3), "unit": "elements/s",
             "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch generators; no data set or weights)",
-            "config": config, "achieved_gbs_formula": fb / (ms / 1e3) / 1e9,
+            "config": config, "achieved_gbs_formula": fb / (ms / 1e3) / 1e9, "step_bandwidth": step_bw,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": launches, "impl": "ours"}
 
@@ -1130,7 +1139,8 @@ def main():
     if rank == 0:
         line = build_line(world, args.steps, max(3, args.warmup), ms, wl["elements"], wl["nd"], wl["config"],
                           roofline, per_kernel, cpu, e2e, clocks, wl["launches_per_step"] * args.steps,
-                          wl["formula_bytes"] if wl["name"].startswith("zero3") else None)
+                          wl["formula_bytes"] if wl["name"].startswith("zero3") else None,
+                          actual_bytes=sum(wl["kernel_bytes"].values()), peak=peak)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -59,6 +59,13 @@ def test_line_fields():
     assert set(line["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
     assert line["achieved_gbs_formula"] == pytest.approx(1_557_611_200 * 42 / 0.010 / 1e9)
     assert line["config"]["workload"] == "w" and "model" not in line["config"]
+    assert line["step_bandwidth"] is None
+    two_pass = bench.build_line(1, 100, 5, 10.0, 1000, 4, {"workload": "w"}, roof, {}, cpu, e2e, clocks, 200,
+                                actual_bytes=38 * 1000, peak=6792.1)
+    bw = two_pass["step_bandwidth"]
+    assert bw["formula_bytes"] == 34 * 1000 and bw["actual_gbs"] == pytest.approx(38 * 1000 / 0.010 / 1e9)
+    assert bw["actual_frac"] == pytest.approx(bw["actual_gbs"] / 6792.1)
+    assert bw["formula_frac_of_nominal"] == pytest.approx(bw["formula_gbs"] / bench.NOMINAL_HBM_GBS)
 
 
 def test_every_input_helper_bench_and_tests_use_exists():
