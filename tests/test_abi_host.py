@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -176,3 +177,16 @@ def test_round_robin_equals_oracle(Z, orc):
             assert Z.zero_plan_round_robin(n, ws) == orc.round_robin(n, ws).tolist()
     with pytest.raises(Z.ZeroError):
         Z.zero_plan_round_robin(4, 0)
+
+
+def test_import_without_the_library_fails_loudly(tmp_path):
+    """The package has no fallback: without its built library the import
+    raises, and nothing in it reaches for the oracle."""
+    pkg = tmp_path / "zero_dp_partitioned_gb300"
+    pkg.mkdir()
+    src = open(os.path.join(ROOT, "zero_dp_partitioned_gb300", "__init__.py")).read()
+    assert "oracle" not in src
+    (pkg / "__init__.py").write_text(src)
+    r = subprocess.run([sys.executable, "-c", "import zero_dp_partitioned_gb300"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode != 0 and "ImportError" in r.stderr and "libzero_gb300.so is missing" in r.stderr
