@@ -17,9 +17,11 @@ int cuda_fail(cudaError_t e, const char* what);
 // Measured on GB300 over the full workloads: passes that write a third or
 // more of their bytes (the fused pass with few slices, the apply pass) reach
 // more of the HBM bandwidth with fewer concurrent warps -- 2 blocks of 256
-// threads per SM: 10.8 ms vs 11.7 ms for the 8-slice fused GPT-2 step at the 4
-// blocks its registers allow, 8.5 ms vs 9.7 ms for the Llama apply pass --
-// while read-dominated passes want every block they can get (the 64-slice
+// threads per SM: 10.8 ms vs 11.7 ms for the 8-slice fused GPT-2 step at 4
+// blocks (with an earlier 64-register loop; the loop now used needs up to 128
+// registers, so 2 blocks is also all that fits), 8.6 ms vs 9.5 ms at 3
+// blocks for the Llama apply pass -- while read-dominated passes want every
+// block they can get (the 64-slice
 // fused pass: 2.63 ms at 4 blocks, 3.11 ms at 2; the reduce pass is best at
 // 6: 2.98 ms, against 3.13 at 4 and 3.11 at the 8 its 32 registers allow);
 // the gather (a copy) peaks at 4.
@@ -66,8 +68,8 @@ int launch_gather_bulk(const BulkGatherArgs& a, int grid, cudaStream_t s);
 
 // The shared-memory-staged passes with a block-wide cycle per chunk
 // (zero_stream.cu): selected only by ZERO_GB300_PATH=stream; on GB300 they
-// are slower than the register-staged passes (14.1 ms vs 10.8 ms for the
-// fused GPT-2 step at the time) and than the producer/consumer fused pass.
+// are slower than the register-staged passes (14.1 ms for the fused GPT-2
+// step, against 10.8 ms for the register pass of the time and 9.5 ms now).
 struct StreamArgs;
 int stream_stages(int n_grad_arrays);
 int launch_stream(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
