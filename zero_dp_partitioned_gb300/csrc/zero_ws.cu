@@ -1,11 +1,15 @@
 // zero_ws.cu -- the fused single pass with a producer warp feeding TMA-staged
 // chunks to consumer warps.
 //
-// The register-staged fused pass keeps the bytes in flight its registers
-// allow; moving the same traffic mix by bulk asynchronous copies reaches more
-// of the HBM bandwidth (6.8-7.1 TB/s against 6.7 for registers).  The
-// staged pass with a block-wide cycle per chunk loses that again to the
-// cycle.  Here the roles are split (two blocks of 8 warps per SM):
+// An alternative to the register-staged fused pass, selected by
+// ZERO_GB300_PATH=ws.  Moving the pass's traffic mix by bulk asynchronous
+// copies reached more of the HBM bandwidth than a 64-register pass could
+// (6.8-7.1 TB/s against 6.7), and this pass measured 9.62-9.71 ms on the
+// GPT-2 step against 10.01 ms for that register pass; the register pass that
+// now keeps every load of a vector in flight (up to 128 registers) takes
+// 9.50 ms, so this one is opt-in.  The staged pass with a block-wide cycle
+// per chunk loses the copies' advantage to the cycle.  Here the roles are
+// split (two blocks of 8 warps per SM):
 //   warp 0, lane 0 (producer): for each chunk of this block, waits until the
 //     stage it needs is free, then issues the bulk loads of the chunk's
 //     gradient slices and fp32 state into it (one full mbarrier per stage,
@@ -42,7 +46,7 @@ constexpr int WS_HEADER = 128;                           // 8 full + 8 empty mba
 // Two blocks per SM: 14 consumer warps with 8 elements each.  Measured on the
 // GPT-2 step (N_d = 8): 9.83 ms, against 9.89 / 9.92 ms with 4 elements at 2 / 3
 // blocks, 10.28 ms with 8 elements at one block (4 stages), 12.3 ms with 4
-// elements at one block; the register-staged pass takes 10.01 ms.
+// elements at one block; the 64-register pass of the time took 10.01 ms.
 constexpr int WS_BLOCKS_PER_SM = 2;
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
