@@ -5,10 +5,12 @@
 // producer lane and consumer warps without that cycle.  This file also holds
 // the PTX wrappers (mbarrier, bulk copies) the TMA kernels share.
 //
-// Why: the register-staged kernels keep at most ~4 blocks of 256 threads per
-// SM (64 / 50 registers), so the bytes they keep in flight, and with them the
-// HBM bandwidth they reach, are bounded by registers; seven 128-bit stores
-// per thread per 8 elements also fill the store queue.  Here each array's
+// Why it was built: register-staged kernels bound the bytes they keep in
+// flight, and with them the HBM bandwidth they reach, by their registers;
+// seven 128-bit stores per thread per 8 elements also fill the store queue.
+// (Measured since: a chunk's block-wide cycle costs more than the copies
+// save -- 14.1 ms for the GPT-2 step -- and the register pass with every load
+// of a vector in flight reaches the copy bandwidth.)  Here each array's
 // chunk is moved by one bulk asynchronous copy (cp.async.bulk, executed by
 // the TMA unit) into a ring of shared-memory stages tracked by mbarriers, and
 // the results leave by bulk stores from a double-buffered output stage.
