@@ -262,8 +262,7 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
     flat = W.flat_params(specs, P, torch.bfloat16, wl.param_seed, dev)
     grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
         [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(nd)], specs, W.gpt2_grad_std())
-    sets = [[flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)],
-            [torch.empty(P, device=dev) for _ in range(3)]]
+    sets = [[torch.empty(P, device=dev) for _ in range(3)] for _ in range(2)]
 
     def shards(cur):
         i, o = sets[cur], sets[1 - cur]
@@ -272,6 +271,7 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                 for off, n in zip(plan["rank_offsets"], plan["rank_numels"])]
 
     variants = [shards(0), shards(1)]
+    Z.zero_shard_init(variants[0], flat, Z.ZERO_BF16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
@@ -377,8 +377,7 @@ def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None):
     grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
         [torch.empty(P, dtype=torch.float16, device=dev) for _ in range(nd)], wl.specs, lambda s: wl.grad_std,
         wl.loss_scale)
-    sets = [[flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)],
-            [torch.empty(P, device=dev) for _ in range(3)]]
+    sets = [[torch.empty(P, device=dev) for _ in range(3)] for _ in range(2)]
 
     def shards(cur):
         i, o = sets[cur], sets[1 - cur]
@@ -387,6 +386,7 @@ def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None):
                 for off, n in zip(plan["rank_offsets"], plan["rank_numels"])]
 
     variants = [shards(0), shards(1)]
+    Z.zero_shard_init(variants[0], flat, Z.ZERO_F16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
@@ -461,10 +461,11 @@ def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None):
     flat = W.flat_params(specs, P, torch.bfloat16, wl.param_seed, dev)
     grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
         [torch.empty(P, dtype=torch.bfloat16, device=dev) for _ in range(nd)], specs, W.gpt2_grad_std())
-    state = [flat.float(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)]
+    state = [torch.empty(P, device=dev) for _ in range(3)]
     avg = torch.empty(P, dtype=torch.bfloat16, device=dev)          # the all-reduced gradient
     sh = [Z.shard(n, off, off, *(x[off:off + n] for x in state), grad_shard=avg[off:off + n])
           for off, n in zip(plan["rank_offsets"], plan["rank_numels"])]
+    Z.zero_shard_init(sh, flat, Z.ZERO_BF16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     stats = torch.zeros(16, dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
@@ -505,9 +506,10 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
     flat = W.flat_params(wl.specs, P, torch.bfloat16, wl.param_seed, dev)
     slices = W.GradStream([2 + j for j in range(nd)], dev).draw_plain(
         [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(nd)], wl.grad_std)
-    master, m, v = flat[o:o + n].float(), torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    master, m, v = (torch.empty(n, device=dev) for _ in range(3))
     gshard = torch.empty(n, dtype=torch.bfloat16, device=dev)
     sh = [Z.shard(n, 0, o, master, m, v, grad_shard=gshard)]
+    Z.zero_shard_init(sh, flat, Z.ZERO_BF16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     stats = torch.zeros(16, dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
@@ -554,9 +556,9 @@ def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None):
     slices = W.GradStream([4 + j for j in range(nd)], dev).draw_plain(
         [torch.empty(n, dtype=torch.float16, device=dev) for _ in range(nd)], wl.grad_std, wl.loss_scale)
     W.zero_every_100th_(slices[0])
-    sets = [[flat[o:o + n].float(), torch.zeros(n, device=dev), torch.zeros(n, device=dev)],
-            [torch.empty(n, device=dev) for _ in range(3)]]
+    sets = [[torch.empty(n, device=dev) for _ in range(3)] for _ in range(2)]
     variants = [[Z.shard(n, 0, o, *sets[c], *sets[1 - c])] for c in (0, 1)]
+    Z.zero_shard_init(variants[0], flat, Z.ZERO_F16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
@@ -618,9 +620,10 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
         gs.draw_plain(row, wl.grad_std)
         buckets.append((u, row))
     layer = torch.empty(max(units), dtype=torch.bfloat16, device=dev)
-    master, m, v = rshards[me].float(), torch.zeros(L, device=dev), torch.zeros(L, device=dev)
+    master, m, v = (torch.empty(L, device=dev) for _ in range(3))
     gshard = torch.empty(L, dtype=torch.bfloat16, device=dev)
     sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
+    Z.zero_shard_init(sh, rshards[me], Z.ZERO_BF16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     stats = torch.zeros(16, dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
@@ -687,9 +690,10 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
         buckets[u] = gs.draw_plain([torch.empty(units[u], dtype=torch.bfloat16, device=dev) for _ in range(nd)],
                                    wl.grad_std)
     layer = torch.empty(max(units), dtype=torch.bfloat16, device=dev)
-    master, m, v = segs[me].float(), torch.zeros(L, device=dev), torch.zeros(L, device=dev)
+    master, m, v = (torch.empty(L, device=dev) for _ in range(3))
     gseg = torch.empty(L, dtype=torch.bfloat16, device=dev)
     sh_apply = [Z.shard(L, 0, 0, master, m, v, grad_shard=gseg)]
+    Z.zero_shard_init(sh_apply, segs[me], Z.ZERO_BF16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     stats = torch.zeros(16, dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
@@ -764,9 +768,10 @@ def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, tokens=1024, gathe
     X = W.fill_normal_(torch.empty(tokens * cols, dtype=torch.bfloat16, device=dev), 1.0,
                        W.generator(77, dev)).view(tokens, cols)
     Y = torch.empty(max(units) // cols, tokens, dtype=torch.bfloat16, device=dev)
-    master, m, v = rshards[me].float(), torch.zeros(L, device=dev), torch.zeros(L, device=dev)
+    master, m, v = (torch.empty(L, device=dev) for _ in range(3))
     gshard = torch.empty(L, dtype=torch.bfloat16, device=dev)
     sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
+    Z.zero_shard_init(sh, rshards[me], Z.ZERO_BF16)
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     stats = torch.zeros(16, dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)

@@ -307,6 +307,19 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
                     void* workspace, size_t workspace_bytes,
                     zero_result* result, void* stream);
 
+/* State initialisation, before the first step: for every shard, master_in[i]
+ * = fp32(flat_param[param_offset + i]) (the exact widening of the 16-bit
+ * value) and m_in[i] = v_in[i] = 0.
+ * Source: DeepSpeed ZeRO stages 1-2 walkthrough, 4 (3): each rank keeps an
+ * fp32 copy of its own partition of the 16-bit parameters (the master
+ * weights); Adam's moments start at zero (reading notes, 3).
+ * shards and flat_param as for zero_shard_step (all six state pointers set and
+ * 4-byte aligned; only the *_in set is written; grad_offset and grad_shard
+ * are not used); param_dtype is flat_param's.  Errors: ZERO_EINVAL,
+ * ZERO_EALIGN, ZERO_ELIMIT (more than ZERO_MAX_SHARDS shards), ZERO_ECUDA. */
+int zero_shard_init(const zero_shard* shards, int n_shards, const void* flat_param, int param_dtype,
+                    void* stream);
+
 /* First pass alone: reduce each shard's slices into its grad_shard
  * (a = round16(sum_r fp32(g_r) / n_slices), rank order) and add the shards'
  * sum of squares and overflow flag to *stats (device).  accumulate = 0 starts

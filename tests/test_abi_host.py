@@ -159,6 +159,18 @@ def test_argument_errors_before_any_device_work(Z):
     assert e.value.code == Z.ZERO_EINVAL
     with pytest.raises(Z.ZeroError):
         Z.zero_plan([1, 2], 0)
+    for shards, flat, pdt, code in ((sh, fake, 3, Z.ZERO_EINVAL),                              # unknown dtype
+                                    (sh, fake + 1, Z.ZERO_BF16, Z.ZERO_EINVAL),                # odd parameter buffer
+                                    (sh, 0, Z.ZERO_BF16, Z.ZERO_EINVAL),                       # no parameter buffer
+                                    ([Z.shard(8, 0, 0, fake + 2, fake, fake, fake, fake, fake)], fake, Z.ZERO_BF16,
+                                     Z.ZERO_EALIGN),
+                                    ([Z.shard(8, 0, 0, 0, fake, fake, fake, fake, fake)], fake, Z.ZERO_BF16,
+                                     Z.ZERO_EINVAL),
+                                    (sh * 65, fake, Z.ZERO_BF16, Z.ZERO_ELIMIT)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_init(shards, flat, pdt, stream=0)
+        assert e.value.code == code
+    Z.zero_shard_init([Z.shard(0, 0, 0, 0, 0, 0, 0, 0, 0)], 0, Z.ZERO_BF16, stream=0)   # nothing to do: no launch
 
 
 def test_comm_volume_equals_oracle(Z, orc):

@@ -39,8 +39,7 @@ class ChainRun:
         self.Z, self.p, self.dt, self.h = Z, p, dt, h
         P = flat.size
         self.flat = dev16(flat, dt)
-        self.sets = [[self.flat.float(), torch.zeros(P, device=DEV), torch.zeros(P, device=DEV)],
-                     [torch.empty(P, device=DEV) for _ in range(3)]]
+        self.sets = [[torch.empty(P, device=DEV) for _ in range(3)] for _ in range(2)]
         self.gshard = torch.empty(P, dtype=TDT[dt], device=DEV)
         self.chain = chain_tensor(Z, 1, S)
         self.hyper = Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], h["max_grad_norm"], 1)
@@ -52,6 +51,7 @@ class ChainRun:
         self.shards = [Z.shard(int(n), int(o), int(o), *(x[int(o):int(o) + int(n)] for x in A),
                                *(x[int(o):int(o) + int(n)] for x in B), self.gshard[int(o):int(o) + int(n)])
                        for o, n in zip(p["rank_offsets"], p["rank_numels"])]
+        Z.zero_shard_init(self.shards, self.flat, dt)     # master = fp32(parameters), m = v = 0
 
     def step(self, slices_dev, stream=None):
         self.Z.zero_shard_step_chained(slices_dev, self.dt, self.shards, self.flat, self.dt, self.hyper, self.table, 1,

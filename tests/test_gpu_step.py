@@ -63,10 +63,11 @@ class DeviceRun:
         for r in ranks:
             o, n = int(p["rank_offsets"][r]), int(p["rank_numels"][r])
             mk = lambda v: torch.cat([torch.zeros(state_pad, device=DEV), v])[state_pad:]
-            A = [mk(self.flat[o:o + n].float()), mk(torch.zeros(n, device=DEV)), mk(torch.zeros(n, device=DEV))]
+            A = [mk(torch.empty(n, device=DEV)) for _ in range(3)]
             B = [mk(torch.empty(n, device=DEV)) for _ in range(3)] if pingpong else A
             g = torch.empty(n, dtype=TDT[dt], device=DEV) if want_grad else None
             self.state.append(dict(o=o, n=n, A=A, B=B, g=g))
+        Z.zero_shard_init(self.shards(), self.flat, dt)       # master = fp32(parameters), m = v = 0
         self.ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
         self.res = torch.zeros(48, dtype=torch.uint8, device=DEV)
 
@@ -255,6 +256,43 @@ def test_hyperparameters_at_their_edges(Z, dt, case, kernel_path):
         S = 2.0 ** -8
     res = run_both(Z, [20000, 4096, 333], 4, dt, 0, 70, hyper32(**kw), S, True, steps=2, t0=t0)
     assert all(g["applied"] == 1 for g, _ in res)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("state_pad", [0, 1])
+def test_shard_init_widens_the_parameters(Z, dt, state_pad):
+    """zero_shard_init: every rank's master_in = fp32(its 16-bit parameters),
+    bit for bit the oracle's widening, and m_in = v_in = 0, over a group with
+    odd shard offsets (the unpadded plan), an empty rank, state pointers on
+    and off 16-byte alignment, and parameters holding infinities, zeros of
+    both signs and subnormals (NaN patterns need only widen to NaN)."""
+    numels, nd = [20000, 4096, 7, 333], 5
+    p, flat, _ = make_problem(numels, nd, dt, 1, 90, steps=1)
+    flat = flat.copy()
+    specials = ([0x7C00, 0xFC00, 0x7E00, 0x0001, 0x8001, 0x03FF, 0x0000, 0x8000] if dt == 1 else
+                [0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001, 0x007F, 0x0000, 0x8000])
+    flat[100:108] = specials
+    flat[int(p["rank_offsets"][3]):int(p["rank_offsets"][3]) + 8] = specials
+    fdev = dev16(flat, dt)
+    ranks = list(range(nd)) + [nd]       # plus an empty shard
+    shards, state = [], []
+    for r in ranks:
+        o = int(p["rank_offsets"][r]) if r < nd else 0
+        n = int(p["rank_numels"][r]) if r < nd else 0
+        bufs = [torch.full((n + state_pad,), float("nan"), device=DEV)[state_pad:] for _ in range(3)]
+        shards.append(Z.shard(n, o, o, *bufs, *bufs))
+        state.append((o, n, bufs))
+    Z.zero_shard_init(shards, fdev, dt)
+    torch.cuda.synchronize()
+    for o, n, (m0, m1, m2) in state:
+        want = orc.widen_16(flat[o:o + n], dt)
+        got = m0.cpu().numpy()
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+        for z in (m1, m2):
+            assert np.array_equal(z.cpu().numpy().view(np.uint32), np.zeros(n, np.uint32))
+    assert torch.equal(fdev.view(torch.int16), dev16(flat, dt).view(torch.int16))     # parameters untouched
 
 
 def test_unaligned_pointers_take_the_scalar_path(Z):

@@ -79,6 +79,7 @@ _SIGS = {
     "zero_workspace_bytes": (ctypes.c_size_t, []),
     "zero_shard_step": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, ctypes.c_double, _I, _P,
                              ctypes.c_size_t, _P, _P]),
+    "zero_shard_init": (_I, [_P, _I, _P, _I, _P]),
     "zero_shard_reduce": (_I, [_P, _I, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
     "zero_shard_apply": (_I, [_P, _I, _I, _P, _I, _P, ctypes.c_float, _P, ctypes.c_double, _I, _P, ctypes.c_size_t,
                               _P, _P]),
@@ -218,6 +219,13 @@ def zero_shard_step_noalloc(grad_slices, grad_dtype, shards, flat_param, param_d
     _check(lib.zero_shard_step_noalloc(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards),
                                        _ptr(flat_param), param_dtype, ctypes.byref(hyper), loss_scale, extra_sumsq,
                                        int(extra_overflow), _ptr(result), _stream(stream)))
+
+
+def zero_shard_init(shards, flat_param, param_dtype, stream=None):
+    """Before the first step: every shard's master_in = fp32(its 16-bit
+    parameters in flat_param), m_in = v_in = 0."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_init(sh, len(shards), _ptr(flat_param), param_dtype, _stream(stream)))
 
 
 def zero_shard_reduce(grad_slices, grad_dtype, shards, accumulate, stats, workspace, workspace_bytes, stream=None):

@@ -470,6 +470,18 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
     return launch_apply(a, grad_dtype, param_dtype, vec, s);
 }
 
+int zero_shard_init(const zero_shard* shards, int n_shards, const void* flat_param, int param_dtype, void* stream) {
+    if (!valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    int rc;
+    if ((rc = pack_shards(a, shards, n_shards, 1)) != ZERO_OK) return rc;
+    if (!any_elements(a)) return ZERO_OK;
+    if (!flat_param || !aligned(flat_param, 2)) return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = const_cast<void*>(flat_param);
+    return launch_init(a, param_dtype, static_cast<cudaStream_t>(stream));
+}
+
 int zero_adam_scalar_table(const zero_hyper* hyper, int64_t t0, int64_t n, float* table_out) {
     if (!hyper || t0 < 1 || n < 0 || (n > 0 && !table_out)) return fail(ZERO_EINVAL, "zero_adam_scalar_table: bad argument");
     zero_hyper h = *hyper;

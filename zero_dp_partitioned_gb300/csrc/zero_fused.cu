@@ -56,6 +56,35 @@ int launch_recover(const StepArgs& a, int pdt, cudaStream_t s) {
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "recover launch");
 }
 
+// ---------------------------------------------------------------- K0: state initialisation
+// Every shard's *_in set: master = fp32(param) (the exact widening of the
+// 16-bit value at the shard's parameter offset), m = v = 0.
+template <int PDT>
+__global__ void __launch_bounds__(TILE_THREADS) k_init(const __grid_constant__ StepArgs a) {
+    const uint16_t* P = static_cast<const uint16_t*>(a.flat_param);
+    for (int si = 0; si < a.n_shards; ++si) {
+        const ShardDev& d = a.shards[si];
+        float* M = const_cast<float*>(d.mi);
+        float* Mm = const_cast<float*>(d.mmi);
+        float* V = const_cast<float*>(d.vi);
+        for (int64_t i = (int64_t)blockIdx.x * TILE_THREADS + threadIdx.x; i < d.numel;
+             i += (int64_t)gridDim.x * TILE_THREADS) {
+            M[i] = Half16<PDT>::widen(P[d.param_off + i]);
+            Mm[i] = 0.0f;
+            V[i] = 0.0f;
+        }
+    }
+}
+
+int launch_init(const StepArgs& a, int pdt, cudaStream_t s) {
+    const void* f = pdt == ZERO_BF16 ? (const void*)k_init<ZERO_BF16> : (const void*)k_init<ZERO_F16>;
+    int64_t n = 0;
+    for (int i = 0; i < a.n_shards; ++i) n = a.shards[i].numel > n ? a.shards[i].numel : n;
+    const int grid = grid_for(f, (n + TILE_THREADS - 1) / TILE_THREADS, 0);
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "init launch");
+}
+
 // ---------------------------------------------------------------- chained steps: the bookkeeping
 // After a chained step's kernels: applied -> next t, the other state set;
 // overflow -> half the loss scale; another failure -> counted only.

@@ -43,6 +43,7 @@ int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int ma
 // ZERO_OK or ZERO_ECUDA.  vec is 8 or 1.
 int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s);
 int launch_recover(const StepArgs& a, int pdt, cudaStream_t s);
+int launch_init(const StepArgs& a, int pdt, cudaStream_t s);
 int launch_chain_update(zero_chain* chain, const zero_result* result, cudaStream_t s);
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s);
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s);
