@@ -22,20 +22,29 @@ def _port():
 def _worker(rank, port, out):
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2",
+                      LOCAL_RANK=str(rank))
     dist.init_process_group("gloo", rank=rank, world_size=2)
     import bench
-    got = bench.max_over_ranks(10.0 + 3.5 * rank, 2, "cpu")          # rank 1 is the slower one
+    r, w, local = bench.dist_env()
+    got = bench.max_over_ranks(10.0 + 3.5 * rank, w, "cpu")          # rank 1 is the slower one
+    line = bench.build_line(w, 100, 5, got, 1000, 8, {"workload": "w"}, {}, {}, None, None, {}, 300)
     dist.barrier()
-    open(f"{out}.{rank}", "w").write(repr(got))
+    open(f"{out}.{rank}", "w").write(f"{r} {w} {local} {got!r} {line['value']!r} {line['n_gpus']}")
     dist.destroy_process_group()
 
 
 @pytest.mark.timeout(300)
-def test_max_over_two_ranks(tmp_path):
+def test_two_ranks_charge_the_slowest_and_sum_the_work(tmp_path):
+    """The N > 1 timing path over two gloo processes: each rank reads its rank
+    from the environment, both are charged the slowest rank's time, and the
+    job's value counts both ranks' elements over that time (weak scaling)."""
     out = str(tmp_path / "r")
     mp.start_processes(_worker, args=(_port(), out), nprocs=2, start_method="spawn", join=True)
-    assert [float(open(f"{out}.{r}").read()) for r in range(2)] == [13.5, 13.5]
+    for rank in range(2):
+        r, w, local, got, value, n = open(f"{out}.{rank}").read().split()
+        assert (int(r), int(w), int(local), int(n)) == (rank, 2, rank, 2)
+        assert float(got) == 13.5 and float(value) == pytest.approx(2 * 1000 / 0.0135)
 
 
 def test_single_rank_needs_no_process_group():
@@ -106,3 +115,4 @@ def test_all_cores_oracle_timing_splits_the_work_exactly():
         oracle.zero_step(grads, 2, shards, ref, 2, dict(h, max_grad_norm=0.0), t, 1.0)
     assert not np.array_equal(ref, flat)
     assert np.array_equal(got, ref)
+
