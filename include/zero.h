@@ -40,6 +40,18 @@
  *    message (per thread).  Conditions found on the device (overflow) are
  *    reported in zero_result, never by a trap.
  *  - 16-bit element offsets and counts are in elements, int64.
+ *
+ * Earlier descriptions of this interface used other names for some calls and
+ * codes; each stands for the entry point given here:
+ *  - zero_shard_stats (the reduce phase alone)   -> zero_shard_reduce
+ *  - a `divisor` argument of the step            -> none: the averaging divisor
+ *    is n_slices (N_d); the ZeRO-3 shard update, whose gradient is already
+ *    averaged (divisor 1), is zero_shard_apply on the reduced shard
+ *  - zero_workspace_bytes(n_shards, max_numel)  -> zero_workspace_bytes(void):
+ *    the workspace has one fixed size, whatever the shards
+ *  - ZERO_ENOMEM_WS                              -> ZERO_EWORKSPACE
+ *  - an out-parameter "overflow flag + norm"     -> zero_result (overflow,
+ *    applied, sumsq, grad_norm, clip_coef, grad_mult)
  */
 #ifndef ZERO_GB300_H
 #define ZERO_GB300_H
@@ -60,10 +72,9 @@ typedef enum {
     ZERO_EALIGN = -2,      /* a pointer is not aligned to its element size */
     ZERO_EWORKSPACE = -3,  /* workspace missing or smaller than zero_workspace_bytes() */
     ZERO_ECUDA = -4,       /* a CUDA runtime call or launch failed */
-    ZERO_ELIMIT = -5,      /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards; a call beyond
+    ZERO_ELIMIT = -5       /* more than ZERO_MAX_SLICES slices or ZERO_MAX_SHARDS shards; a call beyond
                               zero_shard_step_noalloc's scratch; (zero_result.status) a chained step outside
                               its scalar table */
-    ZERO_ETIMEOUT = -6     /* (zero_result.status only) a device-side wait gave up; the step was not applied */
 } zero_status;
 
 typedef enum { ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype;
@@ -212,18 +223,10 @@ typedef struct {
  *            then the *_in state is the current state, and the parameters are
  *            as before the call (restored by the library where a speculative
  *            pass had written them)
- * path       which kernels ran the update: 1 = fused single pass (register
- *            staged), 2 = apply pass (register staged), 3 = fused single pass
- *            through shared-memory stages fed by bulk asynchronous (TMA)
- *            copies, 4 = apply pass through such stages, 5 = fused single
- *            pass with a producer warp issuing TMA copies into stages that
- *            consumer warps work from, 6 = apply pass built the same way
- * status     0, or ZERO_ETIMEOUT when a device-side wait gave up: the step is
- *            then reported as not applied, the parameters are restored, and
- *            the *_out state is indeterminate (for an in-place update that is
- *            the state itself: treat the state as lost); ZERO_ELIMIT for a
- *            chained step whose t lies outside its scalar table (nothing is
- *            updated)
+ * path       which kernels ran the update: 1 = the fused single pass,
+ *            2 = the apply pass (after the reduce pass)
+ * status     0, or ZERO_ELIMIT for a chained step whose t lies outside its
+ *            scalar table (nothing is updated)
  * sumsq      sum of squares of the scaled reduced gradient plus extra_sumsq
  * grad_norm  sqrt(sumsq) / loss_scale
  * clip_coef  max_grad_norm / (grad_norm + 1e-6) when that is below 1, else 1
@@ -236,24 +239,13 @@ typedef struct {
 } zero_result;
 
 /* Bytes of device workspace the step calls need (zero_shard_step,
- * zero_shard_reduce, zero_shard_apply, zero3_reduce_bucket): per-block partial
- * sums and flags, a completion counter and the step's internal statistics.
- * The workspace must be zero-filled once before its first use; every call
- * leaves it ready for the next.  Calls that share a workspace must not overlap
- * on the device.
- *
- * Environment (read at each call; meant for tests and measurements):
- *   ZERO_GB300_PATH=register          the register-staged kernels (the default)
- *   ZERO_GB300_PATH=stream            the fused and apply passes through
- *       shared-memory stages with a block-wide cycle per chunk, where the
- *       alignment rules below allow it (slower on GB300; kept for comparison)
- *   ZERO_GB300_PATH=ws                the producer/consumer fused and apply
- *       passes where allowed (a producer warp feeding TMA stages to consumer
- *       warps; 1-10% slower than the register passes on GB300)
- *   ZERO_GB300_SPIN_LIMIT=n           tries per device-side wait of the
- *       shared-memory-staged kernels (default 4194304); 0 makes every first
- *       wait give up, which exercises the ZERO_ETIMEOUT path without hanging
- *       anything */
+ * zero_shard_reduce, zero_shard_apply, zero3_reduce_bucket,
+ * zero_shard_step_chained): per-block partial sums and flags, a completion
+ * counter and the step's internal statistics.  The amount is fixed (it
+ * depends on the most blocks a pass launches, not on the shard sizes), so the
+ * call takes no size arguments.  The workspace must be zero-filled once before
+ * its first use; every call leaves it ready for the next.  Calls that share a
+ * workspace must not overlap on the device. */
 size_t zero_workspace_bytes(void);
 
 /* The whole partitioned step over n_shards shards that share one global
@@ -288,17 +280,12 @@ size_t zero_workspace_bytes(void);
  * state and the parameters once; if the step is not applied a second, short
  * kernel restores the parameters from master_in (parameters always equal
  * round16(master)).  Otherwise two passes: reduce into grad_shard (required
- * then), then apply.  Both passes are register-staged (paths 1 and 2), with
- * 16-byte vectors where every slice address (+ grad_offset), state pointer
- * and grad_shard is 16-byte aligned.  ZERO_GB300_PATH=ws runs them as a
- * producer warp issuing bulk asynchronous (TMA) copies into shared-memory
- * stages for consumer warps (paths 5 and 6) when there are at most 8 slices
- * and the same addresses are aligned.  With
- * ZERO_GB300_PATH=stream the fused and apply passes run through stages with a
- * block-wide cycle per chunk under the same alignment rules (grad_shard
- * 16-byte aligned too).
- * Errors: ZERO_EINVAL, ZERO_EALIGN (16-bit pointers must be 2-byte aligned,
- * fp32 pointers 4-byte aligned), ZERO_EWORKSPACE, ZERO_ELIMIT, ZERO_ECUDA. */
+ * then), then apply.  Both run 16-byte vectors where every slice address
+ * (+ grad_offset), state pointer and grad_shard is 16-byte aligned, and
+ * element by element otherwise.
+ * Errors (all before any work is enqueued): ZERO_EINVAL, ZERO_EALIGN (16-bit
+ * pointers must be 2-byte aligned, fp32 pointers 4-byte aligned),
+ * ZERO_EWORKSPACE, ZERO_ELIMIT; ZERO_ECUDA if a launch fails. */
 int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype,
                     const zero_shard* shards, int n_shards,
                     void* flat_param, int param_dtype,
@@ -385,6 +372,9 @@ int zero3_gather_segments(const void* const* segment_ptrs, const int64_t* segmen
  * CTA); otherwise the register-staged gather runs on at most n_ctas blocks.
  * status: device int32 the caller zero-fills; a CTA whose bounded wait for a
  * copy runs out sets bit 0 and stops, and layer_out is then incomplete.
+ * Environment (read at each call; meant for tests): ZERO_GB300_SPIN_LIMIT=n
+ * sets the tries per bounded wait (default 4194304); 0 makes every first
+ * wait give up, which exercises the timeout path without hanging anything.
  * Errors (before any work): ZERO_EINVAL (NULL, negative sizes or n_ctas,
  * unknown dtype, status not 4-byte aligned), ZERO_EALIGN, ZERO_ELIMIT,
  * ZERO_ECUDA. */
@@ -450,15 +440,21 @@ int zero_shard_step_noalloc(const void* const* grad_slices, int n_slices, int gr
  * step        t of the next step (1-based)
  * loss_scale  S of the next step
  * applied, skipped, failed   steps applied, skipped on overflow, and ended
- *             with a nonzero status
+ *             with a nonzero status or an overflow at the loss-scale floor
+ * min_loss_scale   floor of S: an overflow halves S only while S / 2 stays at
+ *             or above it; <= 0 means 2^-126 (the smallest S whose
+ *             reciprocal, the fused pass's multiplier, is finite in fp32)
  * After each step: applied -> step += 1 and cur ^= 1; overflow -> loss_scale
- * halves (no hysteresis, as zero_shard_step's callers do); a nonzero status
- * (timeout, or step outside the scalar table) changes nothing but `failed`. */
+ * halves (no hysteresis, as zero_shard_step's callers do) and `skipped`
+ * counts it, or, when halving would go below the floor, S stays and `failed`
+ * counts it; a nonzero status (step outside the scalar table) changes nothing
+ * but `failed`. */
 typedef struct {
     int32_t cur, reserved;
     int64_t step;
     double loss_scale;
     int64_t applied, skipped, failed;
+    double min_loss_scale;
 } zero_chain;
 
 /* The two step-dependent AdamW scalars for steps t0 .. t0 + n - 1, computed

@@ -18,7 +18,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libzero_gb300.so")
 
-ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA, ZERO_ELIMIT, ZERO_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA, ZERO_ELIMIT = 0, -1, -2, -3, -4, -5
 ZERO_F16, ZERO_BF16 = 1, 2
 ZERO_PLAN_PADDED, ZERO_PLAN_UNPADDED = 0, 1
 ZERO_MAX_SLICES = ZERO_MAX_SHARDS = 64
@@ -50,7 +50,7 @@ class zero_stats(ctypes.Structure):
 class zero_chain(ctypes.Structure):
     _fields_ = [("cur", ctypes.c_int32), ("reserved", ctypes.c_int32), ("step", ctypes.c_int64),
                 ("loss_scale", ctypes.c_double), ("applied", ctypes.c_int64), ("skipped", ctypes.c_int64),
-                ("failed", ctypes.c_int64)]
+                ("failed", ctypes.c_int64), ("min_loss_scale", ctypes.c_double)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_ if not k.startswith("reserved")}
@@ -66,7 +66,7 @@ class zero_result(ctypes.Structure):
 
 
 assert ctypes.sizeof(zero_hyper) == 32 and ctypes.sizeof(zero_shard) == 80
-assert ctypes.sizeof(zero_stats) == 16 and ctypes.sizeof(zero_result) == 48
+assert ctypes.sizeof(zero_stats) == 16 and ctypes.sizeof(zero_result) == 48 and ctypes.sizeof(zero_chain) == 56
 
 _P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _SIGS = {
@@ -279,13 +279,14 @@ def zero_adam_scalar_table(hyper, t0, n):
     return out
 
 
-def chain(step=1, loss_scale=1.0, cur=0):
-    """A zero_chain to copy to the device (48 bytes) as the start of a chain."""
-    return zero_chain(cur, 0, step, loss_scale, 0, 0, 0)
+def chain(step=1, loss_scale=1.0, cur=0, min_loss_scale=0.0):
+    """A zero_chain to copy to the device (56 bytes) as the start of a chain;
+    min_loss_scale <= 0 leaves the library's floor of 2^-126."""
+    return zero_chain(cur, 0, step, loss_scale, 0, 0, 0, min_loss_scale)
 
 
 def read_chain(t) -> zero_chain:
-    """A zero_chain from a 48-byte tensor (device or host)."""
+    """A zero_chain from a 56-byte tensor (device or host)."""
     b = bytes(t.detach().cpu().view(-1).numpy().tobytes()) if hasattr(t, "detach") else bytes(t)
     return zero_chain.from_buffer_copy(b[:ctypes.sizeof(zero_chain)])
 

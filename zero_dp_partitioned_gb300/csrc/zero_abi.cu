@@ -8,10 +8,11 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <tuple>
 #include <utility>
 
 #include "zero_internal.h"
-#include "zero_stream.cuh"
+#include "zero_tma.cuh"
 
 namespace zdp {
 
@@ -26,29 +27,37 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int max_per_sm) {
+    // Occupancy and SM count are cached per (device, kernel, dynamic shared
+    // memory): a process may see GPUs with different SM counts.
     static std::mutex mu;
-    static std::map<std::pair<const void*, size_t>, int> per_sm[16];    // (kernel, dynamic smem) -> blocks
-    static int sms[16] = {0};
+    static std::map<std::tuple<int, const void*, size_t>, int> per_sm;   // -> resident blocks per SM
+    static std::map<int, int> sms;                                        // device -> SM count
     int dev = 0;
     cudaGetDevice(&dev);
-    dev &= 15;
-    int nb = 0;
+    int nb = 0, n_sm = 0;
     {
         std::lock_guard<std::mutex> g(mu);
-        if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        const auto key = std::make_pair(func, dynamic_smem);
-        auto it = per_sm[dev].find(key);
-        if (it == per_sm[dev].end()) {
+        auto si = sms.find(dev);
+        if (si == sms.end()) {
+            if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
+                n_sm = 1;
+            sms[dev] = n_sm;
+        } else {
+            n_sm = si->second;
+        }
+        const auto key = std::make_tuple(dev, func, dynamic_smem);
+        auto it = per_sm.find(key);
+        if (it == per_sm.end()) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, func, TILE_THREADS, dynamic_smem) != cudaSuccess ||
                 nb < 1)
                 nb = 1;
-            per_sm[dev][key] = nb;
+            per_sm[key] = nb;
         } else {
             nb = it->second;
         }
     }
     if (max_per_sm > 0 && nb > max_per_sm) nb = max_per_sm;
-    int64_t g = (int64_t)nb * (sms[dev] > 0 ? sms[dev] : 1);
+    int64_t g = (int64_t)nb * n_sm;
     if (g > n_tiles) g = n_tiles;
     if (g > MAX_BLOCKS) g = MAX_BLOCKS;
     if (g < 1) g = 1;
@@ -59,20 +68,8 @@ int grid_for(const void* func, int64_t n_tiles, int max_per_sm) {
     return grid_for_smem(func, n_tiles, 0, max_per_sm);
 }
 
-// Implementation choice and wait limit, from the environment (tests and measurements).
-// 0 default (the register-staged passes), 1 register only (the same), 2
-// staged with a block-wide cycle, 3 producer/consumer fused and apply
-// passes.  On GB300 the register passes measure fastest: the GPT-2 fused step
-// 9.51 ms against 9.63 ms producer/consumer, the Llama-3-8B apply pass 8.56
-// ms against 9.52 ms.
-static int path_choice() {
-    const char* e = std::getenv("ZERO_GB300_PATH");
-    if (e && !std::strcmp(e, "register")) return 1;
-    if (e && !std::strcmp(e, "stream")) return 2;
-    if (e && !std::strcmp(e, "ws")) return 3;
-    return 0;
-}
-
+// Tries per bounded wait of the TMA gather, from the environment (tests force
+// a limit of 0 to exercise the timeout path without hanging anything).
 static unsigned spin_limit() {
     const char* e = std::getenv("ZERO_GB300_SPIN_LIMIT");
     if (!e) return SPIN_LIMIT;
@@ -218,67 +215,6 @@ static bool vec8_ok(const StepArgs& a, int need) {
     return true;
 }
 
-// The staged passes need 16-byte aligned bulk-copy addresses: every slice at
-// its shard's gradient offset (fused), the grad shard (apply), every state
-// pointer; and at most MAX_STREAM_SLICES slices.
-static bool stream_ok(const StepArgs& a, bool fused) {
-    if (fused && a.n_slices > MAX_STREAM_SLICES) return false;
-    return vec8_ok(a, fused ? 1 : 3);
-}
-
-static bool param_bulk_ok(const StepArgs& a) {
-    if (!aligned(a.flat_param, 16)) return false;
-    for (int i = 0; i < a.n_shards; ++i)
-        if (a.shards[i].numel > 0 && (a.shards[i].param_off & 7)) return false;
-    return true;
-}
-
-static int run_stream(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s) {
-    StreamArgs sa;
-    std::memset(&sa, 0, sizeof sa);
-    number_tiles(a, CHUNK / TILE_THREADS);     // chunks of CHUNK elements
-    sa.a = a;
-    sa.stages = stream_stages(fused ? a.n_slices : 1);
-    sa.spin_limit = spin_limit();
-    sa.drain_limit = SPIN_LIMIT;
-    sa.param_bulk = param_bulk_ok(a) ? 1 : 0;
-    return launch_stream(sa, gdt, pdt, fused, s);
-}
-
-// Chunks of `chunk` elements numbered shard after shard, after each shard's
-// head (the elements before its dominant stream reaches a 128-byte
-// boundary); a shard that is all head still gets one chunk, whose block does
-// the head.
-static void number_chunks(StepArgs& a, int64_t chunk, int kind) {
-    int64_t t = 0;
-    for (int i = 0; i < a.n_shards; ++i) {
-        ShardDev& d = a.shards[i];
-        d.head = shard_head(a, d, kind);
-        if (d.head > d.numel) d.head = d.numel;
-        d.tile_begin = t;
-        const int64_t rest = d.numel - d.head;
-        t += d.numel == 0 ? 0 : (rest > 0 ? (rest + chunk - 1) / chunk : 1);
-    }
-    a.n_tiles = t;
-}
-
-// The producer/consumer passes need what the staged ones need (16-byte
-// aligned bulk-copy addresses, at most 8 slices) and two stages.
-static bool ws_ok(const StepArgs& a, bool fused) {
-    return stream_ok(a, fused) && ws_stages(fused ? a.n_slices : 1) >= 2;
-}
-
-static int run_ws(StepArgs& a, int gdt, int pdt, bool fused, cudaStream_t s) {
-    StreamArgs sa;
-    std::memset(&sa, 0, sizeof sa);
-    number_chunks(a, ws_chunk(), fused ? HEAD_GRADS : HEAD_STATE);
-    sa.a = a;
-    sa.stages = ws_stages(fused ? a.n_slices : 1);
-    sa.spin_limit = spin_limit();
-    sa.drain_limit = SPIN_LIMIT;
-    return launch_ws(sa, gdt, pdt, fused, s);
-}
-
 static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
     if (!ws) return fail(ZERO_EWORKSPACE, "workspace is NULL");
     if (ws_bytes < WS_BYTES) return fail(ZERO_EWORKSPACE, "workspace smaller than zero_workspace_bytes()");
@@ -301,6 +237,73 @@ static bool any_elements(const StepArgs& a) {
     for (int i = 0; i < a.n_shards; ++i)
         if (a.shards[i].numel > 0) return true;
     return false;
+}
+
+// Every argument check of zero_shard_step, then the packed kernel arguments
+// and the path: nothing is enqueued, so a failing call leaves the device and
+// the workspace untouched.
+int plan_step(StepPlan& sp, const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
+              int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper, float loss_scale,
+              double extra_sumsq, int extra_overflow, void* workspace, size_t workspace_bytes, zero_result* result) {
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    int rc;
+    if ((rc = check_hyper(hyper, loss_scale)) != ZERO_OK) return rc;
+    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
+    StepArgs& a = sp.a;
+    std::memset(&a, 0, sizeof a);
+    if ((rc = pack_slices(a, grad_slices, n_slices)) != ZERO_OK) return rc;
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+
+    // One fused pass needs a second state set to write (the skip decision is
+    // only known at its end) and no clipping (the norm is needed before the
+    // first update); otherwise reduce, then apply.
+    bool fused = hyper->max_grad_norm <= 0.0f;
+    for (int i = 0; fused && i < n_shards && shards; ++i)
+        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
+                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
+            fused = false;
+    if ((rc = pack_shards(a, shards, n_shards, fused ? 1 : 2)) != ZERO_OK) return rc;
+    if (!fused && (rc = pack_shards(a, shards, n_shards, 3)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = flat_param;
+    a.sc = adam_scalars(*hyper);
+    a.loss_scale = (double)loss_scale;
+    a.max_norm = (double)hyper->max_grad_norm;
+    a.extra_sumsq = extra_sumsq;
+    a.extra_overflow = extra_overflow ? 1 : 0;
+    a.result = result;
+    if (fused) {
+        a.k = (float)(1.0 / (double)loss_scale);
+    } else {
+        a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
+        a.accumulate = 0;
+    }
+    sp.fused = fused;
+    sp.gdt = grad_dtype;
+    sp.pdt = param_dtype;
+    return ZERO_OK;
+}
+
+// The kernels of a planned step: the fused pass and the parameter restore
+// check, or the reduce and apply passes.
+int run_step(StepPlan& sp, cudaStream_t s) {
+    StepArgs& a = sp.a;
+    int rc;
+    if (sp.fused) {
+        const int vec = vec8_ok(a, 1) ? 8 : 1;
+        number_tiles(a, vec, HEAD_GRADS);
+        const int grid = grid_for(fused_kernel(sp.gdt, sp.pdt, vec, fused_ns(a.n_slices)), a.n_tiles,
+                                  a.n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+        if ((rc = launch_fused(a, sp.gdt, sp.pdt, vec, grid, s)) != ZERO_OK) return rc;
+        return launch_recover(a, sp.pdt, s);
+    }
+    int vec = vec8_ok(a, 2) ? 8 : 1;
+    number_tiles(a, vec, HEAD_GRADS);
+    if ((rc = launch_reduce(a, sp.gdt, vec, s)) != ZERO_OK) return rc;
+    vec = vec8_ok(a, 3) ? 8 : 1;
+    number_tiles(a, vec, HEAD_STATE);
+    return launch_apply(a, sp.gdt, sp.pdt, vec, s);
 }
 
 }  // namespace zdp
@@ -414,60 +417,11 @@ int zero_shard_step(const void* const* grad_slices, int n_slices, int grad_dtype
                     int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper, float loss_scale,
                     double extra_sumsq, int extra_overflow, void* workspace, size_t workspace_bytes,
                     zero_result* result, void* stream) {
-    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
-    int rc;
-    if ((rc = check_hyper(hyper, loss_scale)) != ZERO_OK) return rc;
-    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
-    StepArgs a;
-    std::memset(&a, 0, sizeof a);
-    if ((rc = pack_slices(a, grad_slices, n_slices)) != ZERO_OK) return rc;
-    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
-
-    bool fused = hyper->max_grad_norm <= 0.0f;
-    for (int i = 0; fused && i < n_shards && shards; ++i)
-        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
-                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
-            fused = false;
-    if ((rc = pack_shards(a, shards, n_shards, fused ? 1 : 2)) != ZERO_OK) return rc;
-    if (!fused && (rc = pack_shards(a, shards, n_shards, 3)) != ZERO_OK) return rc;
-    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
-        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
-    a.flat_param = flat_param;
-    a.sc = adam_scalars(*hyper);
-    a.loss_scale = (double)loss_scale;
-    a.max_norm = (double)hyper->max_grad_norm;
-    a.extra_sumsq = extra_sumsq;
-    a.extra_overflow = extra_overflow ? 1 : 0;
-    a.result = result;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    const int choice = path_choice();
-    if (fused) {
-        a.k = (float)(1.0 / (double)loss_scale);
-        if (choice == 2 && stream_ok(a, true)) {
-            if ((rc = run_stream(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
-        } else if (choice == 3 && ws_ok(a, true)) {
-            if ((rc = run_ws(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
-        } else {
-            const int vec = vec8_ok(a, 1) ? 8 : 1;
-            number_tiles(a, vec, HEAD_GRADS);
-            const int grid =
-                grid_for(fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
-                         n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
-            if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
-        }
-        return launch_recover(a, param_dtype, s);
-    }
-    a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
-    a.accumulate = 0;
-    int vec = vec8_ok(a, 2) ? 8 : 1;
-    number_tiles(a, vec, HEAD_GRADS);
-    if ((rc = launch_reduce(a, grad_dtype, vec, s)) != ZERO_OK) return rc;
-    if (choice == 2 && stream_ok(a, false)) return run_stream(a, grad_dtype, param_dtype, false, s);
-    if (choice == 3 && ws_ok(a, false)) return run_ws(a, grad_dtype, param_dtype, false, s);
-    vec = vec8_ok(a, 3) ? 8 : 1;
-    number_tiles(a, vec, HEAD_STATE);
-    return launch_apply(a, grad_dtype, param_dtype, vec, s);
+    StepPlan sp;
+    const int rc = plan_step(sp, grad_slices, n_slices, grad_dtype, shards, n_shards, flat_param, param_dtype, hyper,
+                             loss_scale, extra_sumsq, extra_overflow, workspace, workspace_bytes, result);
+    if (rc != ZERO_OK) return rc;
+    return run_step(sp, static_cast<cudaStream_t>(stream));
 }
 
 int zero_shard_init(const zero_shard* shards, int n_shards, const void* flat_param, int param_dtype, void* stream) {
@@ -535,15 +489,11 @@ int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int gr
 
     if (fused) {
         // the fused pass derives k = fp32(1/S) from chain->loss_scale on the device
-        if (path_choice() == 3 && ws_ok(a, true)) {
-            if ((rc = run_ws(a, grad_dtype, param_dtype, true, s)) != ZERO_OK) return rc;
-        } else {
-            const int vec = vec8_ok(a, 1) ? 8 : 1;
-            number_tiles(a, vec, HEAD_GRADS);
-            const int grid = grid_for(fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
-                                      n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
-            if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
-        }
+        const int vec = vec8_ok(a, 1) ? 8 : 1;
+        number_tiles(a, vec, HEAD_GRADS);
+        const int grid = grid_for(fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
+                                  n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+        if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
         if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
     } else {
         a.stats = reinterpret_cast<zero_stats*>(static_cast<char*>(workspace) + WS_STATS);
@@ -599,11 +549,6 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
     a.stats = const_cast<zero_stats*>(stats);
     a.result = result;
     if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
-    const int choice = path_choice();
-    if (choice == 2 && stream_ok(a, false))
-        return run_stream(a, grad_dtype, param_dtype, false, static_cast<cudaStream_t>(stream));
-    if (choice == 3 && ws_ok(a, false))
-        return run_ws(a, grad_dtype, param_dtype, false, static_cast<cudaStream_t>(stream));
     const int vec = vec8_ok(a, 3) ? 8 : 1;
     number_tiles(a, vec, HEAD_STATE);
     return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));

@@ -20,9 +20,8 @@ const void* fused_kernel(int gdt, int pdt, int vec, int ns) {
     return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_F16, ZERO_BF16>(vec, ns) : fused_ptr_v<ZERO_F16, ZERO_F16>(vec, ns);
 }
 
-// Chained steps take the generic slice loop (the producer/consumer pass
-// covers the common case; this one runs for more than 8 slices or misaligned
-// data).
+// Chained steps: the same passes, instantiated with the device-side
+// bookkeeping (t, S and the state set read from the chain).
 template <int G, int P, int V>
 static const void* fused_chain_ptr_v(int ns) {
     return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW, true> : (const void*)k_step_fused<G, P, V, 0, true>;
@@ -87,7 +86,10 @@ int launch_init(const StepArgs& a, int pdt, cudaStream_t s) {
 
 // ---------------------------------------------------------------- chained steps: the bookkeeping
 // After a chained step's kernels: applied -> next t, the other state set;
-// overflow -> half the loss scale; another failure -> counted only.
+// overflow -> half the loss scale, unless that would take it below the
+// floor (then S stays and the step counts as failed: a chain stuck at its
+// floor must not slide towards an S whose reciprocal overflows fp32);
+// another failure -> counted only.
 __global__ void k_chain_update(zero_chain* chain, const zero_result* result) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     const zero_result r = *result;
@@ -96,8 +98,14 @@ __global__ void k_chain_update(zero_chain* chain, const zero_result* result) {
         chain->cur ^= 1;
         chain->applied += 1;
     } else if (r.overflow && r.status == 0) {
-        chain->loss_scale *= 0.5;
-        chain->skipped += 1;
+        const double floor = chain->min_loss_scale > 0.0 ? chain->min_loss_scale : 0x1p-126;
+        const double half = chain->loss_scale * 0.5;
+        if (half >= floor) {
+            chain->loss_scale = half;
+            chain->skipped += 1;
+        } else {
+            chain->failed += 1;
+        }
     } else {
         chain->failed += 1;
     }

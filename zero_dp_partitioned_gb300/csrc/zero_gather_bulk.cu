@@ -30,7 +30,7 @@
 #include <cuda_runtime.h>
 
 #include "zero_internal.h"
-#include "zero_stream.cuh"
+#include "zero_tma.cuh"
 
 namespace zdp {
 

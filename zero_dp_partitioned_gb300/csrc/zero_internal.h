@@ -67,20 +67,18 @@ struct BulkGatherArgs {
 size_t gather_bulk_smem(int chunk, int stages);
 int launch_gather_bulk(const BulkGatherArgs& a, int grid, cudaStream_t s);
 
-// The shared-memory-staged passes with a block-wide cycle per chunk
-// (zero_stream.cu): selected only by ZERO_GB300_PATH=stream; on GB300 they
-// are slower than the register-staged passes (14.1 ms for the fused GPT-2
-// step, against 10.8 ms for the register pass of the time and 9.5 ms now).
-struct StreamArgs;
-int stream_stages(int n_grad_arrays);
-int launch_stream(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
-
-// The fused and apply passes with a producer warp and consumer warps
-// (zero_ws.cu): chunks of ws_chunk() elements, ws_stages(ng) shared-memory
-// stages for ng 16-bit arrays (the slices, or the reduced gradient).
-int ws_chunk();
-int ws_stages(int ng);
-int launch_ws(const StreamArgs& sa, int gdt, int pdt, bool fused, cudaStream_t s);
+// zero_shard_step in two phases: plan_step makes every argument check and
+// packs the kernel arguments without touching the device (an argument error
+// therefore enqueues nothing); run_step launches the planned kernels.
+struct StepPlan {
+    StepArgs a;
+    bool fused;          // one fused pass (+ parameter restore check), else reduce + apply
+    int gdt, pdt;
+};
+int plan_step(StepPlan& sp, const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
+              int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper, float loss_scale,
+              double extra_sumsq, int extra_overflow, void* workspace, size_t workspace_bytes, zero_result* result);
+int run_step(StepPlan& sp, cudaStream_t s);
 
 // Kernel addresses, for the occupancy query.
 const void* fused_kernel(int gdt, int pdt, int vec, int ns);
