@@ -29,6 +29,8 @@ standard deviation, times the loss scale where one is given) and rounded to the
 """
 from __future__ import annotations
 
+import json
+import os
 from dataclasses import dataclass, field
 
 import torch
@@ -179,14 +181,24 @@ def workload(name: str) -> Workload:
     raise KeyError(name)
 
 
+OTHER_RANKS_SUMSQ = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tests", "golden",
+                                 "other_ranks_sumsq.json")
+
+
 def other_ranks_sumsq(wl: Workload) -> float:
     """The rank-local views need the other ranks' share of the global sum of
     squares (the operands of the norm's scalar all-reduce that this rank does
-    not compute).  It is an input of the step: a synthetic constant per
-    workload, of the size the other ranks' gradients of that workload would
-    give (Llama-3-8B rank 1: three shards of 2.0e9 elements of averaged
-    N(0, 5e-4^2) gradients)."""
-    return {"llama3-8b-nd4-r1": 376.42}.get(wl.name, 0.0)
+    not compute).  It is an input of the step, generated once from data:
+    tests/golden/make_other_ranks_sumsq.py draws every other rank's staged
+    slices with the workload's recipe from their own seeded generators and has
+    the oracle reduce them and sum the squares exactly; the value is stored in
+    tests/golden/other_ranks_sumsq.json with its recipe.  Workloads without a
+    stored share (every rank simulated, or no clipping) take 0."""
+    try:
+        with open(OTHER_RANKS_SUMSQ) as f:
+            return float(json.load(f)[wl.name]["value"])
+    except (OSError, KeyError):
+        return 0.0
 
 
 # ------------------------------------------------------------------ device-side input sets
