@@ -150,15 +150,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ kernel timing
 class KernelTimer:
-    """CUDA events around each library call on the launching (current) stream,
-    grouped by kernel kind."""
+    """CUDA events on the launching (current) stream around library calls,
+    grouped by kernel kind.  One pair of events may enclose several
+    back-to-back launches of the same kernel (`launches`): consecutive
+    launches then run with no event between them, and the kind's time per
+    launch is the enclosed time divided by the launch count."""
 
     def __init__(self, torch):
         self.torch = torch
-        self.events = []          # (kind, start, end)
+        self.events = []          # (kind, launches, start, end)
         self.on = False
 
-    def __call__(self, kind):
+    def __call__(self, kind, launches=1):
         timer = self
 
         class _Ctx:
@@ -171,17 +174,18 @@ class KernelTimer:
                 if timer.on:
                     b = timer.torch.cuda.Event(enable_timing=True)
                     b.record()
-                    timer.events.append((kind, self.a, b))
+                    timer.events.append((kind, launches, self.a, b))
         return _Ctx()
 
     def per_kind(self, steps):
         out, each = {}, {}
-        for kind, a, b in self.events:
-            d = out.setdefault(kind, {"ms_total": 0.0, "launches": 0})
+        for kind, n, a, b in self.events:
+            d = out.setdefault(kind, {"ms_total": 0.0, "launches": 0, "event_pairs": 0})
             ms = a.elapsed_time(b)
             d["ms_total"] += ms
-            d["launches"] += 1
-            each.setdefault(kind, []).append(ms)
+            d["launches"] += n
+            d["event_pairs"] += 1
+            each.setdefault(kind, []).append(ms / n)
         for kind, d in out.items():
             d["ms_per_launch"] = d["ms_total"] / d["launches"]
             d["ms_median"] = statistics.median(each[kind])
@@ -193,10 +197,7 @@ def _hyper(Z, h, t, clip=0.0):
     return Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], clip, t)
 
 
-PATH_NAMES = {1: "k_step_fused (register-staged)", 2: "k_apply (register-staged)",
-              3: "k_stream<fused> (TMA bulk-copy staged)", 4: "k_stream<apply> (TMA bulk-copy staged)",
-              5: "k_ws<fused> (producer warp, TMA stages, consumer warps)",
-              6: "k_ws<apply> (producer warp, TMA stages, consumer warps)"}
+PATH_NAMES = {1: "k_step_fused (fused single pass)", 2: "k_apply (apply pass after k_reduce)"}
 
 
 def _finish_step(Z, torch, res, res_h, st):
@@ -213,6 +214,30 @@ def _finish_step(Z, torch, res, res_h, st):
 
 
 E2E_SOURCE = {"mode": None}
+
+
+def _device_chain(Z, torch, dev, wl, n_table=1 << 16):
+    """A device zero_chain starting at t = 1 with the workload's loss scale, and
+    the AdamW scalar table of steps 1 .. n_table: the chained calls read t, S
+    and the current state set from it, so steps follow one another with no
+    host round trip."""
+    hy = _hyper(Z, wl.hyper, 1, wl.max_grad_norm)
+    table = torch.from_numpy(Z.zero_adam_scalar_table(hy, 1, n_table)).to(dev)
+    chain = torch.frombuffer(bytearray(bytes(Z.chain(step=1, loss_scale=wl.loss_scale))), dtype=torch.uint8).to(dev)
+    return hy, table, n_table, chain
+
+
+def _check_chain(Z, chain):
+    """After the timed steps: no chained step may have failed."""
+    def check(steps):
+        c = Z.read_chain(chain)
+        if c.failed:
+            raise RuntimeError(f"{c.failed} chained steps failed (status != 0)")
+        return {"chain_after_timing": {"step": c.step, "applied": c.applied, "skipped": c.skipped}}
+    return check
+
+
+
 
 
 def _pin_copies(torch, bufs, e2e):
@@ -243,21 +268,28 @@ def _pin_copies(torch, bufs, e2e):
 
 
 # ------------------------------------------------------------------ workloads (our path)
+def _small(layers, vocab):
+    """Name suffix of a reduced case (fewer layers and/or a smaller vocabulary)
+    of a workload's group: the same kernels on a few GB, for profiler captures."""
+    return (f"-{layers}layers" if layers else "") + (f"-v{vocab}" if vocab else "")
+
+
 def gpt2_desc(name, layers=48):
     """The GPT-2 workload's description, shared by both arms' `config`."""
     return (f"{name}: GPT-2-shaped group ({layers} layers, d=1600, vocab 50257, ctx 1024), "
             "N_d=8, all 8 ranks simulated on one GPU")
 
 
-def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
+def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """GPT-2 1.5B-shaped group, N_d = 8, all ranks on this GPU, bf16, ping-pong state (fused single pass)."""
     wl = W.workload("gpt2-1.5b-nd8")
+    small = layers or vocab
     layers = layers or 48
-    specs = wl.specs if layers == 48 else W.gpt2_group(L=layers)
+    specs = W.gpt2_group(L=layers, V=vocab or 50257) if small else wl.specs
     nd = wl.nd
     plan = Z.zero_plan(W.numels(specs), nd)
     P = plan["padded_total"]
-    name = "gpt2-1.5b-nd8" if layers == 48 else f"gpt2-{layers}layers-nd8"
+    name = f"gpt2{_small(layers, vocab)}-nd8" if small else "gpt2-1.5b-nd8"
     log(f"[bench] {name}: Psi={P} N_d={nd}; generating inputs")
     flat = W.flat_params(specs, P, torch.bfloat16, wl.param_seed, dev)
     grads = W.GradStream([1 + r for r in range(nd)], dev).draw_flat(
@@ -293,13 +325,23 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                 raise RuntimeError(f"{c.failed} chained steps failed (status != 0)")
             st.update(cur=c.cur, t=c.step, S=c.loss_scale, chained=False)
     # End to end, the next step's gradients cross the host link on a copy
-    # stream into a second device set while this step computes.
-    host = dict(sets=[grads], copy=None, copied=None, consumed=None, i=0, pending=None)
+    # stream into a second device set while this step computes, and the
+    # step's product -- the updated 16-bit flat parameters, the all-gather
+    # destination -- goes back to pinned host memory on a third stream, beside
+    # the next upload (the link carries both directions at once).
+    host = dict(sets=[grads], copy=None, copied=None, consumed=None, i=0, pending=None, params=None)
     if pinned is not None:
         host["sets"].append([torch.empty_like(g) for g in grads])
         host["copy"] = torch.cuda.Stream(device=dev)
         host["copied"] = [torch.cuda.Event(), torch.cuda.Event()]
         host["consumed"] = [torch.cuda.Event(), torch.cuda.Event()]
+        if mem_available_bytes() > flat.numel() * flat.element_size() + (16 << 30):
+            host["params"] = torch.empty(flat.shape, dtype=flat.dtype, pin_memory=True)
+            host["fetch"] = torch.cuda.Stream(device=dev)
+            host["stepped"] = torch.cuda.Event()
+            host["fetched"] = torch.cuda.Event()
+        else:
+            log("[bench] not enough host memory for the parameter download of the end-to-end run")
 
     def upload(b):
         """This step's-to-be gradients into device set b, on the copy stream,
@@ -326,33 +368,89 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
             if host["pending"] != b:
                 upload(b)
             main.wait_event(host["copied"][b])
+            if host["params"] is not None:
+                main.wait_event(host["fetched"])    # the last step's parameters have left before they are rewritten
         with timer("fused pass+k_recover"):
             Z.zero_shard_step(host["sets"][b], Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16,
                               _hyper(Z, wl.hyper, st["t"]), st["S"], 0.0, 0, ws, ws.numel(), res)
         if from_host:
             host["consumed"][b].record(main)
+            if host["params"] is not None:
+                host["stepped"].record(main)
+                host["fetch"].wait_event(host["stepped"])
+                with torch.cuda.stream(host["fetch"]):
+                    host["params"].copy_(flat, non_blocking=True)
+                host["fetched"].record(host["fetch"])
             host["i"] += 1
             upload(1 - b)              # the next step's gradients, under this step's compute
         _finish_step(Z, torch, res, res_h, st)
 
     def e2e_drain():
-        """The copy in flight for the step after the last belongs to the timed
-        region too: one copy per step."""
+        """The upload in flight for the step after the last belongs to the
+        timed region too (one upload per step), and so does the last step's
+        parameter download."""
         if host["pending"] is not None:
             torch.cuda.current_stream().wait_event(host["copied"][host["pending"]])
+        if host["params"] is not None:
+            torch.cuda.current_stream().wait_event(host["fetched"])
 
     def path_of_last_step():
         return Z.read_result(res).path
+
+    def e2e_parts():
+        """The host link alone, timed like the end-to-end steps: one step's
+        gradient upload, one parameter download, and both at once on their two
+        streams (what the end-to-end steps overlap)."""
+        out = {}
+        if host["params"] is None:
+            return out
+        main = torch.cuda.current_stream()
+
+        def up():
+            with torch.cuda.stream(host["copy"]):
+                for g, hp in zip(host["sets"][0], pinned):
+                    g.copy_(hp, non_blocking=True)
+
+        def down():
+            with torch.cuda.stream(host["fetch"]):
+                host["params"].copy_(flat, non_blocking=True)
+
+        times = {"upload_ms": [], "download_ms": [], "both_ms": []}
+        for _ in range(3):                       # interleaved, so that each leg sees the link's moods
+            for key, fns in (("upload_ms", (up,)), ("download_ms", (down,)), ("both_ms", (up, down))):
+                torch.cuda.synchronize()
+                a = torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                for st_ in (host["copy"], host["fetch"]):
+                    st_.wait_event(a)
+                for f in fns:
+                    f()
+                for st_ in (host["copy"], host["fetch"]):
+                    main.wait_stream(st_)
+                b = torch.cuda.Event(enable_timing=True)
+                b.record(main)
+                torch.cuda.synchronize()
+                times[key].append(a.elapsed_time(b))
+        for key, x in times.items():
+            out[key] = statistics.median(x)
+            out[key + "_all"] = x
+        out["upload_gbs"] = sum(g.numel() * 2 for g in grads) / (out["upload_ms"] / 1e3) / 1e9
+        out["download_gbs"] = flat.numel() * 2 / (out["download_ms"] / 1e3) / 1e9
+        return out
 
     bytes_step = (2 * nd + 26) * P
     return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=3,
                 path_of_last_step=path_of_last_step,
                 kernel_bytes={"fused pass+k_recover": bytes_step},
                 dominant_label=None,
-                h2d=sum(g.numel() * 2 for g in grads) if pinned else None, d2h=48, e2e_ok=pinned is not None,
-                e2e_drain=e2e_drain,
+                h2d=sum(g.numel() * 2 for g in grads) if pinned else None,
+                d2h=(flat.numel() * flat.element_size() if host["params"] is not None else 0) + 48,
+                e2e_ok=pinned is not None,
+                e2e_drain=e2e_drain, e2e_parts=e2e_parts,
                 e2e_note="each step's gradients are copied from pinned host memory on a copy stream into one of two "
-                         "device sets while the previous step computes; the timed region holds one copy per step",
+                         "device sets while the previous step computes, and each step's updated 16-bit flat "
+                         "parameters are copied to pinned host memory on a third stream; the timed region holds one "
+                         "upload, one parameter download and one result read per step",
                 config={"workload": gpt2_desc(name, layers),
                         "psi": P, "n_d": nd, "shard_elements": plan["rank_numels"][0], "grad_dtype": "bf16",
                         "param_dtype": "bf16", "state": "f32 master/m/v, ping-pong", "path": "fused single pass",
@@ -363,7 +461,7 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None):
                 formula_bytes=bytes_step, sample_for_cpu=lambda n: cpu_sample_gpt2(W, n))
 
 
-def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None):
+def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """The small fp16 group (Psi = 70,282, N_d = 3, all ranks, S = 1024): a
     launch-bound step.  Its 2.3 MB of inputs fit in L2, so every step first
     writes a 256 MB buffer (an L2 flush); the flush is inside the step time,
@@ -446,7 +544,7 @@ def tiny_nd3(Z, W, torch, dev, e2e, timer, layers=None):
                               "time); the kernels' own time is in kernels.*.ms_per_launch"})
 
 
-def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None):
+def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """The GPT-2 1.5B group with stage 1's full all-reduce: the reduce pass
     writes the whole averaged gradient (the all-reduce result every rank
     holds), then each rank's shard is updated from its slice of it."""
@@ -491,13 +589,14 @@ def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None):
                 sample_for_cpu=None)
 
 
-def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
+def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """Llama-3-8B-shaped group, N_d = 4, rank 1's shard with 4 staged slices,
     clip 1.0: two passes (reduce + statistics, then apply), state in place."""
     wl = W.workload("llama3-8b-nd4-r1")
-    if layers:
-        wl.specs = W.llama_group(L=layers)
-        wl.name = f"llama3-{layers}layers-nd4-r1"
+    extra = W.other_ranks_sumsq(wl)
+    if layers or vocab:
+        wl.specs = W.llama_group(L=layers or 32, V=vocab or 128256)
+        wl.name = f"llama3{_small(layers, vocab)}-nd4-r1"
     nd, me = wl.nd, 1
     plan = Z.zero_plan(W.numels(wl.specs), nd)
     P = plan["padded_total"]
@@ -515,38 +614,49 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None):
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
-    extra = W.other_ranks_sumsq(wl)
     pinned = _pin_copies(torch, slices, e2e)
+    hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
 
     def step(from_host=False):
+        # chained: t, S and the bookkeeping on the device (the apply pass, then
+        # a one-thread update of the chain); end to end, the result is read
+        # back every step
         if from_host:
             for g, hp in zip(slices, pinned):
                 g.copy_(hp, non_blocking=True)
         with timer("k_reduce"):
             Z.zero_shard_reduce(slices, Z.ZERO_BF16, sh, 0, stats, ws, ws.numel())
         with timer("k_apply"):
-            Z.zero_shard_apply(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"], wl.max_grad_norm),
-                               st["S"], stats, extra, 0, ws, ws.numel(), res)
-        _finish_step(Z, torch, res, res_h, st)
+            Z.zero_shard_apply_chained(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, hy, table, 1, n_table, chain, stats,
+                                       extra, 0, ws, ws.numel(), res)
+        if from_host:
+            res_h.copy_(res)
 
-    return dict(name=wl.name, step=step, state=st, elements=n, nd=nd, launches_per_step=2,
+    def path_of_last_step():
+        return Z.read_result(res).path
+
+    return dict(name=wl.name, step=step, state=st, elements=n, nd=nd, launches_per_step=3,
+                path_of_last_step=path_of_last_step, extra=_check_chain(Z, chain),
                 kernel_bytes={"k_reduce": (2 * nd + 2) * n, "k_apply": 28 * n},
                 dominant_label=None, h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 formula_bytes=(2 * nd + 26) * n,
                 config={"workload": f"{wl.name}: Llama-3-8B-shaped group, N_d=4, rank 1's shard, 4 staged "
                                     "bf16 slices, global-norm clip 1.0", "psi": P, "n_d": nd, "shard_elements": n,
+                        "other_ranks_sumsq": extra,
                         "path": "two passes (reduce+stats, apply), state in place",
+                        "steps": "zero_shard_reduce + zero_shard_apply_chained: t, S and the state set in use stay "
+                                 "on the device (3 launches a step: reduce, apply, the bookkeeping)",
                         "bytes_per_step_actual": (2 * nd + 30) * n, "bytes_per_step_formula": (2 * nd + 26) * n,
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
 
 
-def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None):
+def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """The 7.5B GPT-like group, N_d = 64, rank 63's shard, fp16, S = 65536: fused single pass."""
     wl = W.workload("gpt-7.5b-nd64-r63")
-    if layers:
-        wl.specs = W.gpt2_group(layers, 3456, 50257, 1024)
-        wl.name = f"gpt-{layers}layers-nd64-r63"
+    if layers or vocab:
+        wl.specs = W.gpt2_group(layers or 52, 3456, vocab or 50257, 1024)
+        wl.name = f"gpt{_small(layers, vocab)}-nd64-r63"
     nd, me = wl.nd, 63
     plan = Z.zero_plan(W.numels(wl.specs), nd)
     P = plan["padded_total"]
@@ -564,23 +674,32 @@ def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None):
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
     pinned = _pin_copies(torch, slices, e2e)
+    hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
 
     def step(from_host=False):
+        # chained: t, S and the state set in use on the device
         if from_host:
             for g, hp in zip(slices, pinned):
                 g.copy_(hp, non_blocking=True)
         with timer("fused pass+k_recover"):
-            Z.zero_shard_step(slices, Z.ZERO_F16, variants[st["cur"]], flat, Z.ZERO_F16, _hyper(Z, wl.hyper, st["t"]),
-                              st["S"], 0.0, 0, ws, ws.numel(), res)
-        _finish_step(Z, torch, res, res_h, st)
+            Z.zero_shard_step_chained(slices, Z.ZERO_F16, variants[0], flat, Z.ZERO_F16, hy, table, 1, n_table, chain,
+                                      0.0, 0, ws, ws.numel(), res)
+        if from_host:
+            res_h.copy_(res)
 
-    return dict(name=wl.name, step=step, state=st, elements=n, nd=nd, launches_per_step=2,
+    def path_of_last_step():
+        return Z.read_result(res).path
+
+    return dict(name=wl.name, step=step, state=st, elements=n, nd=nd, launches_per_step=3,
+                path_of_last_step=path_of_last_step, extra=_check_chain(Z, chain),
                 kernel_bytes={"fused pass+k_recover": (2 * nd + 26) * n}, dominant_label=None,
                 h2d=nd * n * 2 if pinned else None, d2h=48, e2e_ok=pinned is not None,
                 formula_bytes=(2 * nd + 26) * n,
                 config={"workload": f"{wl.name}: GPT-like 7.5B-shaped group, N_d=64, rank 63's shard "
                                     "(flat offset = 6 mod 8), fp16, loss scale 65536", "psi": P, "n_d": nd,
                         "shard_elements": n, "path": "fused single pass, ping-pong state",
+                        "steps": "zero_shard_step_chained: t, S and the state set in use stay on the device "
+                                 "(3 launches a step: the pass, the parameter restore check, the bookkeeping)",
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
 
@@ -594,14 +713,14 @@ def _gather_status_check(gstatus):
     return check
 
 
-def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
+def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """ZeRO-3 per-layer path, Llama-3-8B group as 34 units, N_d = 4, rank 1:
     per step 34 forward gathers, 34 backward gathers (reverse order), 34 bucket
     reduces onto rank 1's parts, one shard update."""
     wl = W.workload("zero3-llama3-8b")
-    if layers:
-        wl.specs = W.llama_group(L=layers)
-        wl.name = f"zero3-llama3-{layers}layers"
+    if layers or vocab:
+        wl.specs = W.llama_group(L=layers or 32, V=vocab or 128256)
+        wl.name = f"zero3-llama3{_small(layers, vocab)}"
     nd, me = wl.nd, 1
     units = W.llama_units(wl.specs, L=layers or 32)
     parts = [u // nd for u in units]
@@ -629,36 +748,51 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None):
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
+    hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
     part_ptrs = [[rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)] for u in range(len(units))]
 
     gstatus = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    order = list(range(len(units))) + list(reversed(range(len(units))))
+
     def step(from_host=False):
-        for u in list(range(len(units))) + list(reversed(range(len(units)))):
-            with timer("k_gather_bulk"):
+        # one event pair per group of back-to-back launches of a kernel: the
+        # 68 gathers, the 34 reduces, the apply
+        with timer("k_gather_bulk", len(order)):
+            for u in order:
                 Z.zero3_gather_bulk(part_ptrs[u], [parts[u]] * nd, Z.ZERO_BF16, layer, 0, gstatus)
-        for k, (u, row) in enumerate(buckets):
-            with timer("k_reduce"):
+        with timer("k_reduce", len(buckets)):
+            for k, (u, row) in enumerate(buckets):
                 Z.zero3_reduce_bucket(row, me, units[u], Z.ZERO_BF16, gshard[uoff[u]:uoff[u] + parts[u]], k > 0,
                                       stats, ws, ws.numel())
         with timer("k_apply"):
-            Z.zero_shard_apply(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"],
-                               stats, 0.0, 0, ws, ws.numel(), res)
-        _finish_step(Z, torch, res, res_h, st)
+            Z.zero_shard_apply_chained(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, hy, table, 1, n_table, chain,
+                                       stats, 0.0, 0, ws, ws.numel(), res)
+
+    def path_of_last_step():
+        return Z.read_result(res).path
+
+    def checks(steps):
+        out = _gather_status_check(gstatus)(steps)
+        out.update(_check_chain(Z, chain)(steps))
+        return out
 
     total_units = sum(units)
-    return dict(name=wl.name, step=step, state=st, elements=L, nd=nd, launches_per_step=3 * len(units) + 1,
+    return dict(name=wl.name, step=step, state=st, elements=L, nd=nd, launches_per_step=3 * len(units) + 2,
+                path_of_last_step=path_of_last_step,
                 kernel_bytes={"k_gather_bulk": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
-                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=_gather_status_check(gstatus),
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=checks,
                 formula_bytes=2 * 4 * total_units + (2 * nd + 2) * L + 28 * L,
                 config={"workload": "zero3-llama3-8b: Llama-3-8B group as 34 ZeRO-3 units, N_d=4, rank 1",
                         "units": len(units), "shard_elements": L, "psi": total_units,
-                        "path": "per unit: gather x2 (zero3_gather_bulk on every SM), bucket reduce; then apply",
+                        "path": "per unit: gather x2 (zero3_gather_bulk on every SM), bucket reduce; then "
+                                "zero_shard_apply_chained (t, S and the bookkeeping on the device, no host round "
+                                "trip between steps)",
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
 
 
-def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
+def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     """ZeRO-3 with owner broadcast on the Llama-3-8B group, N_d = 4, rank 1:
     each rank keeps one contiguous segment of the flat vector (the plan's
     partition); per step every one of the 34 units is rebuilt forward and
@@ -706,12 +840,14 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
 
     gstatus = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    order = list(range(len(units))) + list(reversed(range(len(units))))
+
     def step(from_host=False):
-        for u in list(range(len(units))) + list(reversed(range(len(units)))):
-            with timer("k_gather_bulk"):
+        with timer("k_gather_bulk", len(order)):
+            for u in order:
                 Z.zero3_gather_bulk(gathers[u][0], gathers[u][1], Z.ZERO_BF16, layer, 0, gstatus)
-        for k, (bk, sh) in enumerate(reduces):
-            with timer("k_reduce"):
+        with timer("k_reduce", len(reduces)):
+            for k, (bk, sh) in enumerate(reduces):
                 Z.zero_shard_reduce(bk, Z.ZERO_BF16, sh, k > 0, stats, ws, ws.numel())
         with timer("k_apply"):
             Z.zero_shard_apply(sh_apply, Z.ZERO_BF16, segs[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]),
@@ -733,7 +869,7 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None):
                 sample_for_cpu=None)
 
 
-def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, tokens=1024, gather_ctas=32):
+def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, vocab=None, tokens=1024, gather_ctas=32):
     """ZeRO-3 on the Llama-3-8B group (N_d = 4, rank 1) with the parameter
     gather of the next unit prefetched on a side stream while the current unit
     computes.  The units' computation is a stand-in: per unit a bf16 GEMM of
@@ -1033,45 +1169,19 @@ def build_line(world, steps, warmup, ms, elements, nd, config, roofline, kernels
 
 
 # ------------------------------------------------------------------ main
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gpt2-1.5b-nd8", choices=sorted(WORKLOADS))
-    ap.add_argument("--layers", type=int, default=None,
-                    help="layer count of the workload's group (default: the full model); fewer gives a small case "
-                         "of the same kernels, e.g. for profiler captures")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--tokens", type=int, default=1024,
-                    help="zero3-prefetch-llama3-8b: activations of the stand-in GEMM per unit")
-    ap.add_argument("--gather-ctas", type=int, default=32,
-                    help="zero3-prefetch-llama3-8b: CTAs the prefetched gather may use")
-    args = ap.parse_args()
-    rank, world, local = dist_env()
-    import workloads as W
+# Workloads measured after the headline one in the default run, each on its
+# own (the previous one's buffers freed first): the clipped rank-local
+# Llama-3-8B step and the ZeRO-3 Llama-3-8B step (the 8B-shaped
+# configurations), and the 7.5B-shaped rank-local step with 64 slices.
+ALSO = ("llama3-8b-nd4-r1", "zero3-llama3-8b", "gpt-7.5b-nd64-r63")
 
-    if args.impl == "reference":
-        return reference_arm(args, rank, world, W)
 
-    import torch
-    import torch.distributed as dist
-    import zero_dp_partitioned_gb300 as Z
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    timer = KernelTimer(torch)
-    kw = dict(tokens=args.tokens, gather_ctas=args.gather_ctas) if args.workload == "zero3-prefetch-llama3-8b" else {}
-    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, layers=args.layers, **kw)
+def measure(wl, args, world, local, dev, torch, timer, barrier, e2e_on):
+    """W untimed steps, then K steps between barriers and synchronisations,
+    timed by CUDA events on the launching stream, with the SM clocks sampled
+    during the timed region; then, if the workload has one, the end-to-end
+    leg.  Returns the step time (max over ranks), the per-kernel times, the
+    clock record and the end-to-end record."""
     step = wl["step"]
     sampler = ClockSampler(local)
     for _ in range(max(3, args.warmup)):
@@ -1083,6 +1193,7 @@ def main():
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    timer.events.clear()
     timer.on = True
     start.record()
     for _ in range(args.steps):
@@ -1100,7 +1211,7 @@ def main():
         wl["config"].update(wl["extra"](args.steps))
 
     e2e = None
-    if wl["e2e_ok"]:
+    if e2e_on and wl["e2e_ok"]:
         for _ in range(2):
             step(from_host=True)
         torch.cuda.synchronize()
@@ -1121,18 +1232,24 @@ def main():
                "note": "bound by the host link: ~211 GB/s at best on this host, shared with other tenants"}
         if wl.get("e2e_note"):
             e2e["overlap"] = wl["e2e_note"]
+        if wl.get("e2e_parts"):
+            e2e["link_alone"] = wl["e2e_parts"]()
+    return ms, kinds, clocks, e2e
 
+
+def kernel_figures(wl, kinds, steps):
+    """Per-kernel algorithmic bytes and bandwidth, and the roofline entry of the
+    dominant kernel (the one with the most time per step)."""
     peak, peak_src = measured_peaks()
     per_kernel = {}
     for kind, d in kinds.items():
-        per_launch_bytes = wl["kernel_bytes"][kind] / (d["launches"] / args.steps)
+        per_launch_bytes = wl["kernel_bytes"][kind] / (d["launches"] / steps)
         gbs = per_launch_bytes / (d["ms_per_launch"] / 1e3) / 1e9
         per_kernel[kind] = dict(d, algorithmic_bytes_per_launch=per_launch_bytes, achieved_gbs=gbs,
                                 frac=gbs / peak)
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
     dk = per_kernel[dom]
-    wl["config"]["update_kernel"] = PATH_NAMES.get(wl["state"]["path"], "?")
-    wl["config"]["kernel_path_env"] = os.environ.get("ZERO_GB300_PATH", "auto")
+    wl["config"]["update_kernel"] = PATH_NAMES.get(wl["state"].get("path"), "?")
     roofline = {"bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dk["achieved_gbs"] / peak, "traffic": ncu_traffic(wl["name"], dom),
                 "peak_source": peak_src,
@@ -1142,15 +1259,93 @@ def main():
                 "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": dk["achieved_gbs"] / NOMINAL_HBM_GBS}
     if roofline["traffic"] is not None:
         dram = roofline["traffic"] / (dk["ms_per_launch"] / 1e3) / 1e9
-        roofline.update(dram_gbs=dram, dram_frac=dram / peak, dram_frac_of_nominal=dram / NOMINAL_HBM_GBS)
+        roofline.update(dram_gbs=dram, dram_frac=dram / peak, dram_frac_of_nominal=dram / NOMINAL_HBM_GBS,
+                        traffic_over_algorithmic=roofline["traffic"] / dk["algorithmic_bytes_per_launch"])
+    return roofline, per_kernel, peak
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2-1.5b-nd8", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer count of the workload's group (default: the full model); fewer gives a small case "
+                         "of the same kernels, e.g. for profiler captures")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="vocabulary of the workload's group (default: the model's); smaller gives a small case")
+    ap.add_argument("--no-also", action="store_true",
+                    help="measure only --workload (the default run also measures " + ", ".join(ALSO) + ")")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--tokens", type=int, default=1024,
+                    help="zero3-prefetch-llama3-8b: activations of the stand-in GEMM per unit")
+    ap.add_argument("--gather-ctas", type=int, default=32,
+                    help="zero3-prefetch-llama3-8b: CTAs the prefetched gather may use")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    import workloads as W
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world, W)
+
+    import gc
+
+    import torch
+    import torch.distributed as dist
+    import zero_dp_partitioned_gb300 as Z
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    timer = KernelTimer(torch)
+    kw = dict(tokens=args.tokens, gather_ctas=args.gather_ctas) if args.workload == "zero3-prefetch-llama3-8b" else {}
+    wl = WORKLOADS[args.workload](Z, W, torch, dev, not args.no_e2e, timer, layers=args.layers, vocab=args.vocab,
+                                  **kw)
+    ms, kinds, clocks, e2e = measure(wl, args, world, local, dev, torch, timer, barrier, not args.no_e2e)
+    roofline, per_kernel, peak = kernel_figures(wl, kinds, args.steps)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and wl["sample_for_cpu"]:
         cpu = cpu_baseline(wl)
+    line = None
     if rank == 0:
         line = build_line(world, args.steps, max(3, args.warmup), ms, wl["elements"], wl["nd"], wl["config"],
                           roofline, per_kernel, cpu, e2e, clocks, wl["launches_per_step"] * args.steps,
                           wl["formula_bytes"] if wl["name"].startswith("zero3") else None,
                           actual_bytes=sum(wl["kernel_bytes"].values()), peak=peak)
+    also = [] if (args.no_also or args.workload != "gpt2-1.5b-nd8" or args.layers or args.vocab) else ALSO
+    if also:
+        del wl
+        gc.collect()
+        torch.cuda.empty_cache()
+        entries = []
+        for name in also:
+            w2 = WORKLOADS[name](Z, W, torch, dev, False, timer)
+            ms2, kinds2, clocks2, _ = measure(w2, args, world, local, dev, torch, timer, barrier, False)
+            roof2, per2, _ = kernel_figures(w2, kinds2, args.steps)
+            if rank == 0:
+                sub = build_line(world, args.steps, max(3, args.warmup), ms2, w2["elements"], w2["nd"],
+                                 w2["config"], roof2, per2, None, None, clocks2, w2["launches_per_step"] * args.steps,
+                                 w2["formula_bytes"] if w2["name"].startswith("zero3") else None,
+                                 actual_bytes=sum(w2["kernel_bytes"].values()), peak=peak)
+                for k in ("vs_baseline", "cpu_baseline", "e2e", "impl", "data", "dtype", "higher_is_better",
+                          "scaling", "n_gpus"):
+                    sub.pop(k, None)
+                entries.append(sub)
+            del w2
+            gc.collect()
+            torch.cuda.empty_cache()
+        if rank == 0:
+            line["also"] = entries
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -487,6 +487,28 @@ int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int gr
                             void* workspace, size_t workspace_bytes,
                             zero_result* result, void* stream);
 
+/* The apply pass with its bookkeeping on the device: what zero_shard_apply
+ * computes for t = chain->step and S = chain->loss_scale, reading the state
+ * set chain->cur of every shard and writing the other one, then the chain
+ * updated as for zero_shard_step_chained.  The reduce pass before it needs
+ * no step scalars, so a chained ZeRO-3 step is its gathers and bucket
+ * reduces (zero3_gather_*, zero3_reduce_bucket) followed by this call, and a
+ * chained clipped step is zero_shard_reduce followed by this call: neither
+ * needs a host round trip between steps.  Unlike the fused pass, the apply
+ * pass writes nothing on a skipped step, so a shard may update its state in
+ * place (*_out == *_in; the chain's cur then changes nothing).
+ * Arguments as zero_shard_apply, plus scalar_table, table_t0, n_table and
+ * chain as for zero_shard_step_chained (hyper->step is ignored).  Errors as
+ * zero_shard_apply, and ZERO_EINVAL for a NULL or misaligned chain or
+ * table. */
+int zero_shard_apply_chained(const zero_shard* shards, int n_shards, int grad_dtype,
+                             void* flat_param, int param_dtype,
+                             const zero_hyper* hyper, const float* scalar_table, int64_t table_t0,
+                             int64_t n_table, zero_chain* chain,
+                             const zero_stats* stats, double extra_sumsq, int extra_overflow,
+                             void* workspace, size_t workspace_bytes,
+                             zero_result* result, void* stream);
+
 /* Message of the last error on this thread ("" if none). */
 const char* zero_last_error(void);
 

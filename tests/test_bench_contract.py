@@ -116,3 +116,38 @@ def test_all_cores_oracle_timing_splits_the_work_exactly():
     assert not np.array_equal(ref, flat)
     assert np.array_equal(got, ref)
 
+
+
+class _FakeEvent:
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_grouped_kernel_timing_and_the_dominant_kernel():
+    """One event pair may enclose several back-to-back launches of a kernel
+    (the ZeRO-3 step's 68 gathers, 34 reduces): the time per launch is the
+    enclosed time over the launch count, and the roofline entry names the
+    kernel with the most time per step, with its algorithmic bytes per launch
+    (the workload's bytes per step over its launches per step)."""
+    import bench
+    timer = bench.KernelTimer(None)
+    steps = 2
+    for s in range(steps):
+        timer.events.append(("k_gather_bulk", 68, _FakeEvent(0.0), _FakeEvent(9.92)))
+        timer.events.append(("k_reduce", 34, _FakeEvent(0.0), _FakeEvent(3.06)))
+        timer.events.append(("k_apply", 1, _FakeEvent(0.0), _FakeEvent(8.6)))
+    kinds = timer.per_kind(steps)
+    assert kinds["k_gather_bulk"]["launches"] == 136 and kinds["k_gather_bulk"]["event_pairs"] == 2
+    assert kinds["k_gather_bulk"]["ms_per_launch"] == pytest.approx(9.92 / 68)
+    assert kinds["k_reduce"]["ms_per_step"] == pytest.approx(3.06)
+    wl = {"name": "w", "state": {"path": 2}, "config": {},
+          "kernel_bytes": {"k_gather_bulk": 64_242_089_984, "k_reduce": 20_075_653_120, "k_apply": 56_211_828_736}}
+    roof, per, peak = bench.kernel_figures(wl, kinds, steps)
+    assert roof["kernel"] == "k_gather_bulk" and roof["bound"] == "hbm"
+    assert roof["algorithmic_bytes_per_launch"] == pytest.approx(64_242_089_984 / 68)
+    assert roof["achieved"] == pytest.approx(64_242_089_984 / 68 / (9.92 / 68 / 1e3) / 1e9)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / peak)
+    assert per["k_apply"]["achieved_gbs"] == pytest.approx(56_211_828_736 / 8.6e-3 / 1e9)

@@ -232,3 +232,70 @@ def test_chained_step_argument_errors(Z):
             Z.zero_shard_step_chained(slices, dt, args["shards"], run.flat, dt, run.hyper, args["table"], 1,
                                       args["n_table"], args["chain_dev"], 0.0, 0, run.ws, run.ws.numel(), run.res)
         assert e.value.code == code
+
+
+@pytest.mark.parametrize("inplace", [True, False])
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_chained_apply_after_reduce_matches_the_oracle(Z, inplace, clip):
+    """zero_shard_reduce, then zero_shard_apply_chained: five steps, the second
+    with a NaN in one slice, no host synchronisation in between, each step's
+    result in its own slot.  The chain advances t, halves S on the skipped
+    step and flips its current set; the state is updated in place (the apply
+    pass writes nothing on a skipped step) or between two sets.  Bit-exact
+    against the oracle driven with the same bookkeeping on the host whenever
+    every step's multiplier k equals the oracle's."""
+    numels, nd, dt = [20000, 4096, 992], 4, 2
+    S = 1.0
+    p, flat, grads = make_problem(numels, nd, dt, 0, 66, loss_scale=S, grad_std=1e-2, steps=5)
+    grads[1][2] = grads[1][2].copy()
+    grads[1][2][11] = 0x7FC0
+    h = hyper32(max_grad_norm=clip)
+    run = ChainRun(Z, p, flat, dt, h, S)
+    A, B = run.sets
+    shards = [Z.shard(int(n), int(o), int(o), *(x[int(o):int(o) + int(n)] for x in A),
+                      *(x[int(o):int(o) + int(n)] for x in (A if inplace else B)),
+                      run.gshard[int(o):int(o) + int(n)])
+              for o, n in zip(p["rank_offsets"], p["rank_numels"])]
+    slices = [[dev16(g, dt) for g in step] for step in grads]
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(5, 48, dtype=torch.uint8, device=DEV)
+    for k in range(5):
+        Z.zero_shard_reduce(slices[k], dt, shards, 0, stats, run.ws, run.ws.numel())
+        Z.zero_shard_apply_chained(shards, dt, run.flat, dt, run.hyper, run.table, 1, run.n_table, run.chain, stats,
+                                   0.0, 0, run.ws, run.ws.numel(), res[k])
+    torch.cuda.synchronize()
+    osh, oflat, t, So, results = oracle_run(p, flat, dt, h, S, grads)
+    rg = [Z.read_result(res[k]) for k in range(5)]
+    assert [r.applied for r in rg] == [r.applied for r in results] == [1, 0, 1, 1, 1]
+    assert all(r.path == 2 and r.status == 0 for r in rg)
+    c = Z.read_chain(run.chain)
+    assert (c.step, c.loss_scale, c.applied, c.skipped, c.failed, c.cur) == (t, So, 4, 1, 0, 0)
+    exact = all(a.grad_mult == b.grad_mult for a, b in zip(rg, results) if b.applied)
+    got_flat = t2u16(run.flat)
+    state = A if inplace else run.sets[c.cur]           # four applied steps: the set read first is current again
+    if exact:
+        assert np.array_equal(got_flat, oflat)
+    else:
+        assert np.abs(got_flat.astype(np.int32) - oflat.astype(np.int32)).max() <= 1
+    for o, n, os_ in zip(p["rank_offsets"], p["rank_numels"], osh):
+        o, n = int(o), int(n)
+        for x, ref in zip(state, (os_["master"], os_["m"], os_["v"])):
+            got = x[o:o + n].cpu().numpy()
+            if exact:
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+            else:
+                assert np.allclose(got, ref, rtol=1e-5, atol=1e-3 * np.abs(ref).max())
+
+
+def test_chained_apply_argument_errors(Z):
+    numels, nd, dt = [4096], 2, 2
+    p, flat, grads = make_problem(numels, nd, dt, 0, 67, steps=1)
+    run = ChainRun(Z, p, flat, dt, hyper32(), 1.0)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    for kw in (dict(chain=0), dict(table=0), dict(n_table=0), dict(stats=0), dict(res=run.res[4:])):
+        args = dict(chain=run.chain, table=run.table, n_table=run.n_table, stats=stats, res=run.res)
+        args.update(kw)
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_apply_chained(run.shards, dt, run.flat, dt, run.hyper, args["table"], 1, args["n_table"],
+                                       args["chain"], args["stats"], 0.0, 0, run.ws, run.ws.numel(), args["res"])
+        assert e.value.code == Z.ZERO_EINVAL

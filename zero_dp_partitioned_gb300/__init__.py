@@ -91,6 +91,8 @@ _SIGS = {
     "zero_adam_scalar_table": (_I, [_P, _I64, _I64, _P]),
     "zero_shard_step_chained": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _P, _I64, _I64, _P, ctypes.c_double, _I, _P,
                                      ctypes.c_size_t, _P, _P]),
+    "zero_shard_apply_chained": (_I, [_P, _I, _I, _P, _I, _P, _P, _I64, _I64, _P, _P, ctypes.c_double, _I, _P,
+                                      ctypes.c_size_t, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 # every symbol include/zero.h declares
@@ -302,6 +304,18 @@ def zero_shard_step_chained(grad_slices, grad_dtype, shards, flat_param, param_d
                                        int(table_t0), int(n_table), _ptr(chain_dev), extra_sumsq,
                                        int(extra_overflow), _ptr(workspace), workspace_bytes, _ptr(result),
                                        _stream(stream)))
+
+
+def zero_shard_apply_chained(shards, grad_dtype, flat_param, param_dtype, hyper, scalar_table, table_t0, n_table,
+                             chain_dev, stats, extra_sumsq, extra_overflow, workspace, workspace_bytes, result,
+                             stream=None):
+    """The apply pass with t, S and the state set in use read from the device
+    zero_chain chain_dev, which it then updates; shards may update in place."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_apply_chained(sh, len(shards), grad_dtype, _ptr(flat_param), param_dtype,
+                                        ctypes.byref(hyper), _ptr(scalar_table), int(table_t0), int(n_table),
+                                        _ptr(chain_dev), _ptr(stats), extra_sumsq, int(extra_overflow),
+                                        _ptr(workspace), workspace_bytes, _ptr(result), _stream(stream)))
 
 
 def read_result(t) -> zero_result:

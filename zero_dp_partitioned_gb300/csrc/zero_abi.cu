@@ -554,6 +554,45 @@ int zero_shard_apply(const zero_shard* shards, int n_shards, int grad_dtype, voi
     return launch_apply(a, grad_dtype, param_dtype, vec, static_cast<cudaStream_t>(stream));
 }
 
+int zero_shard_apply_chained(const zero_shard* shards, int n_shards, int grad_dtype, void* flat_param,
+                             int param_dtype, const zero_hyper* hyper, const float* scalar_table, int64_t table_t0,
+                             int64_t n_table, zero_chain* chain, const zero_stats* stats, double extra_sumsq,
+                             int extra_overflow, void* workspace, size_t workspace_bytes, zero_result* result,
+                             void* stream) {
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (!hyper) return fail(ZERO_EINVAL, "hyper is NULL");
+    if (!chain || !aligned(chain, 8)) return fail(ZERO_EINVAL, "chain is NULL or not 8-byte aligned");
+    if (!scalar_table || !aligned(scalar_table, 4) || n_table < 1 || table_t0 < 1)
+        return fail(ZERO_EINVAL, "scalar_table is NULL or misaligned, or n_table / table_t0 < 1");
+    if (!stats || !aligned(stats, 8)) return fail(ZERO_EINVAL, "stats is NULL or not 8-byte aligned");
+    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    int rc;
+    if ((rc = pack_shards(a, shards, n_shards, 3)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+    a.flat_param = flat_param;
+    zero_hyper h1 = *hyper;
+    h1.step = 1;
+    a.sc = adam_scalars(h1);              // t-independent scalars; ss and rb2 come from the table
+    a.max_norm = (double)hyper->max_grad_norm;
+    a.extra_sumsq = extra_sumsq;
+    a.extra_overflow = extra_overflow ? 1 : 0;
+    a.stats = const_cast<zero_stats*>(stats);
+    a.result = result;
+    a.chain = chain;
+    a.sc_table = scalar_table;
+    a.t0 = table_t0;
+    a.n_table = n_table;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int vec = vec8_ok(a, 3) ? 8 : 1;
+    number_tiles(a, vec, HEAD_STATE);
+    if ((rc = launch_apply(a, grad_dtype, param_dtype, vec, s)) != ZERO_OK) return rc;
+    return launch_chain_update(chain, result, s);
+}
+
 // The register-staged gather's arguments for n pieces laid end to end in out
 // (pointers and lengths already validated); returns the vector width.
 static int gather_args(const void* const* src, const int64_t* len, int n, void* out, GatherArgs& g) {

@@ -40,6 +40,8 @@ constexpr int BULK_MAX_STAGES = 8;
 __global__ void __launch_bounds__(32, 1) k_gather_bulk(const __grid_constant__ BulkGatherArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     if (threadIdx.x != 0) {
+        pdl_wait();         // see the programmatic dependent launch note in zero_kernels.cuh
+        pdl_launch_next();
         // CTA 0's other lanes: the unaligned bytes at both ends of every piece
         if (blockIdx.x == 0) {
             for (int p = threadIdx.x - 1; p < a.n; p += 31) {
@@ -62,6 +64,10 @@ __global__ void __launch_bounds__(32, 1) k_gather_bulk(const __grid_constant__ B
     uint32_t* stage_bytes = reinterpret_cast<uint32_t*>(smem + 16 * BULK_MAX_STAGES);
     for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
     fence_mbar_init();
+    // Set-up above touches only this CTA's shared memory, so it overlaps the
+    // previous kernel's tail; global memory is touched only after the wait.
+    pdl_wait();
+    pdl_launch_next();
 
     // Load cursor: the piece holding the next chunk to load, kept in registers
     // (this CTA's chunks only move forward through the pieces).
@@ -128,7 +134,7 @@ int launch_gather_bulk(const BulkGatherArgs& a, int grid, cudaStream_t s) {
                        "bulk gather shared-memory size");
     if (rc != ZERO_OK) return rc;
     void* args[] = {const_cast<BulkGatherArgs*>(&a)};
-    return cuda_fail(cudaLaunchKernel((const void*)k_gather_bulk, dim3(grid), dim3(32), args, smem, s),
+    return cuda_fail(launch_after_previous((const void*)k_gather_bulk, grid, 32, args, smem, s),
                      "bulk gather launch");
 }
 

@@ -39,6 +39,10 @@ constexpr int BPS_RECOVER = 0;
 int grid_for(const void* func, int64_t n_tiles, int max_per_sm = 0);
 int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int max_per_sm = 0);
 
+// Launch of a kernel that starts with pdl_wait() (the gathers and the
+// reduce), allowed to begin while the previous kernel of the stream finishes.
+cudaError_t launch_after_previous(const void* f, int grid, int block, void** args, size_t smem, cudaStream_t s);
+
 // Launchers; each validates nothing (the entry points did) and returns
 // ZERO_OK or ZERO_ECUDA.  vec is 8 or 1.
 int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s);

@@ -15,14 +15,14 @@
 //    bytes in flight; loads and stores use the streaming cache hints because
 //    no byte is touched twice.
 //  * Gradient statistics: squares of the 16-bit reduced values are exact in
-//    fp32 (at most 22 significant bits).  Each thread sums them with
-//    Neumaier's compensated summation on the fp32 pipe (GB300's fp64 rate is
-//    far too low for one fp64 add per element), which keeps the rounding
-//    error of the per-thread sum at the level of fp64; the (sum, compensation)
-//    pair is added into an fp64 accumulator at the end.  A warp shuffle and a
-//    shared-memory pass give one fp64 partial per block, stored in the
-//    workspace; the last block to finish (one atomic per block) adds the
-//    partials in block order, so the result is deterministic for a given grid.
+//    fp32 (at most 22 significant bits).  Each vector's squares are summed on
+//    the fp32 pipe with error-free TwoSum steps, the vector sum is added in
+//    fp64 (one fp64 add per 8 elements: GB300's fp64 rate is far too low for
+//    one per element) and the exact rounding errors are carried apart (see
+//    SumSq).  A warp shuffle and a shared-memory pass give one fp64 partial
+//    per block, stored in the workspace; the last block to finish (one atomic
+//    per block) adds the partials in block order, so the result is
+//    deterministic for a given grid.
 //  * Every fp32 operation of the reduction and of AdamW is an explicitly
 //    rounded intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn) so no
 //    multiply-add is contracted: results are those of the plain IEEE sequence.
@@ -138,6 +138,20 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) { return __ldcs(reinte
 __device__ __forceinline__ float4 ld_stream4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st_stream4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// The gather and reduce kernels run back to back many times per step (two
+// gathers and one reduce per ZeRO-3 unit), 0.1 ms each, and a launch's
+// ramp-up and tail cost them a few microseconds each.  They are launched with
+// programmatic stream serialisation: a launch may begin while the previous
+// kernel of the stream finishes.  Every thread first waits for the previous
+// grid to complete and its memory to be visible (griddepcontrol.wait; at once
+// if there is no such grid), so no access is reordered.  Each block then lets
+// the next kernel of the stream launch (griddepcontrol.launch_dependents).
+// That kernel launches only once every block of this grid has started, so its
+// waiting blocks cannot keep any of this grid's blocks from running.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- per-element arithmetic
 // Reduce-scatter arithmetic for one element: s is the rank-ordered fp32 sum.
 template <int GDT>
@@ -193,64 +207,54 @@ __device__ __forceinline__ void store8(uint16_t* dst, int64_t q, const uint32_t 
 }
 
 // ---------------------------------------------------------------- reductions
-// Compensated running sum of non-negative fp32 terms (Kahan): s - c carries
-// the sum with an error of order n u^2 of the sum instead of n u.
+// Sum of squares of 16-bit values.  A square of a 16-bit value is exact in
+// fp32 (at most 22 significant bits).  The squares of one vector are added in
+// fp32 with TwoSum (Knuth): t = s + q rounded, and e = (s - (t - z)) + (q - z)
+// with z = t - s is exactly the rounding error s + q - t, whatever the
+// operands' magnitudes.  Each vector's fp32 sum goes into an fp64 accumulator
+// (one fp64 add per vector: a small share of GB300's fp64 rate) and its
+// rounding errors into an fp32 one, added in at the end.  The result is then
+// off the exact sum by a few fp64 roundings, far below fp32 resolution, so
+// the multiplier fp32(c / S) derived from it almost never differs from the
+// one an exactly rounded sum gives -- even for a thread that sums only one
+// vector, where a Kahan-compensated fp32 sum loses its compensation (the
+// correction falls below half an ulp of the next term; measured: 3e-9
+// relative off the exact sum on a small clipped step).
 struct SumSq {
-    float s = 0.0f, c = 0.0f;
-    double acc = 0.0;
+    double acc = 0.0;   // sum of the vectors' fp32 sums (and of any squares taken in fp64)
+    float err = 0.0f;   // sum of the exact TwoSum rounding errors
 
-    __device__ __forceinline__ void add(float x) {
-        const float y = __fsub_rn(x, c);
-        const float t = __fadd_rn(s, y);
-        c = __fsub_rn(__fsub_rn(t, s), y);
+    // Add s + q to the running vector sum s, keeping the rounding error.
+    __device__ __forceinline__ void two_sum(float& s, float q) {
+        const float t = __fadd_rn(s, q);
+        const float z = __fsub_rn(t, s);
+        err = __fadd_rn(err, __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(q, z)));
         s = t;
     }
-    // Add the squares of 8 fp32 values (exact products); vectors whose
-    // squares leave the fp32 range go to fp64 directly.
-    __device__ __forceinline__ void add8(const float (&a)[8]) {
-        float q[8];
+    // Add the squares of N fp32 values (exact products); vectors whose squares
+    // leave the fp32 range go to fp64 directly.
+    template <int N>
+    __device__ __forceinline__ void addn(const float (&a)[N]) {
+        float q[N];
         bool ok = true;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < N; ++e) {
             q[e] = __fmul_rn(a[e], a[e]);
             ok &= q[e] < 1e30f;          // false for inf, NaN and huge squares
         }
         if (ok) {
+            float s = q[0];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) add(q[e]);
-            if (s > 1e30f) flush();
+            for (int e = 1; e < N; ++e) two_sum(s, q[e]);
+            acc += (double)s;
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc += (double)a[e] * (double)a[e];
+            for (int e = 0; e < N; ++e) acc += (double)a[e] * (double)a[e];
         }
     }
-    __device__ __forceinline__ void add4(const float (&a)[4]) {
-        float q[4];
-        bool ok = true;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            q[e] = __fmul_rn(a[e], a[e]);
-            ok &= q[e] < 1e30f;
-        }
-        if (ok) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) add(q[e]);
-            if (s > 1e30f) flush();
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc += (double)a[e] * (double)a[e];
-        }
-    }
+    __device__ __forceinline__ void add8(const float (&a)[8]) { addn<8>(a); }
     __device__ __forceinline__ void add_fp64(float a) { acc += (double)a * (double)a; }
-    __device__ __forceinline__ void flush() {
-        acc += (double)s - (double)c;
-        s = 0.0f;
-        c = 0.0f;
-    }
-    __device__ __forceinline__ double total() {
-        flush();
-        return acc;
-    }
+    __device__ __forceinline__ double total() { return acc + (double)err; }
 };
 
 __device__ __forceinline__ double warp_sum(double x) {
@@ -571,6 +575,8 @@ template <int GDT, int VEC, int NS>
 __global__ void __launch_bounds__(TILE_THREADS)
 k_reduce(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
+    pdl_wait();
+    pdl_launch_next();
     SumSq sumsq;
     int ovf = 0;
     int si = 0;
@@ -757,6 +763,8 @@ template <int VEC>
 __global__ void __launch_bounds__(TILE_THREADS) k_gather(const __grid_constant__ GatherArgs a) {
     constexpr int U = VEC == 8 ? GATHER_UNROLL : 2;
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC * U;
+    pdl_wait();
+    pdl_launch_next();
     const int64_t n_tiles = a.tile_begin[a.n];
     uint16_t* O = static_cast<uint16_t*>(a.out);
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {

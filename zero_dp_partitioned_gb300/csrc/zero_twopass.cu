@@ -37,7 +37,7 @@ int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s) {
     const void* f = reduce_kernel(gdt, vec, ns_variant(a.n_slices));
     const int grid = grid_for(f, a.n_tiles, BPS_REDUCE);
     void* args[] = {const_cast<StepArgs*>(&a)};
-    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "reduce launch");
+    return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, 0, s), "reduce launch");
 }
 
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s) {
@@ -52,7 +52,28 @@ int launch_gather(const GatherArgs& a, int vec, cudaStream_t s, int max_grid) {
     int grid = grid_for(f, a.tile_begin[a.n], BPS_GATHER);
     if (max_grid > 0 && grid > max_grid) grid = max_grid;
     void* args[] = {const_cast<GatherArgs*>(&a)};
-    return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "gather launch");
+    return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, 0, s), "gather launch");
+}
+
+}  // namespace zdp
+
+namespace zdp {
+
+// A launch allowed to begin while the previous kernel of the stream finishes
+// (programmatic stream serialisation); the kernel waits for that kernel's
+// completion before its first memory access.
+cudaError_t launch_after_previous(const void* f, int grid, int block, void** args, size_t smem, cudaStream_t s) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 }  // namespace zdp
