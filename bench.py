@@ -161,18 +161,21 @@ class KernelTimer:
         self.events = []          # (kind, launches, start, end)
         self.on = False
 
+    def _event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
     def __call__(self, kind, launches=1):
         timer = self
 
         class _Ctx:
             def __enter__(self):
                 if timer.on:
-                    self.a = timer.torch.cuda.Event(enable_timing=True)
+                    self.a = timer._event()
                     self.a.record()
 
             def __exit__(self, *exc):
                 if timer.on:
-                    b = timer.torch.cuda.Event(enable_timing=True)
+                    b = timer._event()
                     b.record()
                     timer.events.append((kind, launches, self.a, b))
         return _Ctx()
@@ -569,16 +572,20 @@ def gpt2_allreduce(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
+    hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
 
     def step(from_host=False):
         with timer("k_reduce"):
             Z.zero_shard_reduce(grads, Z.ZERO_BF16, sh, 0, stats, ws, ws.numel())
         with timer("k_apply"):
-            Z.zero_shard_apply(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"], stats,
-                               0.0, 0, ws, ws.numel(), res)
-        _finish_step(Z, torch, res, res_h, st)
+            Z.zero_shard_apply_chained(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, hy, table, 1, n_table, chain, stats, 0.0, 0,
+                                       ws, ws.numel(), res)
 
-    return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=2,
+    def path_of_last_step():
+        return Z.read_result(res).path
+
+    return dict(name=name, step=step, state=st, elements=P, nd=nd, launches_per_step=3,
+                path_of_last_step=path_of_last_step, extra=_check_chain(Z, chain),
                 kernel_bytes={"k_reduce": (2 * nd + 2) * P, "k_apply": 28 * P}, dominant_label=None,
                 h2d=None, d2h=48, e2e_ok=False, formula_bytes=(2 * nd + 26) * P,
                 config={"workload": f"{name}: GPT-2-shaped group, N_d=8, all ranks, stage 1 with a full "
@@ -830,6 +837,7 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
+    hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
     gathers = [([segs[r][s0:s0 + ln] for r, u0, s0, ln in pieces[u]], [ln for *_, ln in pieces[u]])
                for u in range(len(units))]
     reduces = [(buckets[u], [Z.shard(ln, u0, 0, None, None, None, grad_shard=gseg[s0:s0 + ln])])
@@ -847,15 +855,22 @@ def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
             for k, (bk, sh) in enumerate(reduces):
                 Z.zero_shard_reduce(bk, Z.ZERO_BF16, sh, k > 0, stats, ws, ws.numel())
         with timer("k_apply"):
-            Z.zero_shard_apply(sh_apply, Z.ZERO_BF16, segs[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]),
-                               st["S"], stats, 0.0, 0, ws, ws.numel(), res)
-        _finish_step(Z, torch, res, res_h, st)
+            Z.zero_shard_apply_chained(sh_apply, Z.ZERO_BF16, segs[me], Z.ZERO_BF16, hy, table, 1, n_table, chain,
+                                       stats, 0.0, 0, ws, ws.numel(), res)
+
+    def path_of_last_step():
+        return Z.read_result(res).path
+
+    def checks(steps):
+        out = _gather_status_check(gstatus)(steps)
+        out.update(_check_chain(Z, chain)(steps))
+        return out
 
     total = sum(units)
     return dict(name=name, step=step, state=st, elements=L, nd=nd,
-                launches_per_step=2 * len(units) + len(reduces) + 1,
+                launches_per_step=2 * len(units) + len(reduces) + 2, path_of_last_step=path_of_last_step,
                 kernel_bytes={"k_gather_bulk": 2 * 4 * total, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
-                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=_gather_status_check(gstatus),
+                dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=checks,
                 formula_bytes=2 * 4 * total + (2 * nd + 2) * L + 28 * L,
                 config={"workload": f"{name}: Llama-3-8B group as {len(units)} ZeRO-3 units, owner broadcast "
                                     "from contiguous rank segments, N_d=4, rank 1",
@@ -911,6 +926,7 @@ def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, vocab=None, tokens
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     gstatus = torch.zeros(1, dtype=torch.int32, device=dev)
     st = dict(cur=0, t=1, S=wl.loss_scale)
+    hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
     part_ptrs = [[rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)] for u in range(len(units))]
     n_units = len(units)
     order = [(u, 1) for u in range(n_units)] + [(u, 2) for u in reversed(range(n_units))]   # (unit, GEMMs)
@@ -931,9 +947,8 @@ def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, vocab=None, tokens
 
     def finish():
         with timer("k_apply"):
-            Z.zero_shard_apply(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, _hyper(Z, wl.hyper, st["t"]), st["S"],
-                               stats, 0.0, 0, ws, ws.numel(), res)
-        _finish_step(Z, torch, res, res_h, st)
+            Z.zero_shard_apply_chained(sh, Z.ZERO_BF16, rshards[me], Z.ZERO_BF16, hy, table, 1, n_table, chain, stats,
+                                       0.0, 0, ws, ws.numel(), res)
 
     def step(from_host=False):
         main = torch.cuda.current_stream()
@@ -984,11 +999,12 @@ def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, vocab=None, tokens
             out[key] = a.elapsed_time(b) / steps
         if int(gstatus.item()) != 0:
             raise RuntimeError("zero3_gather_bulk reported a timed-out wait")
+        out.update(_check_chain(Z, chain)(steps))
         return out
 
     total = sum(units)
     return dict(name=name, step=step, state=st, elements=L, nd=nd,
-                launches_per_step=len(order) + n_units + 1,
+                launches_per_step=len(order) + n_units + 2,
                 kernel_bytes={"k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
                 dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=extra,
                 formula_bytes=2 * 4 * total + (2 * nd + 2) * L + 28 * L,
