@@ -200,7 +200,8 @@ def _hyper(Z, h, t, clip=0.0):
     return Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], clip, t)
 
 
-PATH_NAMES = {1: "k_step_fused (fused single pass)", 2: "k_apply (apply pass after k_reduce)"}
+PATH_NAMES = {1: "k_step_fused (fused single pass)", 2: "k_apply (apply pass after k_reduce)",
+              3: "k_step_fused partial passes, decided by k_commit"}
 
 
 def _finish_step(Z, torch, res, res_h, st):
@@ -717,21 +718,27 @@ def _gather_status_check(gstatus):
     return check
 
 
-def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
+def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None, vocab=None, fused=True):
     """ZeRO-3 per-layer path, Llama-3-8B group as 34 units, N_d = 4, rank 1:
-    per step 34 forward gathers, 34 backward gathers (reverse order), 34 bucket
-    reduces onto rank 1's parts, one shard update."""
+    per step 34 forward gathers and 34 backward gathers (reverse order); then,
+    fused (the default: this workload does not clip), each unit's buckets
+    reduced onto rank 1's part and that part updated in one partial pass
+    (speculatively, into the second state set) and the step decided by one
+    commit; or, two-pass, 34 bucket reduces and one apply of the whole shard
+    (in place)."""
     wl = W.workload("zero3-llama3-8b")
+    base = "zero3-llama3" if fused else "zero3-twopass-llama3"
+    wl.name = f"{base}-8b"
     if layers or vocab:
         wl.specs = W.llama_group(L=layers or 32, V=vocab or 128256)
-        wl.name = f"zero3-llama3{_small(layers, vocab)}"
+        wl.name = f"{base}{_small(layers, vocab)}"
     nd, me = wl.nd, 1
     units = W.llama_units(wl.specs, L=layers or 32)
     parts = [u // nd for u in units]
     starts = [sum(units[:i]) for i in range(len(units))]
     uoff = [sum(parts[:i]) for i in range(len(parts))]
     L = sum(parts)
-    log(f"[bench] zero3-llama3-8b: {len(units)} units, rank shard {L}; generating inputs")
+    log(f"[bench] {wl.name}: {len(units)} units, rank shard {L}; generating inputs")
     flat = W.flat_params(wl.specs, sum(units), torch.bfloat16, wl.param_seed, dev)
     rshards = [torch.cat([flat[s + r * p: s + (r + 1) * p] for s, p in zip(starts, parts)]) for r in range(nd)]
     del flat
@@ -743,14 +750,16 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
         gs.draw_plain(row, wl.grad_std)
         buckets.append((u, row))
     layer = torch.empty(max(units), dtype=torch.bfloat16, device=dev)
-    master, m, v = (torch.empty(L, device=dev) for _ in range(3))
-    gshard = torch.empty(L, dtype=torch.bfloat16, device=dev)
-    sh = [Z.shard(L, 0, 0, master, m, v, grad_shard=gshard)]
+    A = [torch.empty(L, device=dev) for _ in range(3)]
+    B = [torch.empty(L, device=dev) for _ in range(3)] if fused else A
+    gshard = None if fused else torch.empty(L, dtype=torch.bfloat16, device=dev)
+    sh = [Z.shard(L, 0, 0, *A, *B, grad_shard=gshard)]
     Z.zero_shard_init(sh, rshards[me], Z.ZERO_BF16)
+    part_sh = [Z.shard(parts[u], me * parts[u], uoff[u], *(x[uoff[u]:uoff[u] + parts[u]] for x in A),
+                       *(x[uoff[u]:uoff[u] + parts[u]] for x in B)) for u in range(len(units))]
     ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=dev)
     stats = torch.zeros(16, dtype=torch.uint8, device=dev)
     res = torch.zeros(48, dtype=torch.uint8, device=dev)
-    res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
     hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
     part_ptrs = [[rshards[r][uoff[u]:uoff[u] + parts[u]] for r in range(nd)] for u in range(len(units))]
@@ -760,11 +769,20 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     order = list(range(len(units))) + list(reversed(range(len(units))))
 
     def step(from_host=False):
-        # one event pair per group of back-to-back launches of a kernel: the
-        # 68 gathers, the 34 reduces, the apply
+        # one event pair per group of back-to-back launches of a kernel
         with timer("k_gather_bulk", len(order)):
             for u in order:
                 Z.zero3_gather_bulk(part_ptrs[u], [parts[u]] * nd, Z.ZERO_BF16, layer, 0, gstatus)
+        if fused:
+            with timer("k_step_fused", len(buckets)):
+                for k, (u, row) in enumerate(buckets):
+                    Z.zero_shard_step_partial(row, Z.ZERO_BF16, [part_sh[u]], rshards[me], Z.ZERO_BF16, hy, 0.0,
+                                              k > 0, stats, ws, ws.numel(), scalar_table=table, table_t0=1,
+                                              n_table=n_table, chain_dev=chain)
+            with timer("k_commit+k_recover"):
+                Z.zero_shard_step_commit(sh, rshards[me], Z.ZERO_BF16, 0.0, stats, 0.0, 0, res, table_t0=1,
+                                         n_table=n_table, chain_dev=chain)
+            return
         with timer("k_reduce", len(buckets)):
             for k, (u, row) in enumerate(buckets):
                 Z.zero3_reduce_bucket(row, me, units[u], Z.ZERO_BF16, gshard[uoff[u]:uoff[u] + parts[u]], k > 0,
@@ -782,18 +800,37 @@ def zero3_llama(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
         return out
 
     total_units = sum(units)
-    return dict(name=wl.name, step=step, state=st, elements=L, nd=nd, launches_per_step=3 * len(units) + 2,
-                path_of_last_step=path_of_last_step,
-                kernel_bytes={"k_gather_bulk": 2 * 4 * total_units, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
+    gather_bytes = 2 * 4 * total_units
+    if fused:
+        kernel_bytes = {"k_gather_bulk": gather_bytes, "k_step_fused": (2 * nd + 26) * L, "k_commit+k_recover": 0}
+        launches = 3 * len(units) + 3
+        path = ("per unit: gather x2 (zero3_gather_bulk on every SM); then per unit the bucket reduce fused with the "
+                "part's AdamW (zero_shard_step_partial, speculative, ping-pong state), and one commit "
+                "(zero_shard_step_commit: the decision, the parameter restore check, the bookkeeping); t, S and the "
+                "state set on the device, no host round trip between steps")
+    else:
+        kernel_bytes = {"k_gather_bulk": gather_bytes, "k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L}
+        launches = 3 * len(units) + 2
+        path = ("per unit: gather x2 (zero3_gather_bulk on every SM), bucket reduce; then zero_shard_apply_chained "
+                "(in place; t, S and the bookkeeping on the device, no host round trip between steps)")
+    return dict(name=wl.name, step=step, state=st, elements=L, nd=nd, launches_per_step=launches,
+                path_of_last_step=path_of_last_step, kernel_bytes=kernel_bytes,
                 dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=checks,
-                formula_bytes=2 * 4 * total_units + (2 * nd + 2) * L + 28 * L,
-                config={"workload": "zero3-llama3-8b: Llama-3-8B group as 34 ZeRO-3 units, N_d=4, rank 1",
-                        "units": len(units), "shard_elements": L, "psi": total_units,
-                        "path": "per unit: gather x2 (zero3_gather_bulk on every SM), bucket reduce; then "
-                                "zero_shard_apply_chained (t, S and the bookkeeping on the device, no host round "
-                                "trip between steps)",
+                formula_bytes=gather_bytes + (2 * nd + 2) * L + 28 * L,
+                config={"workload": f"{wl.name}: Llama-3-8B group as {len(units)} ZeRO-3 units, N_d=4, rank 1",
+                        "units": len(units), "shard_elements": L, "psi": total_units, "path": path,
+                        "state": "f32 master/m/v, ping-pong" if fused else "f32 master/m/v, in place",
+                        "formula_bytes_are": "the two-pass accounting: gathers 8 psi + reduce (2 N_d + 2) + apply 28 "
+                                             "per shard element; the fused path moves (2 N_d + 26) per shard element "
+                                             "instead of (2 N_d + 30)",
                         "l2": "inputs larger than L2, no flush"},
                 sample_for_cpu=None)
+
+
+def zero3_twopass(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
+    """The ZeRO-3 step with the two-pass update (bucket reduces, then one apply
+    of the whole shard in place): the path a clipped ZeRO-3 step takes."""
+    return zero3_llama(Z, W, torch, dev, e2e, timer, layers, vocab, fused=False)
 
 
 def zero3_broadcast(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
@@ -1039,8 +1076,8 @@ def cpu_sample_gpt2(W, n_per_shard):
 
 
 WORKLOADS = {"gpt2-1.5b-nd8": gpt2_all_ranks, "gpt2-1.5b-nd8-allreduce": gpt2_allreduce, "tiny-nd3": tiny_nd3,
-             "llama3-8b-nd4-r1": llama_rank_local,
-             "gpt-7.5b-nd64-r63": gpt75_rank63, "zero3-llama3-8b": zero3_llama,
+             "llama3-8b-nd4-r1": llama_rank_local, "gpt-7.5b-nd64-r63": gpt75_rank63,
+             "zero3-llama3-8b": zero3_llama, "zero3-twopass-llama3-8b": zero3_twopass,
              "zero3-bcast-llama3-8b": zero3_broadcast, "zero3-prefetch-llama3-8b": zero3_prefetch}
 
 
@@ -1155,7 +1192,7 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 
 # Timer labels of the update pass, whose kernel the path choice names.
-UPDATE_KINDS = ("fused pass+k_recover", "k_apply")
+UPDATE_KINDS = ("fused pass+k_recover", "k_apply", "k_step_fused")
 
 
 def build_line(world, steps, warmup, ms, elements, nd, config, roofline, kernels, cpu, e2e, clocks, launches,

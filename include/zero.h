@@ -224,7 +224,8 @@ typedef struct {
  *            as before the call (restored by the library where a speculative
  *            pass had written them)
  * path       which kernels ran the update: 1 = the fused single pass,
- *            2 = the apply pass (after the reduce pass)
+ *            2 = the apply pass (after the reduce pass), 3 = partial fused
+ *            passes decided by zero_shard_step_commit
  * status     0, or ZERO_ELIMIT for a chained step whose t lies outside its
  *            scalar table (nothing is updated)
  * sumsq      sum of squares of the scaled reduced gradient plus extra_sumsq
@@ -508,6 +509,57 @@ int zero_shard_apply_chained(const zero_shard* shards, int n_shards, int grad_dt
                              const zero_stats* stats, double extra_sumsq, int extra_overflow,
                              void* workspace, size_t workspace_bytes,
                              zero_result* result, void* stream);
+
+/* ------------------------------------------------------------------------
+ * A step split into partial fused passes and a commit.
+ * Source: reading notes 9 (ZeRO-3: after a unit's backward its gradients are
+ * reduced onto the owner; the optimizer updates the owner's shard) and the
+ * DeepSpeed ZeRO stages 1-2 walkthrough, 6 (skip the whole step on any
+ * overflow).  Without clipping nothing of a shard's update depends on the
+ * other shards but the skip decision, so each part of a shard can be reduced
+ * and updated in one pass as soon as its gradients are ready -- for ZeRO-3,
+ * right after each unit's bucket reduce-scatter -- speculatively, into the
+ * second state set, with the decision taken once after the last part.  Per
+ * element this moves 2 N_d + 26 bytes, where a reduce pass and an apply pass
+ * move 2 N_d + 30.
+ *
+ * zero_shard_step_partial: what zero_shard_step's fused pass computes for
+ * these shards (rank-order reduce of their slices, AdamW from *_in to *_out,
+ * the parameters stored), with the shards' sum of squares and overflow flag
+ * added to *stats (accumulate = 0 starts it afresh) instead of a decision.
+ * Arguments as zero_shard_step, plus: max_grad_norm must be 0 (clipping
+ * needs the global norm before any update), *_out distinct from *_in;
+ * chain NULL takes t from hyper->step and S from loss_scale; otherwise t, S
+ * and the state set in use come from the device chain and the scalar table
+ * (as zero_shard_step_chained; loss_scale is ignored).  For a ZeRO-3 unit:
+ * grad_slices are the world_size full-unit buckets, the shard is the owner's
+ * part (grad_offset = owner * unit_numel / world_size) at its place in the
+ * rank's parameter shard (flat_param, param_offset) and state.
+ *
+ * zero_shard_step_commit: the decision from *stats plus extra_sumsq /
+ * extra_overflow, written to *result (path 3); on overflow the parameters of
+ * every shard given (all the step's parts, or one shard spanning them) are
+ * restored from the state set read, and the caller (or the chain) keeps
+ * that set; a chain (may be NULL: then loss_scale is the step's S) is
+ * updated as after zero_shard_step_chained, and a chained step whose t lies
+ * outside [table_t0, table_t0 + n_table) is reported as ZERO_ELIMIT and not
+ * applied.  The partial passes and the commit of one step must run in stream
+ * order, on one workspace, with nothing between them that reads the *_out
+ * state or relies on the parameters of a step that may be skipped.
+ * Errors: ZERO_EINVAL (also for clipping or in-place state), ZERO_EALIGN,
+ * ZERO_EWORKSPACE, ZERO_ELIMIT, ZERO_ECUDA, before any work is enqueued. */
+int zero_shard_step_partial(const void* const* grad_slices, int n_slices, int grad_dtype,
+                            const zero_shard* shards, int n_shards,
+                            void* flat_param, int param_dtype,
+                            const zero_hyper* hyper, float loss_scale,
+                            const float* scalar_table, int64_t table_t0, int64_t n_table, zero_chain* chain,
+                            int accumulate, zero_stats* stats,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+int zero_shard_step_commit(const zero_shard* shards, int n_shards, void* flat_param, int param_dtype,
+                           float loss_scale, int64_t table_t0, int64_t n_table, zero_chain* chain,
+                           const zero_stats* stats, double extra_sumsq, int extra_overflow,
+                           zero_result* result, void* stream);
 
 /* Message of the last error on this thread ("" if none). */
 const char* zero_last_error(void);

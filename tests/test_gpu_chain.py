@@ -364,3 +364,55 @@ def test_chained_zero3_step_replayed_from_a_cuda_graph(Z):
                     graphed["st"] + [graphed["rsh"][me], graphed["layer"], graphed["status"]]):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     assert int(graphed["status"].item()) == 0
+
+
+@pytest.mark.parametrize("numels,nd,dt", [([20000, 4096, 992], 4, 2), ([20000, 555], 3, 1)])
+def test_chained_partial_passes_then_commit_match_the_oracle(Z, numels, nd, dt):
+    """A step split into partial fused passes -- one per shard, each adding its
+    statistics -- and a commit, chained: five steps, the second with a NaN in
+    one slice, no host synchronisation, each step's result in its own slot.
+    Equal to the oracle's whole steps with the same bookkeeping, bit for bit.
+    Then a step outside the scalar table: reported ZERO_ELIMIT by the commit,
+    nothing updated, the chain's t and set kept."""
+    S = 256.0 if dt == 1 else 1.0
+    p, flat, grads = make_problem(numels, nd, dt, 0, 68, loss_scale=S, grad_std=1e-2, steps=6)
+    grads[1][0] = grads[1][0].copy()
+    grads[1][0][7] = 0x7E00 if dt == 1 else 0x7FC0
+    h = hyper32()
+    run = ChainRun(Z, p, flat, dt, h, S, n_table=6)
+    slices = [[dev16(g, dt) for g in step] for step in grads]
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(6, 48, dtype=torch.uint8, device=DEV)
+
+    def step(k):
+        for i, sh in enumerate(run.shards):
+            Z.zero_shard_step_partial(slices[k], dt, [sh], run.flat, dt, run.hyper, 0.0, i > 0, stats, run.ws,
+                                      run.ws.numel(), scalar_table=run.table, table_t0=1, n_table=run.n_table,
+                                      chain_dev=run.chain)
+        Z.zero_shard_step_commit(run.shards, run.flat, dt, 0.0, stats, 0.0, 0, res[k], table_t0=1,
+                                 n_table=run.n_table, chain_dev=run.chain)
+
+    for k in range(5):
+        step(k)
+    torch.cuda.synchronize()
+    osh, oflat, t, So, results = oracle_run(p, flat, dt, h, S, grads[:5])
+    rg = [Z.read_result(res[k]) for k in range(5)]
+    assert [r.applied for r in rg] == [r.applied for r in results] == [1, 0, 1, 1, 1]
+    assert all(r.path == 3 and r.status == 0 for r in rg)
+    assert all(a.grad_mult == b.grad_mult for a, b in zip(rg, results))
+    c = check(run, p, osh, oflat, True)
+    assert (c.step, c.loss_scale, c.applied, c.skipped, c.failed) == (t, So, 4, 1, 0)
+    # four steps applied: t = 5; a table of steps 1..4 does not cover it
+    assert c.step == 5
+    run.n_table = 4
+    before_flat = t2u16(run.flat)
+    c5, s5 = run.state()
+    step(5)
+    torch.cuda.synchronize()
+    r = Z.read_result(res[5])
+    c6, s6 = run.state()
+    assert r.applied == 0 and r.status == Z.ZERO_ELIMIT
+    assert (c6.step, c6.cur, c6.applied, c6.failed) == (c5.step, c5.cur, c5.applied, 1)
+    assert np.array_equal(t2u16(run.flat), before_flat)
+    for a, b in zip(s5, s6):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

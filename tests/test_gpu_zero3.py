@@ -362,3 +362,112 @@ def test_prefetch_schedule_gives_every_consumer_its_own_unit(Z):
     assert int(status.item()) == 0
     for i, u in enumerate(order):
         assert np.array_equal(t2u16(snaps[i]), orc.gather_segments([h.copy() for h in host[u]])), (i, u)
+
+
+def _fused_pipeline_problem(seed, units, nd, dt, steps, S):
+    """Rank shards of a ZeRO-3 group (every rank's part of every unit) and, per
+    step, every rank's full-unit gradient buckets, as host bit patterns."""
+    parts = [u // nd for u in units]
+    g = W.generator(seed, "cpu")
+    shards = []
+    for r in range(nd):
+        x = torch.zeros(sum(parts), dtype=TDT[dt])
+        W.fill_normal_(x, 0.02, g)
+        shards.append(t2u16(x))
+    gens = [W.generator(seed + 1 + r, "cpu") for r in range(nd)]
+    buckets = []
+    for _ in range(steps):
+        step = []
+        for U in units:
+            row = []
+            for r in range(nd):
+                b = torch.zeros(U, dtype=TDT[dt])
+                W.fill_normal_(b, 1e-2, gens[r], S)
+                row.append(t2u16(b))
+            step.append(row)
+        buckets.append(step)
+    return parts, shards, buckets
+
+
+def _owner_slices(buckets_step, parts, nd, me):
+    """Rank r's gradient over the owner's concatenated shard: its bucket of
+    every unit, cut to the owner's part -- what the oracle reduces."""
+    return [np.concatenate([buckets_step[u][r][me * p:(me + 1) * p] for u, p in enumerate(parts)]) for r in range(nd)]
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+def test_fused_unit_passes_then_commit_match_the_oracle(Z, dt):
+    """ZeRO-3 without clipping, fused per unit: after each unit's backward its
+    buckets are reduced onto rank 1's part and that part is updated in the
+    same pass (zero_shard_step_partial, speculatively, into the second state
+    set), and the step is decided after the last unit (zero_shard_step_commit).
+    Three steps, the second with +inf in one rank's bucket of the middle unit:
+    skipped everywhere, the parameters restored, t kept, S halved.  Bit-exact
+    against the oracle's step over the concatenated shard."""
+    nd, me, steps = 4, 1, 3
+    units = [4096 * 4, 10001 * 4, 333 * 4, 7 * 4]
+    S = 256.0 if dt == 1 else 1.0
+    parts, shards, buckets = _fused_pipeline_problem(40 + dt, units, nd, dt, steps, S)
+    buckets[1][1][2] = buckets[1][1][2].copy()
+    buckets[1][1][2][me * parts[1] + 17] = 0x7C00 if dt == 1 else 0x7F80
+    uoff = [sum(parts[:i]) for i in range(len(parts))]
+    L = sum(parts)
+    param = dev16(shards[me], dt)
+    sets = [[torch.from_numpy(orc.widen_16(shards[me], dt)).to(DEV), torch.zeros(L, device=DEV),
+             torch.zeros(L, device=DEV)], [torch.empty(L, device=DEV) for _ in range(3)]]
+    wsb = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    h = hyper32()
+    o = dict(numel=L, grad_off=0, param_off=0, master=orc.widen_16(shards[me], dt), m=np.zeros(L, np.float32),
+             v=np.zeros(L, np.float32))
+    o_param = shards[me].copy()
+    cur, t, So = 0, 1, S
+    applied = []
+    for k in range(steps):
+        A, B = sets[cur], sets[1 - cur]
+        hy = Z.hyper(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], 0.0, t)
+        for i, u in enumerate(reversed(range(len(units)))):
+            part = Z.shard(parts[u], me * parts[u], uoff[u], *(x[uoff[u]:uoff[u] + parts[u]] for x in A),
+                           *(x[uoff[u]:uoff[u] + parts[u]] for x in B))
+            Z.zero_shard_step_partial([dev16(b, dt) for b in buckets[k][u]], dt, [part], param, dt, hy, So, i > 0,
+                                      stats, wsb, wsb.numel())
+        whole = [Z.shard(L, 0, 0, *A, *B)]
+        Z.zero_shard_step_commit(whole, param, dt, So, stats, 0.0, 0, res)
+        torch.cuda.synchronize()
+        rg = Z.read_result(res)
+        ro, _ = orc.zero_step(_owner_slices(buckets[k], parts, nd, me), dt, [o], o_param, dt, h, t, np.float32(So))
+        assert (rg.overflow, rg.applied, rg.path, rg.status) == (ro.overflow, ro.applied, 3, 0)
+        assert rg.grad_mult == ro.grad_mult
+        if ro.applied:
+            assert rg.sumsq == pytest.approx(ro.sumsq, rel=1e-9)
+            cur ^= 1
+            t += 1
+        else:
+            So /= 2
+        applied.append(rg.applied)
+        assert np.array_equal(t2u16(param), o_param)
+        for x, ref in zip(sets[cur], (o["master"], o["m"], o["v"])):
+            assert np.array_equal(x.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert applied == [1, 0, 1]
+
+
+def test_partial_pass_argument_errors(Z):
+    n = 4096
+    g = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+    st = [torch.zeros(n, device=DEV) for _ in range(6)]
+    flat = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+    wsb = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    two = [Z.shard(n, 0, 0, *st)]
+    for sh, hy, s_, code in (([Z.shard(n, 0, 0, *st[:3])], Z.hyper(), stats, Z.ZERO_EINVAL),     # in place
+                             (two, Z.hyper(max_grad_norm=1.0), stats, Z.ZERO_EINVAL),            # clipping
+                             (two, Z.hyper(), 0, Z.ZERO_EINVAL),                                  # no stats
+                             (two, Z.hyper(step=0), stats, Z.ZERO_EINVAL)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_step_partial([g], Z.ZERO_BF16, sh, flat, Z.ZERO_BF16, hy, 1.0, 0, s_, wsb, wsb.numel())
+        assert e.value.code == code
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_shard_step_commit(two, flat, Z.ZERO_BF16, 1.0, stats, 0.0, 0, res[4:])
+    assert e.value.code == Z.ZERO_EINVAL

@@ -93,6 +93,9 @@ _SIGS = {
                                      ctypes.c_size_t, _P, _P]),
     "zero_shard_apply_chained": (_I, [_P, _I, _I, _P, _I, _P, _P, _I64, _I64, _P, _P, ctypes.c_double, _I, _P,
                                       ctypes.c_size_t, _P, _P]),
+    "zero_shard_step_partial": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, _P, _I64, _I64, _P, _I, _P, _P,
+                                     ctypes.c_size_t, _P]),
+    "zero_shard_step_commit": (_I, [_P, _I, _P, _I, ctypes.c_float, _I64, _I64, _P, _P, ctypes.c_double, _I, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 # every symbol include/zero.h declares
@@ -316,6 +319,30 @@ def zero_shard_apply_chained(shards, grad_dtype, flat_param, param_dtype, hyper,
                                         ctypes.byref(hyper), _ptr(scalar_table), int(table_t0), int(n_table),
                                         _ptr(chain_dev), _ptr(stats), extra_sumsq, int(extra_overflow),
                                         _ptr(workspace), workspace_bytes, _ptr(result), _stream(stream)))
+
+
+def zero_shard_step_partial(grad_slices, grad_dtype, shards, flat_param, param_dtype, hyper, loss_scale, accumulate,
+                            stats, workspace, workspace_bytes, scalar_table=None, table_t0=1, n_table=0,
+                            chain_dev=None, stream=None):
+    """A fused pass over some shards of a step, adding their statistics to
+    stats; the step is decided later by zero_shard_step_commit.  With
+    chain_dev, t, S and the state set in use come from the device chain."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_step_partial(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards),
+                                       _ptr(flat_param), param_dtype, ctypes.byref(hyper), loss_scale,
+                                       _ptr(scalar_table), int(table_t0), int(n_table), _ptr(chain_dev),
+                                       int(accumulate), _ptr(stats), _ptr(workspace), workspace_bytes,
+                                       _stream(stream)))
+
+
+def zero_shard_step_commit(shards, flat_param, param_dtype, loss_scale, stats, extra_sumsq, extra_overflow, result,
+                           table_t0=1, n_table=0, chain_dev=None, stream=None):
+    """The decision of a step made of partial fused passes: the result from
+    their statistics, the parameters restored on a skip, the chain updated."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_step_commit(sh, len(shards), _ptr(flat_param), param_dtype, loss_scale, int(table_t0),
+                                      int(n_table), _ptr(chain_dev), _ptr(stats), extra_sumsq, int(extra_overflow),
+                                      _ptr(result), _stream(stream)))
 
 
 def read_result(t) -> zero_result:

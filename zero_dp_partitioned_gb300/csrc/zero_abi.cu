@@ -593,6 +593,109 @@ int zero_shard_apply_chained(const zero_shard* shards, int n_shards, int grad_dt
     return launch_chain_update(chain, result, s);
 }
 
+// The step's scalars from the chain (t, S, the state set) when there is one,
+// else from hyper->step and loss_scale; checks shared by the partial pass and
+// the commit.
+static int step_source(StepArgs& a, const zero_hyper* hyper, float loss_scale, const float* scalar_table,
+                       int64_t table_t0, int64_t n_table, zero_chain* chain) {
+    if (!hyper) return fail(ZERO_EINVAL, "hyper is NULL");
+    if (chain) {
+        if (!aligned(chain, 8)) return fail(ZERO_EINVAL, "chain is not 8-byte aligned");
+        if (!scalar_table || !aligned(scalar_table, 4) || n_table < 1 || table_t0 < 1)
+            return fail(ZERO_EINVAL, "scalar_table is NULL or misaligned, or n_table / table_t0 < 1");
+        zero_hyper h1 = *hyper;
+        h1.step = 1;
+        a.sc = adam_scalars(h1);          // t-independent scalars; ss and rb2 come from the table
+        a.chain = chain;
+        a.sc_table = scalar_table;
+        a.t0 = table_t0;
+        a.n_table = n_table;
+        return ZERO_OK;
+    }
+    int rc;
+    if ((rc = check_hyper(hyper, loss_scale)) != ZERO_OK) return rc;
+    a.sc = adam_scalars(*hyper);
+    a.loss_scale = (double)loss_scale;
+    a.k = (float)(1.0 / (double)loss_scale);
+    return ZERO_OK;
+}
+
+static bool state_in_place(const zero_shard* shards, int n_shards) {
+    for (int i = 0; i < n_shards && shards; ++i)
+        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
+                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
+            return true;
+    return false;
+}
+
+int zero_shard_step_partial(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,
+                            int n_shards, void* flat_param, int param_dtype, const zero_hyper* hyper,
+                            float loss_scale, const float* scalar_table, int64_t table_t0, int64_t n_table,
+                            zero_chain* chain, int accumulate, zero_stats* stats, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (!stats || !aligned(stats, 8)) return fail(ZERO_EINVAL, "stats is NULL or not 8-byte aligned");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    int rc;
+    if ((rc = step_source(a, hyper, loss_scale, scalar_table, table_t0, n_table, chain)) != ZERO_OK) return rc;
+    if (hyper->max_grad_norm > 0.0f)
+        return fail(ZERO_EINVAL, "zero_shard_step_partial: clipping needs the global norm before any update; "
+                                 "use zero_shard_reduce and zero_shard_apply");
+    if (state_in_place(shards, n_shards))
+        return fail(ZERO_EINVAL, "zero_shard_step_partial: a shard updates its state in place; give two sets");
+    if ((rc = pack_slices(a, grad_slices, n_slices)) != ZERO_OK) return rc;
+    if ((rc = check_workspace(a, workspace, workspace_bytes)) != ZERO_OK) return rc;
+    if ((rc = pack_shards(a, shards, n_shards, 1)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = flat_param;
+    a.stats = stats;
+    a.accumulate = accumulate ? 1 : 0;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int vec = vec8_ok(a, 1) ? 8 : 1;
+    number_tiles(a, vec, HEAD_GRADS);
+    const void* f = chain ? fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices))
+                          : fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices));
+    const int grid = grid_for(f, a.n_tiles, n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+    return launch_fused_early(a, grad_dtype, param_dtype, vec, grid, s);
+}
+
+int zero_shard_step_commit(const zero_shard* shards, int n_shards, void* flat_param, int param_dtype,
+                           float loss_scale, int64_t table_t0, int64_t n_table, zero_chain* chain,
+                           const zero_stats* stats, double extra_sumsq, int extra_overflow, zero_result* result,
+                           void* stream) {
+    if (!valid_dtype(param_dtype)) return fail(ZERO_EINVAL, "unknown dtype");
+    if (!stats || !aligned(stats, 8)) return fail(ZERO_EINVAL, "stats is NULL or not 8-byte aligned");
+    if (!result || !aligned(result, 8)) return fail(ZERO_EINVAL, "result is NULL or not 8-byte aligned");
+    if (chain && !aligned(chain, 8)) return fail(ZERO_EINVAL, "chain is not 8-byte aligned");
+    if (chain && (n_table < 1 || table_t0 < 1)) return fail(ZERO_EINVAL, "n_table / table_t0 < 1");
+    if (!chain && (!(loss_scale > 0.0f) || !std::isfinite(loss_scale)))
+        return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    int rc;
+    if ((rc = pack_shards(a, shards, n_shards, 1)) != ZERO_OK) return rc;
+    if (any_elements(a) && (!flat_param || !aligned(flat_param, 2)))
+        return fail(ZERO_EINVAL, "flat_param is NULL or not 2-byte aligned");
+    a.flat_param = flat_param;
+    a.stats = const_cast<zero_stats*>(stats);
+    a.extra_sumsq = extra_sumsq;
+    a.extra_overflow = extra_overflow ? 1 : 0;
+    a.result = result;
+    a.chain = chain;
+    a.loss_scale = (double)loss_scale;
+    a.k = chain ? 0.0f : (float)(1.0 / (double)loss_scale);
+    // a chained step whose t lies outside the partial passes' scalar table was
+    // skipped by them: the commit reports it (ZERO_ELIMIT) rather than apply it
+    a.t0 = table_t0;
+    a.n_table = n_table;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = launch_commit(a, s)) != ZERO_OK) return rc;
+    if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
+    return chain ? launch_chain_update(chain, result, s) : ZERO_OK;
+}
+
 // The register-staged gather's arguments for n pieces laid end to end in out
 // (pointers and lengths already validated); returns the vector width.
 static int gather_args(const void* const* src, const int64_t* len, int n, void* out, GatherArgs& g) {

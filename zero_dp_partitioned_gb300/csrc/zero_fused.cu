@@ -84,6 +84,41 @@ int launch_init(const StepArgs& a, int pdt, cudaStream_t s) {
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "init launch");
 }
 
+// ---------------------------------------------------------------- K1d: the decision after partial fused passes
+// A step whose shards were updated by partial fused passes (each adding its
+// statistics to *a.stats) is decided here, from every pass's statistics and
+// the other ranks' share: skip on overflow (k_recover, launched next,
+// restores the parameters), or commit (the caller or the chain keeps the
+// written state set).  One thread.
+__global__ void k_commit(const __grid_constant__ StepArgs a) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const zero_stats st = *a.stats;
+    const double S = step_S(a);
+    zero_result r;
+    r.overflow = (st.overflow | a.extra_overflow) ? 1 : 0;
+    r.status = (a.chain && step_bad(a)) ? ZERO_ELIMIT : 0;
+    r.applied = (r.overflow || r.status) ? 0 : 1;
+    r.path = 3;
+    r.sumsq = st.sumsq + a.extra_sumsq;
+    r.grad_norm = sqrt(r.sumsq) / S;
+    r.clip_coef = 1.0;
+    r.grad_mult = a.chain ? (float)(1.0 / S) : a.k;
+    r.reserved = 0.0f;
+    *a.result = r;
+}
+
+int launch_commit(const StepArgs& a, cudaStream_t s) {
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(cudaLaunchKernel((const void*)k_commit, dim3(1), dim3(32), args, 0, s), "commit launch");
+}
+
+int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s) {
+    const int ns = fused_ns(a.n_slices);
+    const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec, ns) : fused_kernel(gdt, pdt, vec, ns);
+    void* args[] = {const_cast<StepArgs*>(&a)};
+    return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, 0, s), "partial fused pass launch");
+}
+
 // ---------------------------------------------------------------- chained steps: the bookkeeping
 // After a chained step's kernels: applied -> next t, the other state set;
 // overflow -> half the loss scale, unless that would take it below the

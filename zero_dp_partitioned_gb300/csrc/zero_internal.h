@@ -49,6 +49,10 @@ int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStr
 int launch_recover(const StepArgs& a, int pdt, cudaStream_t s);
 int launch_init(const StepArgs& a, int pdt, cudaStream_t s);
 int launch_chain_update(zero_chain* chain, const zero_result* result, cudaStream_t s);
+int launch_commit(const StepArgs& a, cudaStream_t s);
+// The fused pass launched early (programmatic stream serialisation): for the
+// partial passes, which run back to back, one per ZeRO-3 unit.
+int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s);
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s);
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s);
 int launch_gather(const GatherArgs& a, int vec, cudaStream_t s, int max_grid = 0);

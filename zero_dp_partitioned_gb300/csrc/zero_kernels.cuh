@@ -482,6 +482,8 @@ template <int GDT, int PDT, int VEC, int NS, bool CHAIN = false>
 __global__ void __launch_bounds__(TILE_THREADS, NS == 0 ? (CHAIN ? 3 : 4) : 2)   // chained: 3, so no spills
 k_step_fused(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
+    pdl_wait();             // a no-op unless launched early (partial passes, one per ZeRO-3 unit)
+    pdl_launch_next();
     SumSq sumsq;
     int ovf = 0;
     uint16_t* P = static_cast<uint16_t*>(a.flat_param);
@@ -540,7 +542,13 @@ k_step_fused(const __grid_constant__ StepArgs a) {
     double sum;
     int flag;
     combine_partials(a, sum, flag);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && a.stats) {
+        // a partial pass: its statistics join the step's, decided later by k_commit
+        zero_stats st = a.accumulate ? *a.stats : zero_stats{0.0, 0, 0};
+        st.sumsq += sum;
+        st.overflow |= flag;
+        *a.stats = st;
+    } else if (threadIdx.x == 0) {
         zero_result r;
         r.overflow = (flag | a.extra_overflow) ? 1 : 0;
         r.status = (CHAIN && step_bad(a)) ? ZERO_ELIMIT : 0;
