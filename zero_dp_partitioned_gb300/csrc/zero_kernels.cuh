@@ -355,7 +355,24 @@ __device__ __forceinline__ void reduce8(const StepArgs& a, int64_t off, float (&
 #pragma unroll
             for (int q = 0; q < 8; ++q) add8<GDT>(s, w[q]);
         }
-        for (; r < n; ++r) add8<GDT>(s, ld_ro(static_cast<const uint16_t*>(a.slices[r]) + off));
+        if (NS < 0) {
+            // The few-slice loop (up to 128 registers): the last n - r < 8
+            // slices too with every load issued before the first add.  One at
+            // a time, a slice's load would wait for the previous slice's add:
+            // with 4 slices (a ZeRO-3 unit pass) that is every slice.
+            const int rem = n - r;
+            if (rem > 0) {
+                uint4 w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < rem) w[q] = ld_ro(static_cast<const uint16_t*>(a.slices[r + q]) + off);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < rem) add8<GDT>(s, w[q]);
+            }
+        } else {
+            for (; r < n; ++r) add8<GDT>(s, ld_ro(static_cast<const uint16_t*>(a.slices[r]) + off));
+        }
     }
 }
 
