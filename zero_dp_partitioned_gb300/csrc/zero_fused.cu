@@ -6,6 +6,7 @@ namespace zdp {
 
 template <int G, int P, int V>
 static const void* fused_ptr(int ns) {
+    if (ns == 4) return (const void*)k_step_fused<G, P, V, 4>;
     return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW> : (const void*)k_step_fused<G, P, V, 0>;
 }
 
@@ -24,6 +25,7 @@ const void* fused_kernel(int gdt, int pdt, int vec, int ns) {
 // bookkeeping (t, S and the state set read from the chain).
 template <int G, int P, int V>
 static const void* fused_chain_ptr_v(int ns) {
+    if (ns == 4) return (const void*)k_step_fused<G, P, V, 4, true>;
     return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW, true> : (const void*)k_step_fused<G, P, V, 0, true>;
 }
 

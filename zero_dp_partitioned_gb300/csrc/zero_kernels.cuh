@@ -488,11 +488,13 @@ __device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d,
 // parameters are restored by k_recover on overflow.
 // NS: 0 = the generic slice loop for many slices, 4 blocks per SM (at most
 // 64 registers; chained steps 3, at most 85); NS_FEW = the same loop for at
-// most FEW_SLICES slices, 2
-// blocks per SM (up to 128 registers: every load of a vector is in flight
-// at once).  Measured on the GPT-2 step (8 slices): 9.51 ms with NS_FEW,
-// against 9.72 ms for the loop unrolled for exactly 8 slices and 10.77 ms
-// for the 64-register loop.
+// most FEW_SLICES slices, 2 blocks per SM (up to 128 registers: every load of
+// a vector is in flight at once); NS = 4 = the loop unrolled for exactly 4
+// slices, 2 blocks per SM.  Measured on the GPT-2 step (8 slices): 9.51 ms
+// with NS_FEW, against 9.72 ms for the loop unrolled for exactly 8 slices at
+// 64 registers and 10.77 ms for the 64-register generic loop; on the ZeRO-3
+// unit passes (4 slices): 0.3130 ms with NS = 4 against 0.3200 ms with
+// NS_FEW, and 0.341 ms with NS = 4 at 3 blocks per SM.
 // CHAIN: a chained step (t, S and the state set from a.chain); the other
 // instantiations take everything from their arguments.
 template <int GDT, int PDT, int VEC, int NS, bool CHAIN = false>
