@@ -68,6 +68,38 @@ int grid_for(const void* func, int64_t n_tiles, int max_per_sm) {
     return grid_for_smem(func, n_tiles, 0, max_per_sm);
 }
 
+size_t smem_capping(const void* func, int blocks) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void*, int>, size_t> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> g(mu);
+    const auto key = std::make_tuple(dev, func, blocks);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    size_t smem = 0;
+    int occ = 0, per_sm = 0, reserved = 0, optin = 0;
+    bool refused = false;
+    if (blocks > 0) {
+        refused = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, func, TILE_THREADS, 0) != cudaSuccess ||
+                  cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+                  cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+                  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess;
+        // the smallest multiple of 16 bytes beside which a (blocks + 1)-th block no longer fits
+        const long want = ((long)per_sm / (blocks + 1) - reserved + 16 + 15) / 16 * 16;
+        if (!refused && occ > blocks && want > 0 && want <= optin) {
+            int got = 0;
+            refused = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)want) != cudaSuccess ||
+                      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&got, func, TILE_THREADS, (size_t)want) !=
+                          cudaSuccess;
+            if (!refused && got == blocks) smem = (size_t)want;
+        }
+    }
+    if (refused) cudaGetLastError();   // a refusal costs only the cap: leave no error for a later launch check
+    cache[key] = smem;
+    return smem;
+}
+
 // Tries per bounded wait of the TMA gather, from the environment (tests force
 // a limit of 0 to exercise the timeout path without hanging anything).
 static unsigned spin_limit() {
@@ -657,8 +689,10 @@ int zero_shard_step_partial(const void* const* grad_slices, int n_slices, int gr
     number_tiles(a, vec, HEAD_GRADS);
     const void* f = chain ? fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices))
                           : fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices));
-    const int grid = grid_for(f, a.n_tiles, n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
-    return launch_fused_early(a, grad_dtype, param_dtype, vec, grid, s);
+    const int bps = n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY;
+    const size_t smem = smem_capping(f, bps);
+    const int grid = grid_for_smem(f, a.n_tiles, smem, bps);
+    return launch_fused_early(a, grad_dtype, param_dtype, vec, grid, smem, s);
 }
 
 int zero_shard_step_commit(const zero_shard* shards, int n_shards, void* flat_param, int param_dtype,

@@ -114,11 +114,11 @@ int launch_commit(const StepArgs& a, cudaStream_t s) {
     return cuda_fail(cudaLaunchKernel((const void*)k_commit, dim3(1), dim3(32), args, 0, s), "commit launch");
 }
 
-int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s) {
+int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, size_t smem, cudaStream_t s) {
     const int ns = fused_ns(a.n_slices);
     const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec, ns) : fused_kernel(gdt, pdt, vec, ns);
     void* args[] = {const_cast<StepArgs*>(&a)};
-    return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, 0, s), "partial fused pass launch");
+    return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, smem, s), "partial fused pass launch");
 }
 
 // ---------------------------------------------------------------- chained steps: the bookkeeping

@@ -39,6 +39,14 @@ constexpr int BPS_RECOVER = 0;
 int grid_for(const void* func, int64_t n_tiles, int max_per_sm = 0);
 int grid_for_smem(const void* func, int64_t n_tiles, size_t dynamic_smem, int max_per_sm = 0);
 
+// Dynamic shared memory for `func` (256-thread blocks) that leaves room for
+// at most `blocks` resident blocks per SM, the kernel's limit raised to it;
+// 0 when its registers already allow no more or the device refuses.  A grid
+// of `blocks` per SM launched early, while the previous pass still runs,
+// would otherwise let the next pass's blocks take the free slots first and
+// settle three to an SM on some SMs and one on others.
+size_t smem_capping(const void* func, int blocks);
+
 // Launch of a kernel that starts with pdl_wait() (the gathers and the
 // reduce), allowed to begin while the previous kernel of the stream finishes.
 cudaError_t launch_after_previous(const void* f, int grid, int block, void** args, size_t smem, cudaStream_t s);
@@ -52,7 +60,7 @@ int launch_chain_update(zero_chain* chain, const zero_result* result, cudaStream
 int launch_commit(const StepArgs& a, cudaStream_t s);
 // The fused pass launched early (programmatic stream serialisation): for the
 // partial passes, which run back to back, one per ZeRO-3 unit.
-int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s);
+int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, size_t smem, cudaStream_t s);
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s);
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s);
 int launch_gather(const GatherArgs& a, int vec, cudaStream_t s, int max_grid = 0);
