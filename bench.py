@@ -241,9 +241,6 @@ def _check_chain(Z, chain):
     return check
 
 
-
-
-
 def _pin_copies(torch, bufs, e2e):
     """Pinned host copies of a step's input buffers for the end-to-end run.
     Every rank of the job pins at the same time, so the check is on the job's
