@@ -218,6 +218,7 @@ def _finish_step(Z, torch, res, res_h, st):
 
 
 E2E_SOURCE = {"mode": None}
+HOST_RING_BYTES = 512 << 20      # device ring of zero_shard_step_host in the end-to-end runs
 
 
 def _device_chain(Z, torch, dev, wl, n_table=1 << 16):
@@ -325,95 +326,57 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
             if c.failed:
                 raise RuntimeError(f"{c.failed} chained steps failed (status != 0)")
             st.update(cur=c.cur, t=c.step, S=c.loss_scale, chained=False)
-    # End to end, the next step's gradients cross the host link on a copy
-    # stream into a second device set while this step computes, and the
-    # step's product -- the updated 16-bit flat parameters, the all-gather
-    # destination -- goes back to pinned host memory on a third stream, beside
-    # the next upload (the link carries both directions at once).
-    host = dict(sets=[grads], copy=None, copied=None, consumed=None, i=0, pending=None, params=None)
+    # End to end, the step takes its gradients from pinned host memory and
+    # returns its product -- the updated 16-bit flat parameters, the
+    # all-gather destination -- there: zero_shard_step_host copies the slices
+    # up chunk by chunk into a device ring while the chunks already up are
+    # reduced and updated, and copies each chunk's parameters down beside the
+    # uploads (the link carries both directions at once).
+    host = dict(params=None, staging=None)
     if pinned is not None:
-        host["sets"].append([torch.empty_like(g) for g in grads])
-        host["copy"] = torch.cuda.Stream(device=dev)
-        host["copied"] = [torch.cuda.Event(), torch.cuda.Event()]
-        host["consumed"] = [torch.cuda.Event(), torch.cuda.Event()]
+        host["staging"] = torch.empty(HOST_RING_BYTES // 2, dtype=torch.int16, device=dev)
         if mem_available_bytes() > flat.numel() * flat.element_size() + (16 << 30):
             host["params"] = torch.empty(flat.shape, dtype=flat.dtype, pin_memory=True)
-            host["fetch"] = torch.cuda.Stream(device=dev)
-            host["stepped"] = torch.cuda.Event()
-            host["fetched"] = torch.cuda.Event()
         else:
             log("[bench] not enough host memory for the parameter download of the end-to-end run")
 
-    def upload(b):
-        """This step's-to-be gradients into device set b, on the copy stream,
-        after the last step that read set b."""
-        cs = host["copy"]
-        cs.wait_event(host["consumed"][b])
-        with torch.cuda.stream(cs):
-            for g, hp in zip(host["sets"][b], pinned):
-                g.copy_(hp, non_blocking=True)
-        host["copied"][b].record(cs)
-        host["pending"] = b
-
     def step(from_host=False):
-        main = torch.cuda.current_stream()
         if not from_host and st["chained"]:
             with timer("fused pass+k_recover"):
                 Z.zero_shard_step_chained(grads, Z.ZERO_BF16, variants[0], flat, Z.ZERO_BF16, hy, table, 1, n_table,
                                           chain_dev, 0.0, 0, ws, ws.numel(), res)
             return
         host_from_chain()
-        b = 0
+        h = _hyper(Z, wl.hyper, st["t"])
         if from_host:
-            b = host["i"] % 2
-            if host["pending"] != b:
-                upload(b)
-            main.wait_event(host["copied"][b])
-            if host["params"] is not None:
-                main.wait_event(host["fetched"])    # the last step's parameters have left before they are rewritten
-        with timer("fused pass+k_recover"):
-            Z.zero_shard_step(host["sets"][b], Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16,
-                              _hyper(Z, wl.hyper, st["t"]), st["S"], 0.0, 0, ws, ws.numel(), res)
-        if from_host:
-            host["consumed"][b].record(main)
-            if host["params"] is not None:
-                host["stepped"].record(main)
-                host["fetch"].wait_event(host["stepped"])
-                with torch.cuda.stream(host["fetch"]):
-                    host["params"].copy_(flat, non_blocking=True)
-                host["fetched"].record(host["fetch"])
-            host["i"] += 1
-            upload(1 - b)              # the next step's gradients, under this step's compute
+            Z.zero_shard_step_host(pinned, Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16, host["params"], h,
+                                   st["S"], 0.0, 0, host["staging"], HOST_RING_BYTES, ws, ws.numel(), res)
+        else:
+            with timer("fused pass+k_recover"):
+                Z.zero_shard_step(grads, Z.ZERO_BF16, variants[st["cur"]], flat, Z.ZERO_BF16, h, st["S"], 0.0, 0,
+                                  ws, ws.numel(), res)
         _finish_step(Z, torch, res, res_h, st)
-
-    def e2e_drain():
-        """The upload in flight for the step after the last belongs to the
-        timed region too (one upload per step), and so does the last step's
-        parameter download."""
-        if host["pending"] is not None:
-            torch.cuda.current_stream().wait_event(host["copied"][host["pending"]])
-        if host["params"] is not None:
-            torch.cuda.current_stream().wait_event(host["fetched"])
 
     def path_of_last_step():
         return Z.read_result(res).path
 
     def e2e_parts():
         """The host link alone, timed like the end-to-end steps: one step's
-        gradient upload, one parameter download, and both at once on their two
+        gradient upload, one parameter download, and both at once on two
         streams (what the end-to-end steps overlap)."""
         out = {}
         if host["params"] is None:
             return out
         main = torch.cuda.current_stream()
+        lanes = {"up": torch.cuda.Stream(device=dev), "down": torch.cuda.Stream(device=dev)}
 
         def up():
-            with torch.cuda.stream(host["copy"]):
-                for g, hp in zip(host["sets"][0], pinned):
+            with torch.cuda.stream(lanes["up"]):
+                for g, hp in zip(grads, pinned):
                     g.copy_(hp, non_blocking=True)
 
         def down():
-            with torch.cuda.stream(host["fetch"]):
+            with torch.cuda.stream(lanes["down"]):
                 host["params"].copy_(flat, non_blocking=True)
 
         times = {"upload_ms": [], "download_ms": [], "both_ms": []}
@@ -422,11 +385,11 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
                 torch.cuda.synchronize()
                 a = torch.cuda.Event(enable_timing=True)
                 a.record(main)
-                for st_ in (host["copy"], host["fetch"]):
+                for st_ in lanes.values():
                     st_.wait_event(a)
                 for f in fns:
                     f()
-                for st_ in (host["copy"], host["fetch"]):
+                for st_ in lanes.values():
                     main.wait_stream(st_)
                 b = torch.cuda.Event(enable_timing=True)
                 b.record(main)
@@ -447,11 +410,12 @@ def gpt2_all_ranks(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
                 h2d=sum(g.numel() * 2 for g in grads) if pinned else None,
                 d2h=(flat.numel() * flat.element_size() if host["params"] is not None else 0) + 48,
                 e2e_ok=pinned is not None,
-                e2e_drain=e2e_drain, e2e_parts=e2e_parts,
-                e2e_note="each step's gradients are copied from pinned host memory on a copy stream into one of two "
-                         "device sets while the previous step computes, and each step's updated 16-bit flat "
-                         "parameters are copied to pinned host memory on a third stream; the timed region holds one "
-                         "upload, one parameter download and one result read per step",
+                e2e_parts=e2e_parts,
+                e2e_note="zero_shard_step_host: each step's gradients are copied from pinned host memory in chunks "
+                         f"into a {HOST_RING_BYTES >> 20} MiB device ring while the chunks already up are reduced and "
+                         "updated (partial fused passes, one commit), and each chunk's updated 16-bit parameters are "
+                         "copied to pinned host memory beside the uploads; the timed region holds one upload, one "
+                         "parameter download and one result read per step",
                 config={"workload": gpt2_desc(name, layers),
                         "psi": P, "n_d": nd, "shard_elements": plan["rank_numels"][0], "grad_dtype": "bf16",
                         "param_dtype": "bf16", "state": "f32 master/m/v, ping-pong", "path": "fused single pass",
@@ -620,22 +584,28 @@ def llama_rank_local(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
     pinned = _pin_copies(torch, slices, e2e)
+    staging = torch.empty(HOST_RING_BYTES // 2, dtype=torch.int16, device=dev) if pinned else None
     hy, table, n_table, chain = _device_chain(Z, torch, dev, wl)
 
     def step(from_host=False):
         # chained: t, S and the bookkeeping on the device (the apply pass, then
-        # a one-thread update of the chain); end to end, the result is read
-        # back every step
+        # a one-thread update of the chain); end to end, zero_shard_step_host
+        # from the pinned slices, its result read back every step (the host
+        # takes the bookkeeping over from the chain)
         if from_host:
-            for g, hp in zip(slices, pinned):
-                g.copy_(hp, non_blocking=True)
+            if "host" not in st:
+                c = Z.read_chain(chain)
+                st.update(host=True, t=c.step, S=c.loss_scale)
+            Z.zero_shard_step_host(pinned, Z.ZERO_BF16, sh, flat, Z.ZERO_BF16, None,
+                                   _hyper(Z, wl.hyper, st["t"], wl.max_grad_norm), st["S"], extra, 0, staging,
+                                   HOST_RING_BYTES, ws, ws.numel(), res)
+            _finish_step(Z, torch, res, res_h, st)
+            return
         with timer("k_reduce"):
             Z.zero_shard_reduce(slices, Z.ZERO_BF16, sh, 0, stats, ws, ws.numel())
         with timer("k_apply"):
             Z.zero_shard_apply_chained(sh, Z.ZERO_BF16, flat, Z.ZERO_BF16, hy, table, 1, n_table, chain, stats,
                                        extra, 0, ws, ws.numel(), res)
-        if from_host:
-            res_h.copy_(res)
 
     def path_of_last_step():
         return Z.read_result(res).path
@@ -679,15 +649,20 @@ def gpt75_rank63(Z, W, torch, dev, e2e, timer, layers=None, vocab=None):
     res_h = torch.zeros(48, dtype=torch.uint8).pin_memory()
     st = dict(cur=0, t=1, S=wl.loss_scale)
     pinned = _pin_copies(torch, slices, e2e)
+    staging = torch.empty(HOST_RING_BYTES // 2, dtype=torch.int16, device=dev) if pinned else None
 
     def step(from_host=False):
         # host-driven (the caller reads zero_result and swaps the state sets):
         # the chained fused pass for 64 slices needs more registers than 4
         # blocks per SM leave it (3 per SM: 2.77 ms a step, against 2.69-2.74
-        # host-driven at 4 per SM)
+        # host-driven at 4 per SM); end to end, zero_shard_step_host from the
+        # pinned slices
         if from_host:
-            for g, hp in zip(slices, pinned):
-                g.copy_(hp, non_blocking=True)
+            Z.zero_shard_step_host(pinned, Z.ZERO_F16, variants[st["cur"]], flat, Z.ZERO_F16, None,
+                                   _hyper(Z, wl.hyper, st["t"]), st["S"], 0.0, 0, staging, HOST_RING_BYTES, ws,
+                                   ws.numel(), res)
+            _finish_step(Z, torch, res, res_h, st)
+            return
         with timer("fused pass+k_recover"):
             Z.zero_shard_step(slices, Z.ZERO_F16, variants[st["cur"]], flat, Z.ZERO_F16, _hyper(Z, wl.hyper, st["t"]),
                               st["S"], 0.0, 0, ws, ws.numel(), res)
@@ -1258,6 +1233,7 @@ def measure(wl, args, world, local, dev, torch, timer, barrier, e2e_on):
         wl["config"].update(wl["extra"](args.steps))
 
     e2e = None
+    timed_path = wl["state"].get("path")
     if e2e_on and wl["e2e_ok"]:
         for _ in range(2):
             step(from_host=True)
@@ -1267,8 +1243,6 @@ def measure(wl, args, world, local, dev, torch, timer, barrier, e2e_on):
         s2.record()
         for _ in range(args.e2e_steps):
             step(from_host=True)
-        if wl.get("e2e_drain"):
-            wl["e2e_drain"]()
         e2.record()
         torch.cuda.synchronize()
         barrier()
@@ -1281,6 +1255,8 @@ def measure(wl, args, world, local, dev, torch, timer, barrier, e2e_on):
             e2e["overlap"] = wl["e2e_note"]
         if wl.get("e2e_parts"):
             e2e["link_alone"] = wl["e2e_parts"]()
+        e2e["update_kernel"] = PATH_NAMES.get(wl["state"].get("path"), "?")
+        wl["state"]["path"] = timed_path          # the line's kernel figures are the device-timed steps'
     return ms, kinds, clocks, e2e
 
 

@@ -29,9 +29,11 @@
  * Conventions for every entry point:
  *  - Device pointers are CUDA device (or managed) addresses on the current
  *    device; host pointers are plain CPU memory.  The caller owns every
- *    buffer; the library allocates nothing (zero_shard_step_noalloc's scratch
- *    is an array compiled into it) and carries no data from one call to the
- *    next (chained steps carry theirs in the caller's zero_chain).
+ *    buffer; the library allocates no memory (zero_shard_step_noalloc's
+ *    scratch is an array compiled into it; zero_shard_step_host creates two
+ *    streams and a few events per device on its first call there) and carries
+ *    no data from one call to the next (chained steps carry theirs in the
+ *    caller's zero_chain).
  *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and is asynchronous: results land in caller memory when
  *    the stream reaches them.  No entry point synchronises.
@@ -560,6 +562,56 @@ int zero_shard_step_commit(const zero_shard* shards, int n_shards, void* flat_pa
                            float loss_scale, int64_t table_t0, int64_t n_table, zero_chain* chain,
                            const zero_stats* stats, double extra_sumsq, int extra_overflow,
                            zero_result* result, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The step from host memory: gradients read from, parameters returned to,
+ * page-locked host buffers.
+ * Source: the DeepSpeed ZeRO stages 1-2 walkthrough, 6 (the step consumes
+ * the ranks' gradients and ends with the updated 16-bit parameters, which
+ * the all-gather hands back to the training loop).  The same step as
+ * zero_shard_step, for a caller whose gradients arrive in host memory and
+ * who wants the updated parameters there.
+ *
+ * The shards are cut into chunks of C elements.  Chunk j's piece of every
+ * slice is copied up (on a stream of the library's) into slot j mod 4 of the
+ * caller's device ring while the step's kernels run on `stream`: without
+ * clipping and with two state sets, one partial fused pass per chunk (as
+ * zero_shard_step_partial) and one commit (as zero_shard_step_commit: path
+ * 3); otherwise one reduce pass per chunk into grad_shard, then the apply
+ * pass (path 2).  After its partial pass each chunk's parameters are copied
+ * down to host_param (on a third stream); a step the commit skips has its
+ * parameters restored in flat_param and in host_param.  After the apply pass
+ * the shards' parameters are copied down on `stream`.
+ *
+ * host_grad_slices[n_slices]  host array of pointers into page-locked host
+ *                             memory (cudaHostAlloc or cudaHostRegister);
+ *                             the layout of zero_shard_step's grad_slices
+ * host_param                  page-locked host memory the device can
+ *                             address, laid out as flat_param: shard s's
+ *                             parameters land at [param_offset_s, + numel_s);
+ *                             NULL = no copy down
+ * staging, staging_bytes      device ring, 16-byte aligned:
+ *                             C = staging_bytes / (4 * n_slices * 2) elements
+ *                             rounded down to a multiple of 64; C >= 64
+ * the rest                    as zero_shard_step (the caller keeps t, S and
+ *                             the state set on the host: read *result)
+ * Every copy and kernel of the call is ordered after the work enqueued on
+ * `stream` before it, and `stream` waits for all of them (the copies down
+ * included) before anything enqueued on it later; the host buffers must not
+ * change until then.  Calls on one device share the library's two streams:
+ * they are serialised on the host, and a ring must not be shared by calls
+ * that are not ordered on the device.
+ * Errors: ZERO_EINVAL (also for a host buffer that is not page-locked),
+ * ZERO_EALIGN, ZERO_EWORKSPACE (also for a ring of fewer than 64 elements per
+ * chunk), ZERO_ELIMIT, before any work is enqueued; ZERO_ECUDA. */
+int zero_shard_step_host(const void* const* host_grad_slices, int n_slices, int grad_dtype,
+                         const zero_shard* shards, int n_shards,
+                         void* flat_param, int param_dtype, void* host_param,
+                         const zero_hyper* hyper, float loss_scale,
+                         double extra_sumsq, int extra_overflow,
+                         void* staging, size_t staging_bytes,
+                         void* workspace, size_t workspace_bytes,
+                         zero_result* result, void* stream);
 
 /* Message of the last error on this thread ("" if none). */
 const char* zero_last_error(void);

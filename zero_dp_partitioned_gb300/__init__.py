@@ -96,6 +96,8 @@ _SIGS = {
     "zero_shard_step_partial": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, ctypes.c_float, _P, _I64, _I64, _P, _I, _P, _P,
                                      ctypes.c_size_t, _P]),
     "zero_shard_step_commit": (_I, [_P, _I, _P, _I, ctypes.c_float, _I64, _I64, _P, _P, ctypes.c_double, _I, _P, _P]),
+    "zero_shard_step_host": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _P, ctypes.c_float, ctypes.c_double, _I, _P,
+                                  ctypes.c_size_t, _P, ctypes.c_size_t, _P, _P]),
     "zero_last_error": (ctypes.c_char_p, []),
 }
 # every symbol include/zero.h declares
@@ -213,6 +215,21 @@ def zero_shard_step(grad_slices, grad_dtype, shards, flat_param, param_dtype, hy
     _check(lib.zero_shard_step(_ptrs(grad_slices), len(grad_slices), grad_dtype, sh, len(shards), _ptr(flat_param),
                                param_dtype, ctypes.byref(hyper), loss_scale, extra_sumsq, int(extra_overflow),
                                _ptr(workspace), workspace_bytes, _ptr(result), _stream(stream)))
+
+
+def zero_shard_step_host(host_grad_slices, grad_dtype, shards, flat_param, param_dtype, host_param, hyper,
+                         loss_scale, extra_sumsq, extra_overflow, staging, staging_bytes, workspace, workspace_bytes,
+                         result, stream=None):
+    """zero_shard_step with the gradients in page-locked host memory and the
+    updated parameters copied back to page-locked host memory (host_param,
+    laid out as flat_param; None = no copy down): the library copies the
+    slices up chunk by chunk into the device ring `staging` while the chunks
+    already up are reduced and updated."""
+    sh = (zero_shard * max(1, len(shards)))(*shards)
+    _check(lib.zero_shard_step_host(_ptrs(host_grad_slices), len(host_grad_slices), grad_dtype, sh, len(shards),
+                                    _ptr(flat_param), param_dtype, _ptr(host_param), ctypes.byref(hyper), loss_scale,
+                                    extra_sumsq, int(extra_overflow), _ptr(staging), staging_bytes, _ptr(workspace),
+                                    workspace_bytes, _ptr(result), _stream(stream)))
 
 
 def zero_shard_step_noalloc(grad_slices, grad_dtype, shards, flat_param, param_dtype, hyper, loss_scale,

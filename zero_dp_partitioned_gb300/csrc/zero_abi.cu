@@ -108,10 +108,10 @@ static unsigned spin_limit() {
     return (unsigned)std::strtoul(e, nullptr, 10);
 }
 
-static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-static bool valid_dtype(int d) { return d == ZERO_F16 || d == ZERO_BF16; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool valid_dtype(int d) { return d == ZERO_F16 || d == ZERO_BF16; }
 
-static int fail(int code, const char* msg) {
+int fail(int code, const char* msg) {
     set_error(msg);
     return code;
 }
@@ -119,7 +119,7 @@ static int fail(int code, const char* msg) {
 // Host scalars of one AdamW step: each computed in fp64 from the fp32
 // hyper-parameters and rounded once to fp32; the bias corrections are folded
 // into ss = lr / (1 - b1^t) and rb2 = 1 / sqrt(1 - b2^t).
-static AdamScalars adam_scalars(const zero_hyper& h) {
+AdamScalars adam_scalars(const zero_hyper& h) {
     const double t = (double)h.step;
     const double bc1 = 1.0 - std::pow((double)h.beta1, t);
     const double bc2 = 1.0 - std::pow((double)h.beta2, t);
@@ -138,7 +138,7 @@ static AdamScalars adam_scalars(const zero_hyper& h) {
 // Common checks of slices and shards; fills the shard part of a and the tile
 // numbering for vector width vec.  need: 1 = fused (state in/out), 2 = reduce
 // (grad_shard out), 3 = apply (grad_shard in, state in/out).
-static int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int need) {
+int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int need) {
     if (n_shards < 0) return fail(ZERO_EINVAL, "n_shards < 0");
     if (n_shards > ZERO_MAX_SHARDS) return fail(ZERO_ELIMIT, "more than ZERO_MAX_SHARDS shards");
     if (n_shards > 0 && !shards) return fail(ZERO_EINVAL, "shards is NULL");
@@ -175,9 +175,6 @@ static int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int 
     return ZERO_OK;
 }
 
-// Which stream a pass's vector loop aligns to 128 bytes: its dominant one.
-enum HeadKind { HEAD_NONE = 0, HEAD_GRADS = 1, HEAD_STATE = 2 };
-
 // Elements done one by one at the start of a shard so that the vector loop
 // starts where the dominant stream sits on a 128-byte boundary.  Shards start
 // wherever the partition puts them (the pages pad only to 2 * world_size
@@ -200,7 +197,7 @@ static int64_t shard_head(const StepArgs& a, const ShardDev& d, int kind) {
     return (h % 8) ? 0 : h;
 }
 
-static void number_tiles(StepArgs& a, int vec, int kind = HEAD_NONE) {
+void number_tiles(StepArgs& a, int vec, int kind) {
     const int64_t tile = (int64_t)TILE_THREADS * vec;
     int64_t t = 0;
     for (int i = 0; i < a.n_shards; ++i) {
@@ -214,7 +211,7 @@ static void number_tiles(StepArgs& a, int vec, int kind = HEAD_NONE) {
     a.n_tiles = t;
 }
 
-static int pack_slices(StepArgs& a, const void* const* slices, int n_slices) {
+int pack_slices(StepArgs& a, const void* const* slices, int n_slices) {
     if (!slices) return fail(ZERO_EINVAL, "grad_slices is NULL");
     if (n_slices < 1) return fail(ZERO_EINVAL, "n_slices < 1");
     if (n_slices > ZERO_MAX_SLICES) return fail(ZERO_ELIMIT, "more than ZERO_MAX_SLICES slices");
@@ -230,7 +227,7 @@ static int pack_slices(StepArgs& a, const void* const* slices, int n_slices) {
 
 // 16-byte vectors are possible when every gradient address a shard starts at
 // and every pointer the vector path loads from are 16-byte aligned.
-static bool vec8_ok(const StepArgs& a, int need) {
+bool vec8_ok(const StepArgs& a, int need) {
     for (int i = 0; i < a.n_shards; ++i) {
         const ShardDev& d = a.shards[i];
         if (d.numel == 0) continue;
@@ -247,7 +244,7 @@ static bool vec8_ok(const StepArgs& a, int need) {
     return true;
 }
 
-static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
+int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
     if (!ws) return fail(ZERO_EWORKSPACE, "workspace is NULL");
     if (ws_bytes < WS_BYTES) return fail(ZERO_EWORKSPACE, "workspace smaller than zero_workspace_bytes()");
     if (!aligned(ws, 16)) return fail(ZERO_EALIGN, "workspace not 16-byte aligned");
@@ -258,16 +255,24 @@ static int check_workspace(StepArgs& a, void* ws, size_t ws_bytes) {
     return ZERO_OK;
 }
 
-static int check_hyper(const zero_hyper* h, float loss_scale) {
+int check_hyper(const zero_hyper* h, float loss_scale) {
     if (!h) return fail(ZERO_EINVAL, "hyper is NULL");
     if (h->step < 1) return fail(ZERO_EINVAL, "hyper->step must be >= 1");
     if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale)) return fail(ZERO_EINVAL, "loss_scale must be finite and > 0");
     return ZERO_OK;
 }
 
-static bool any_elements(const StepArgs& a) {
+bool any_elements(const StepArgs& a) {
     for (int i = 0; i < a.n_shards; ++i)
         if (a.shards[i].numel > 0) return true;
+    return false;
+}
+
+bool state_in_place(const zero_shard* shards, int n_shards) {
+    for (int i = 0; i < n_shards && shards; ++i)
+        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
+                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
+            return true;
     return false;
 }
 
@@ -650,14 +655,6 @@ static int step_source(StepArgs& a, const zero_hyper* hyper, float loss_scale, c
     a.loss_scale = (double)loss_scale;
     a.k = (float)(1.0 / (double)loss_scale);
     return ZERO_OK;
-}
-
-static bool state_in_place(const zero_shard* shards, int n_shards) {
-    for (int i = 0; i < n_shards && shards; ++i)
-        if (shards[i].numel > 0 && (shards[i].master_out == shards[i].master_in ||
-                                    shards[i].m_out == shards[i].m_in || shards[i].v_out == shards[i].v_in))
-            return true;
-    return false;
 }
 
 int zero_shard_step_partial(const void* const* grad_slices, int n_slices, int grad_dtype, const zero_shard* shards,

@@ -61,7 +61,9 @@ int launch_commit(const StepArgs& a, cudaStream_t s);
 // The fused pass launched early (programmatic stream serialisation): for the
 // partial passes, which run back to back, one per ZeRO-3 unit.
 int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, size_t smem, cudaStream_t s);
-int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s);
+// early: launched with programmatic stream serialisation (back-to-back
+// bucket reduces); plain otherwise.
+int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s, bool early = true);
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s);
 int launch_gather(const GatherArgs& a, int vec, cudaStream_t s, int max_grid = 0);
 
@@ -82,6 +84,26 @@ struct BulkGatherArgs {
 };
 size_t gather_bulk_smem(int chunk, int stages);
 int launch_gather_bulk(const BulkGatherArgs& a, int grid, cudaStream_t s);
+
+// Argument checks and kernel-argument packing shared by the entry points
+// (zero_abi.cu); each check sets the thread's error message and returns its
+// code, and none touches the device.
+bool aligned(const void* p, size_t a);
+bool valid_dtype(int d);
+int fail(int code, const char* msg);
+AdamScalars adam_scalars(const zero_hyper& h);
+int check_hyper(const zero_hyper* h, float loss_scale);
+// need: 1 = fused (state in/out), 2 = reduce (grad_shard out), 3 = apply
+// (grad_shard in, state in/out)
+int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int need);
+int pack_slices(StepArgs& a, const void* const* slices, int n_slices);
+int check_workspace(StepArgs& a, void* ws, size_t ws_bytes);
+bool vec8_ok(const StepArgs& a, int need);
+bool any_elements(const StepArgs& a);
+bool state_in_place(const zero_shard* shards, int n_shards);
+// Which stream a pass's vector loop aligns to 128 bytes: its dominant one.
+enum HeadKind { HEAD_NONE = 0, HEAD_GRADS = 1, HEAD_STATE = 2 };
+void number_tiles(StepArgs& a, int vec, int kind = HEAD_NONE);
 
 // zero_shard_step in two phases: plan_step makes every argument check and
 // packs the kernel arguments without touching the device (an argument error

@@ -33,10 +33,11 @@ const void* apply_kernel(int gdt, int pdt, int vec) {
     return pdt == ZERO_BF16 ? apply_ptr<ZERO_F16, ZERO_BF16>(vec) : apply_ptr<ZERO_F16, ZERO_F16>(vec);
 }
 
-int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s) {
+int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s, bool early) {
     const void* f = reduce_kernel(gdt, vec, ns_variant(a.n_slices));
     const int grid = grid_for(f, a.n_tiles, BPS_REDUCE);
     void* args[] = {const_cast<StepArgs*>(&a)};
+    if (!early) return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "reduce launch");
     return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, 0, s), "reduce launch");
 }
 
