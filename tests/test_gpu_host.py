@@ -64,12 +64,13 @@ class HostRun(DeviceRun):
         return r
 
 
-def run_host(Z, numels, nd, dt, seed, h, S, pingpong, chunk, steps=3, inject=None, mode=0, download=True):
+def run_host(Z, numels, nd, dt, seed, h, S, pingpong, chunk, steps=3, inject=None, mode=0, download=True,
+             ranks=None, extra=(0.0, 0)):
     p, flat, grads = make_problem(numels, nd, dt, mode, seed, loss_scale=S, grad_std=1e-2 if
                                   h["max_grad_norm"] > 0 else 1e-3, steps=steps)
     if inject:
         inject(grads)
-    ranks = list(range(nd))
+    ranks = list(range(nd)) if ranks is None else ranks
     run = HostRun(Z, p, flat, dt, ranks, pingpong, chunk, download=download)
     osh = oracle_shards(p, flat, dt, ranks)
     oflat = flat.copy()
@@ -77,9 +78,9 @@ def run_host(Z, numels, nd, dt, seed, h, S, pingpong, chunk, steps=3, inject=Non
     exact = h["max_grad_norm"] <= 0
     out = []
     for k in range(steps):
-        r_gpu = run.step(grads[k], h, t, Sg)
+        r_gpu = run.step(grads[k], h, t, Sg, extra)
         prev = [(o["master"].copy(), o["m"].copy()) for o in osh]
-        r_or, red = orc.zero_step(grads[k], dt, osh, oflat, dt, h, t, So, 0.0, 0, want_grad=True)
+        r_or, red = orc.zero_step(grads[k], dt, osh, oflat, dt, h, t, So, *extra, want_grad=True)
         compare(run, osh, oflat, r_gpu, r_or, exact, prev, red)
         out.append(r_gpu.as_dict())
         if r_or.applied:
@@ -127,6 +128,17 @@ def test_host_step_skip_restores_host_parameters(Z, pingpong):
     res = run_host(Z, W.numels(W.tiny_group()), 3, 1, 0, hyper32(), 1024.0, pingpong, 1024, inject=inject)
     assert [r["applied"] for r in res] == [1, 0, 1]
     assert res[1]["overflow"] == 1
+
+
+@pytest.mark.parametrize("clip", [0.0, 0.01])
+def test_host_step_rank_local_with_other_ranks_statistics(Z, clip):
+    """One rank's shard of an N_d = 4 group, the other ranks' share of the
+    sum of squares given as extra_sumsq (and their overflow flag clear): the
+    norm, the clip and every update as the oracle's over the same view."""
+    res = run_host(Z, [9000, 13000, 2500], 4, 2, 21, hyper32(max_grad_norm=clip), 1.0, True, 512, ranks=[1],
+                   extra=(0.75, 0))
+    assert all(r["applied"] == 1 and r["path"] == (2 if clip else 3) for r in res)
+    assert all(r["sumsq"] > 0.75 for r in res)
 
 
 def test_host_step_without_download(Z):

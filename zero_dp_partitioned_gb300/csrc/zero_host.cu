@@ -29,6 +29,19 @@ struct HostLane {
 static std::mutex g_lane_mu;                       // held for a whole call: calls are serialised
 static std::map<int, HostLane> g_lanes;
 
+static void drop_lane(HostLane& l) {
+    cudaEvent_t* evs[] = {&l.start, &l.up_done, &l.down_done};
+    for (cudaEvent_t* ev : evs)
+        if (*ev) cudaEventDestroy(*ev);
+    for (int k = 0; k < HOST_RING; ++k) {
+        if (l.landed[k]) cudaEventDestroy(l.landed[k]);
+        if (l.read[k]) cudaEventDestroy(l.read[k]);
+    }
+    if (l.up) cudaStreamDestroy(l.up);
+    if (l.down) cudaStreamDestroy(l.down);
+    l = HostLane{};
+}
+
 static int make_lane(HostLane& l) {
     cudaError_t e = cudaStreamCreateWithFlags(&l.up, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&l.down, cudaStreamNonBlocking);
@@ -39,6 +52,7 @@ static int make_lane(HostLane& l) {
         e = cudaEventCreateWithFlags(&l.landed[k], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&l.read[k], cudaEventDisableTiming);
     }
+    if (e != cudaSuccess) drop_lane(l);
     return cuda_fail(e, "zero_shard_step_host: creating its streams and events");
 }
 
@@ -69,6 +83,104 @@ static zero_shard sub_shard(const zero_shard& z, int64_t lo, int64_t hi) {
     c.v_out = z.v_out + lo;
     c.grad_shard = z.grad_shard ? static_cast<void*>(static_cast<uint16_t*>(z.grad_shard) + lo) : nullptr;
     return c;
+}
+
+// Everything the step enqueues, in order: the copies up on the lane's first
+// stream, each chunk's pass on the caller's stream as the chunk lands, the
+// copies down on the lane's second stream, then the decision (or the apply
+// pass and the shards' copies down).  Returns at the first failed call.
+static int enqueue_host_step(HostLane& lane, const StepArgs& base, const void* const* host_grad_slices, int n_slices,
+                             int grad_dtype, const zero_shard* shards, int n_shards, void* flat_param,
+                             int param_dtype, void* host_param, void* host_param_dev, void* staging, int64_t chunk,
+                             bool fused, cudaStream_t s) {
+    const size_t esz = 2;
+    int rc;
+#define HOST_TRY(call, what)                                                                \
+    do {                                                                                    \
+        if ((rc = cuda_fail((call), "zero_shard_step_host: " what)) != ZERO_OK) return rc; \
+    } while (0)
+    HOST_TRY(cudaEventRecord(lane.start, s), "event");
+    HOST_TRY(cudaStreamWaitEvent(lane.up, lane.start, 0), "event");
+    HOST_TRY(cudaStreamWaitEvent(lane.down, lane.start, 0), "event");
+    if (!any_elements(base)) HOST_TRY(cudaMemsetAsync(base.stats, 0, sizeof(zero_stats), s), "clearing the statistics");
+
+    int64_t j = 0;                        // chunks so far; chunk j uses slot j mod HOST_RING
+    for (int si = 0; si < n_shards; ++si)
+    for (int64_t lo = 0; lo < shards[si].numel; lo += chunk, ++j) {
+        const int k = (int)(j % HOST_RING);
+        const zero_shard& z = shards[si];
+        const int64_t hi = lo + chunk < z.numel ? lo + chunk : z.numel;
+        const int64_t n = hi - lo;
+        // up: slot k once the pass that read it last is done
+        const void* slot[ZERO_MAX_SLICES];
+        HOST_TRY(cudaStreamWaitEvent(lane.up, lane.read[k], 0), "event");
+        for (int r = 0; r < n_slices; ++r) {
+            char* dst = static_cast<char*>(staging) + ((size_t)k * n_slices + r) * (size_t)chunk * esz;
+            const char* src = static_cast<const char*>(host_grad_slices[r]) + (size_t)(z.grad_offset + lo) * esz;
+            HOST_TRY(cudaMemcpyAsync(dst, src, (size_t)n * esz, cudaMemcpyHostToDevice, lane.up), "copy up");
+            slot[r] = dst;
+        }
+        HOST_TRY(cudaEventRecord(lane.landed[k], lane.up), "event");
+        // the chunk's pass, on the caller's stream
+        HOST_TRY(cudaStreamWaitEvent(s, lane.landed[k], 0), "event");
+        StepArgs a = base;
+        const zero_shard part = sub_shard(z, lo, hi);
+        pack_slices(a, slot, n_slices);
+        pack_shards(a, &part, 1, fused ? 1 : 2);
+        a.accumulate = j > 0 ? 1 : 0;
+        if (fused) {
+            const int vec = vec8_ok(a, 1) ? 8 : 1;
+            number_tiles(a, vec, HEAD_GRADS);
+            const int grid = grid_for(fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
+                                      n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
+            if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
+        } else {
+            const int vec = vec8_ok(a, 2) ? 8 : 1;
+            number_tiles(a, vec, HEAD_GRADS);
+            if ((rc = launch_reduce(a, grad_dtype, vec, s, false)) != ZERO_OK) return rc;
+        }
+        HOST_TRY(cudaEventRecord(lane.read[k], s), "event");
+        // down: the chunk's parameters (final unless the commit skips the step)
+        if (fused && host_param) {
+            HOST_TRY(cudaStreamWaitEvent(lane.down, lane.read[k], 0), "event");
+            const size_t off = (size_t)(z.param_offset + lo) * esz;
+            HOST_TRY(cudaMemcpyAsync(static_cast<char*>(host_param) + off, static_cast<const char*>(flat_param) + off,
+                                     (size_t)n * esz, cudaMemcpyDeviceToHost, lane.down),
+                     "copy down");
+        }
+    }
+    HOST_TRY(cudaEventRecord(lane.up_done, lane.up), "event");
+    HOST_TRY(cudaEventRecord(lane.down_done, lane.down), "event");
+    HOST_TRY(cudaStreamWaitEvent(s, lane.up_done, 0), "event");
+    HOST_TRY(cudaStreamWaitEvent(s, lane.down_done, 0), "event");
+
+    if (fused) {
+        // the decision; a skipped step's parameters restored on the device and,
+        // after the copies down have landed, in host memory too
+        StepArgs a = base;
+        if ((rc = launch_commit(a, s)) != ZERO_OK) return rc;
+        if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
+        if (host_param) {
+            a.flat_param = host_param_dev;
+            if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
+        }
+        return ZERO_OK;
+    }
+    StepArgs a = base;
+    pack_shards(a, shards, n_shards, 3);
+    const int vec = vec8_ok(a, 3) ? 8 : 1;
+    number_tiles(a, vec, HEAD_STATE);
+    if ((rc = launch_apply(a, grad_dtype, param_dtype, vec, s)) != ZERO_OK) return rc;
+    if (host_param)
+        for (int i = 0; i < n_shards; ++i) {
+            if (shards[i].numel == 0) continue;
+            const size_t off = (size_t)shards[i].param_offset * esz;
+            HOST_TRY(cudaMemcpyAsync(static_cast<char*>(host_param) + off, static_cast<const char*>(flat_param) + off,
+                                     (size_t)shards[i].numel * esz, cudaMemcpyDeviceToHost, s),
+                     "copy down");
+        }
+#undef HOST_TRY
+    return ZERO_OK;
 }
 
 }  // namespace zdp
@@ -131,92 +243,15 @@ extern "C" int zero_shard_step_host(const void* const* host_grad_slices, int n_s
         return rc;
     }
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t esz = 2;
-#define HOST_TRY(call, what)                                               \
-    do {                                                                   \
-        if ((rc = cuda_fail((call), "zero_shard_step_host: " what)) != ZERO_OK) return rc; \
-    } while (0)
-    HOST_TRY(cudaEventRecord(lane.start, s), "event");
-    HOST_TRY(cudaStreamWaitEvent(lane.up, lane.start, 0), "event");
-    HOST_TRY(cudaStreamWaitEvent(lane.down, lane.start, 0), "event");
-    if (!any_elements(base)) HOST_TRY(cudaMemsetAsync(base.stats, 0, sizeof(zero_stats), s), "clearing the statistics");
-
-    int64_t j = 0;                        // chunks so far; chunk j uses slot j mod HOST_RING
-    for (int si = 0; si < n_shards; ++si)
-    for (int64_t lo = 0; lo < shards[si].numel; lo += chunk, ++j) {
-        const int k = (int)(j % HOST_RING);
-        const zero_shard& z = shards[si];
-        const int64_t hi = lo + chunk < z.numel ? lo + chunk : z.numel;
-        const int64_t n = hi - lo;
-        // up: slot k once the pass that read it last is done
-        const void* slot[ZERO_MAX_SLICES];
-        HOST_TRY(cudaStreamWaitEvent(lane.up, lane.read[k], 0), "event");
-        for (int r = 0; r < n_slices; ++r) {
-            char* dst = static_cast<char*>(staging) + ((size_t)k * n_slices + r) * (size_t)chunk * esz;
-            const char* src = static_cast<const char*>(host_grad_slices[r]) + (size_t)(z.grad_offset + lo) * esz;
-            HOST_TRY(cudaMemcpyAsync(dst, src, (size_t)n * esz, cudaMemcpyHostToDevice, lane.up), "copy up");
-            slot[r] = dst;
-        }
-        HOST_TRY(cudaEventRecord(lane.landed[k], lane.up), "event");
-        // the chunk's pass, on the caller's stream
-        HOST_TRY(cudaStreamWaitEvent(s, lane.landed[k], 0), "event");
-        StepArgs a = base;
-        const zero_shard part = sub_shard(z, lo, hi);
-        pack_slices(a, slot, n_slices);
-        pack_shards(a, &part, 1, fused ? 1 : 2);
-        a.accumulate = j > 0 ? 1 : 0;
-        if (fused) {
-            const int vec = vec8_ok(a, 1) ? 8 : 1;
-            number_tiles(a, vec, HEAD_GRADS);
-            const int grid = grid_for(fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
-                                      n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
-            if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
-        } else {
-            const int vec = vec8_ok(a, 2) ? 8 : 1;
-            number_tiles(a, vec, HEAD_GRADS);
-            if ((rc = launch_reduce(a, grad_dtype, vec, s, false)) != ZERO_OK) return rc;
-        }
-        HOST_TRY(cudaEventRecord(lane.read[k], s), "event");
-        // down: the chunk's parameters (final unless the commit skips the step)
-        if (fused && host_param) {
-            HOST_TRY(cudaStreamWaitEvent(lane.down, lane.read[k], 0), "event");
-            const size_t off = (size_t)(z.param_offset + lo) * esz;
-            HOST_TRY(cudaMemcpyAsync(static_cast<char*>(host_param) + off, static_cast<const char*>(flat_param) + off,
-                                     (size_t)n * esz, cudaMemcpyDeviceToHost, lane.down),
-                     "copy down");
-        }
+    rc = enqueue_host_step(lane, base, host_grad_slices, n_slices, grad_dtype, shards, n_shards, flat_param,
+                           param_dtype, host_param, host_param_dev, staging, chunk, fused, s);
+    if (rc != ZERO_OK) {
+        // an enqueue failed part way: the caller's stream still waits for what
+        // the library's streams hold (best effort; the first error is reported)
+        cudaEventRecord(lane.up_done, lane.up);
+        cudaEventRecord(lane.down_done, lane.down);
+        cudaStreamWaitEvent(s, lane.up_done, 0);
+        cudaStreamWaitEvent(s, lane.down_done, 0);
     }
-    HOST_TRY(cudaEventRecord(lane.up_done, lane.up), "event");
-    HOST_TRY(cudaEventRecord(lane.down_done, lane.down), "event");
-    HOST_TRY(cudaStreamWaitEvent(s, lane.up_done, 0), "event");
-    HOST_TRY(cudaStreamWaitEvent(s, lane.down_done, 0), "event");
-
-    if (fused) {
-        // the decision; a skipped step's parameters restored on the device and,
-        // after the copies down have landed, in host memory too
-        StepArgs a = base;
-        a.result = result;
-        if ((rc = launch_commit(a, s)) != ZERO_OK) return rc;
-        if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
-        if (host_param) {
-            a.flat_param = host_param_dev;
-            if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
-        }
-        return ZERO_OK;
-    }
-    StepArgs a = base;
-    pack_shards(a, shards, n_shards, 3);
-    const int vec = vec8_ok(a, 3) ? 8 : 1;
-    number_tiles(a, vec, HEAD_STATE);
-    if ((rc = launch_apply(a, grad_dtype, param_dtype, vec, s)) != ZERO_OK) return rc;
-    if (host_param)
-        for (int i = 0; i < n_shards; ++i) {
-            if (shards[i].numel == 0) continue;
-            const size_t off = (size_t)shards[i].param_offset * esz;
-            HOST_TRY(cudaMemcpyAsync(static_cast<char*>(host_param) + off, static_cast<const char*>(flat_param) + off,
-                                     (size_t)shards[i].numel * esz, cudaMemcpyDeviceToHost, s),
-                     "copy down");
-        }
-#undef HOST_TRY
-    return ZERO_OK;
+    return rc;
 }
