@@ -180,6 +180,59 @@ def test_gpt2_1p5b_all_ranks(Z, chained):
             check_state(s, *sets[cur], flat, exact=True)
 
 
+def test_gpt2_1p5b_from_host_buffers(Z):
+    """The end-to-end call at full size: the GPT-2 1.5B-shaped group's 8
+    gradient buffers (24.9 GB) in page-locked host memory, zero_shard_step_host
+    with the benchmark's 512 MiB device ring (8 Mi-element chunks), the
+    updated 16-bit parameters returned to page-locked host memory; 2 steps,
+    the host keeping t and the state set.  The statistics against the
+    oracle's over every element, state and parameters at sampled indices bit
+    for bit, and the host copy of the parameters equal to the device's."""
+    wl = W.workload("gpt2-1.5b-nd8")
+    nd, dt = 8, 2
+    plan = Z.zero_plan(W.numels(wl.specs), nd)
+    P = plan["padded_total"]
+    flat = W.flat_params(wl.specs, P, torch.bfloat16, wl.param_seed, DEV)
+    grads = [torch.empty(P, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    host_grads = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True) for _ in range(nd)]
+    host_params = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    gs = W.GradStream([1 + r for r in range(nd)], DEV)
+    sets = [[flat.float(), torch.zeros(P, device=DEV), torch.zeros(P, device=DEV)],
+            [torch.empty(P, device=DEV) for _ in range(3)]]
+    ring_bytes = 512 << 20
+    ring = torch.empty(ring_bytes // 2, dtype=torch.int16, device=DEV)
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    samp = []
+    for r in range(nd):
+        o, n = plan["rank_offsets"][r], plan["rank_numels"][r]
+        idx = o + sample_idx(n, 20 + r, 8000)
+        samp.append(Sampled(idx, u16(flat[torch.from_numpy(idx).to(DEV)]), dt))
+    h = hyper32()
+    hz = {k: h[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")}
+    cur = 0
+    for t in (1, 2):
+        gs.draw_flat(grads, wl.specs, W.gpt2_grad_std())
+        for g, hg in zip(grads, host_grads):
+            hg.copy_(g)
+        A, B = sets[cur], sets[1 - cur]
+        sh = [Z.shard(n, o, o, A[0][o:o + n], A[1][o:o + n], A[2][o:o + n], B[0][o:o + n], B[1][o:o + n],
+                      B[2][o:o + n]) for o, n in zip(plan["rank_offsets"], plan["rank_numels"])]
+        Z.zero_shard_step_host(host_grads, dt, sh, flat, dt, host_params, Z.hyper(step=t, **hz), 1.0, 0.0, 0, ring,
+                               ring_bytes, ws, ws.numel(), res)
+        torch.cuda.synchronize()
+        acc, ovf = oracle_stats(host_grads, dt, 0, P)
+        r_gpu = Z.read_result(res)
+        k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+        assert r_gpu.overflow == ovf == 0 and r_gpu.applied == 1 and r_gpu.path == 3
+        assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
+        assert torch.equal(host_params.view(torch.int16), flat.cpu().view(torch.int16))
+        cur ^= 1
+        for s in samp:
+            s.step([u16(g[torch.from_numpy(s.idx)]) for g in host_grads], dt, k, scalars(h, t))
+            check_state(s, *sets[cur], flat, exact=True)
+
+
 def stats_tensor(Z, sumsq, overflow=0):
     """A device zero_stats holding the given sum of squares and flag."""
     return torch.frombuffer(bytearray(bytes(Z.zero_stats(sumsq, overflow, 0))), dtype=torch.uint8).to(DEV)
@@ -370,6 +423,72 @@ def test_zero3_llama3_8b_rank1(Z):
         orc.apply(a_samp, dt, samp.master, samp.m, samp.v, samp.param, dt, k, scalars(h, t))
         check_state(samp, master, m, v, rshards[me], exact=True)
     assert int(gstatus.item()) == 0
+
+
+def test_zero3_llama3_8b_rank1_fused_units(Z):
+    """The ZeRO-3 update as the benchmark runs it, at full size: per unit, in
+    reverse order, the 4 full-unit buckets reduced onto rank 1's part and
+    that part updated in one partial fused pass (chained: t, S and the state
+    set from the device; the result into the other state set), then one
+    commit deciding the step; 3 steps.  The statistics against the oracle's
+    over every element, the state and parameters at sampled indices of the
+    2.0B-element shard bit for bit."""
+    wl = W.workload("zero3-llama3-8b")
+    nd, dt, me = 4, 2, 1
+    units = W.llama_units(wl.specs)
+    parts = [u // nd for u in units]
+    uoff = np.concatenate([[0], np.cumsum(parts)[:-1]]).astype(np.int64)
+    L = int(sum(parts))
+    flat = W.flat_params(wl.specs, sum(units), torch.bfloat16, wl.param_seed, DEV)
+    starts = np.concatenate([[0], np.cumsum(units)[:-1]])
+    rshard = torch.cat([flat[s + me * p: s + (me + 1) * p] for s, p in zip(starts, parts)])
+    del flat
+    torch.cuda.empty_cache()
+    buckets = [torch.empty(max(units), dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    gs = W.GradStream([5 + r for r in range(nd)], DEV)
+    sets = [[rshard.float(), torch.zeros(L, device=DEV), torch.zeros(L, device=DEV)],
+            [torch.empty(L, device=DEV) for _ in range(3)]]
+    A, B = sets
+    part_sh = [Z.shard(parts[u], me * parts[u], int(uoff[u]), *(x[uoff[u]:uoff[u] + parts[u]] for x in A),
+                       *(x[uoff[u]:uoff[u] + parts[u]] for x in B)) for u in range(len(units))]
+    whole = [Z.shard(L, 0, 0, *A, *B)]
+    ws = torch.zeros(Z.zero_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    stats = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    res = torch.zeros(48, dtype=torch.uint8, device=DEV)
+    h = hyper32()
+    hy = Z.hyper(step=1, **{k: h[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")})
+    table = torch.from_numpy(Z.zero_adam_scalar_table(hy, 1, 16)).to(DEV)
+    chain = torch.frombuffer(bytearray(bytes(Z.chain(step=1, loss_scale=1.0))), dtype=torch.uint8).to(DEV)
+    idx = sample_idx(L, 6)
+    ti = torch.from_numpy(idx).to(DEV)
+    samp = Sampled(idx, u16(rshard[ti]), dt)
+    cur = 0
+    for t in (1, 2, 3):
+        acc = orc.ExactAccumulator()
+        a_samp = np.empty(idx.size, np.uint16)
+        for k_u, u in enumerate(reversed(range(len(units)))):
+            bu = [b[:units[u]] for b in buckets]
+            gs.draw_plain(bu, wl.grad_std)
+            Z.zero_shard_step_partial(bu, dt, [part_sh[u]], rshard, dt, hy, 0.0, k_u > 0, stats, ws, ws.numel(),
+                                      scalar_table=table, table_t0=1, n_table=16, chain_dev=chain)
+            a_u, o_u = oracle_stats(bu, dt, me * parts[u], parts[u])
+            acc.merge(a_u)
+            assert o_u == 0
+            sel = (idx >= uoff[u]) & (idx < uoff[u] + parts[u])
+            if sel.any():
+                loc = torch.from_numpy(idx[sel] - uoff[u] + me * parts[u]).to(DEV)
+                a_samp[sel] = orc.reduce([u16(b[loc]) for b in bu], dt, 0, int(sel.sum()))
+        Z.zero_shard_step_commit(whole, rshard, dt, 0.0, stats, 0.0, 0, res, table_t0=1, n_table=16,
+                                 chain_dev=chain)
+        k, norm, _ = orc.grad_multiplier(acc.value(), 1.0, 0.0)
+        r_gpu = Z.read_result(res)
+        assert r_gpu.applied == 1 and r_gpu.overflow == 0 and r_gpu.path == 3
+        assert r_gpu.grad_norm == pytest.approx(norm, rel=1e-5)
+        cur ^= 1
+        c = Z.read_chain(chain)
+        assert (c.step, c.cur, c.applied, c.skipped, c.failed) == (t + 1, cur, t, 0, 0)
+        orc.apply(a_samp, dt, samp.master, samp.m, samp.v, samp.param, dt, k, scalars(h, t))
+        check_state(samp, *sets[cur], rshard, exact=True)
 
 
 @pytest.mark.parametrize("clip", [0.0, 1.0])
