@@ -6,7 +6,7 @@ updated, and the updated parameters copied back to page-locked host memory.
 Every chunk is an independent piece of a shard, so the results are those of
 zero_shard_step: bit-exact state and parameters without clipping (path 3:
 partial passes and a commit), and with clipping whenever the multiplier k
-equals the oracle's (path 2: a reduce per chunk, then the apply), judged by
+equals the oracle's (path 2: a reduce per chunk, then the apply), held to
 the same comparison as the device-buffer step.  The host copy of the
 parameters must equal the device's bit for bit after every step, a skipped
 step included."""
