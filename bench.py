@@ -1013,6 +1013,7 @@ def zero3_prefetch(Z, W, torch, dev, e2e, timer, layers=None, vocab=None, tokens
 
     total = sum(units)
     return dict(name=name, step=step, state=st, elements=L, nd=nd,
+                path_of_last_step=lambda: Z.read_result(res).path,
                 launches_per_step=len(order) + n_units + 2,
                 kernel_bytes={"k_reduce": (2 * nd + 2) * L, "k_apply": 28 * L},
                 dominant_label=None, h2d=None, d2h=48, e2e_ok=False, extra=extra,
