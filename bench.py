@@ -1304,7 +1304,7 @@ def main():
                     help="measure only --workload (the default run also measures " + ", ".join(ALSO) + ")")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--tokens", type=int, default=1024,
                     help="zero3-prefetch-llama3-8b: activations of the stand-in GEMM per unit")
     ap.add_argument("--gather-ctas", type=int, default=32,
