@@ -171,6 +171,17 @@ def test_argument_errors_before_any_device_work(Z):
             Z.zero_shard_init(shards, flat, pdt, stream=0)
         assert e.value.code == code
     Z.zero_shard_init([Z.shard(0, 0, 0, 0, 0, 0, 0, 0, 0)], 0, Z.ZERO_BF16, stream=0)   # nothing to do: no launch
+    # the step from host buffers: the checks that come before it asks the
+    # driver about any pointer
+    for c in (dict(gdt=3, code=Z.ZERO_EINVAL), dict(loss_scale=float("inf"), code=Z.ZERO_EINVAL),
+              dict(step=0, code=Z.ZERO_EINVAL), dict(result=0, code=Z.ZERO_EINVAL),
+              dict(result=fake + 4, code=Z.ZERO_EINVAL), dict(slices=[], code=Z.ZERO_EINVAL),
+              dict(slices=[fake] * 65, code=Z.ZERO_ELIMIT), dict(slices=[fake + 1], code=Z.ZERO_EALIGN)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_step_host(c.get("slices", [fake]), c.get("gdt", Z.ZERO_BF16), sh, fake, Z.ZERO_BF16, fake,
+                                   Z.hyper(step=c.get("step", 1)), c.get("loss_scale", 1.0), 0.0, 0, fake, 1 << 20,
+                                   fake, ws, c.get("result", fake), stream=0)
+        assert e.value.code == c["code"], (c, str(e.value))
 
 
 def test_comm_volume_equals_oracle(Z, orc):
