@@ -51,11 +51,14 @@ class DeviceRun:
         self.flat_base = base
         self.flat = base[param_pad:]
         self.state = []
+        # state_pad: floats each state array starts into its buffer (one for all
+        # six, or one per array: master, m, v in, then out)
+        pads = tuple(state_pad) if isinstance(state_pad, (tuple, list)) else (state_pad,) * 6
         for r in ranks:
             o, n = int(p["rank_offsets"][r]), int(p["rank_numels"][r])
-            mk = lambda v: torch.cat([torch.zeros(state_pad, device=DEV), v])[state_pad:]
-            A = [mk(torch.empty(n, device=DEV)) for _ in range(3)]
-            B = [mk(torch.empty(n, device=DEV)) for _ in range(3)] if pingpong else A
+            mk = lambda v, q: torch.cat([torch.zeros(q, device=DEV), v])[q:]
+            A = [mk(torch.empty(n, device=DEV), pads[i]) for i in range(3)]
+            B = [mk(torch.empty(n, device=DEV), pads[3 + i]) for i in range(3)] if pingpong else A
             g = torch.empty(n, dtype=TDT[dt], device=DEV) if want_grad else None
             self.state.append(dict(o=o, n=n, A=A, B=B, g=g))
         Z.zero_shard_init(self.shards(), self.flat, dt)       # master = fp32(parameters), m = v = 0
@@ -350,6 +353,23 @@ def test_unaligned_pointers_take_the_scalar_path(Z):
     # state views 1 float into their buffers and a flat parameter buffer 1 element in: not 16-byte aligned
     run_both(Z, [5000, 77], 3, 2, 0, 8, hyper32(), 1.0, True, state_pad=1, param_pad=1, steps=2)
     run_both(Z, [5000, 77], 3, 1, 1, 9, hyper32(), 512.0, False, state_pad=1, param_pad=3, steps=2)
+
+
+@pytest.mark.parametrize("dt", [1, 2])
+@pytest.mark.parametrize("pads", [(4, 4, 4, 4, 4, 4), (0, 0, 4, 0, 0, 0), (0, 0, 0, 0, 0, 12), (8, 8, 8, 8, 8, 8),
+                                  (8, 0, 24, 16, 8, 0)])
+def test_state_on_16_and_32_byte_boundaries(Z, dt, pads):
+    """The apply pass moves a vector's 8 values of each state array in one
+    256-bit access when all six arrays are 32-byte aligned, else in two
+    128-bit accesses (arrays 16 bytes past a 32-byte boundary: all six, or
+    only one).  Neither may change a bit, on the reduce + apply passes with
+    the state in place (clipping on); the fused pass (ping-pong state) runs
+    on the same layouts."""
+    S = 512.0 if dt == 1 else 1.0
+    numels = [5000, 77, 40000]
+    run_both(Z, numels, 3, dt, 0, 60 + sum(pads) + dt, hyper32(), S, True, steps=2, state_pad=pads)
+    run_both(Z, numels, 3, dt, 0, 61 + sum(pads) + dt, hyper32(max_grad_norm=0.01), S, False, steps=2,
+             state_pad=pads[:3] * 2, grad_std=1e-2)
 
 
 def test_empty_shards_and_no_shards(Z):

@@ -204,6 +204,13 @@ void number_tiles(StepArgs& a, int vec, int kind) {
         ShardDev& d = a.shards[i];
         d.head = vec == 8 ? shard_head(a, d, kind) : 0;
         if (d.head > d.numel) d.head = d.numel;
+        // The vector loop's element index is a multiple of 8 (so is the
+        // head), so each state array's vectors are 32-byte aligned when its
+        // base is.
+        const uintptr_t st = reinterpret_cast<uintptr_t>(d.mi) | reinterpret_cast<uintptr_t>(d.mmi) |
+                             reinterpret_cast<uintptr_t>(d.vi) | reinterpret_cast<uintptr_t>(d.mo) |
+                             reinterpret_cast<uintptr_t>(d.mmo) | reinterpret_cast<uintptr_t>(d.vo);
+        d.wide = vec == 8 && d.mi && (st & 31u) == 0 ? 1 : 0;
         d.tile_begin = t;
         const int64_t rest = d.numel - d.head;
         t += d.numel == 0 ? 0 : (rest > 0 ? (rest + tile - 1) / tile : 1);
