@@ -357,14 +357,18 @@ def test_unaligned_pointers_take_the_scalar_path(Z):
 
 @pytest.mark.parametrize("dt", [1, 2])
 @pytest.mark.parametrize("pads", [(4, 4, 4, 4, 4, 4), (0, 0, 4, 0, 0, 0), (0, 0, 0, 0, 0, 12), (8, 8, 8, 8, 8, 8),
-                                  (8, 0, 24, 16, 8, 0)])
+                                  (32, 8, 24, 16, 8, 0)])
 def test_state_on_16_and_32_byte_boundaries(Z, dt, pads):
     """The apply pass moves a vector's 8 values of each state array in one
-    256-bit access when all six arrays are 32-byte aligned, else in two
-    128-bit accesses (arrays 16 bytes past a 32-byte boundary: all six, or
-    only one).  Neither may change a bit, on the reduce + apply passes with
-    the state in place (clipping on); the fused pass (ping-pong state) runs
-    on the same layouts."""
+    256-bit access when, in every shard, all six arrays are 32-byte aligned
+    and the gradient stream starts on a 128-byte line (the last case: master
+    128 bytes into its buffer, the others at other multiples of 32), else in
+    two 128-bit accesses (arrays 16 bytes past a 32-byte boundary, all six or
+    only one; all six 32 bytes in, which puts the gradient stream off its
+    line).
+    Neither may change a bit, on the reduce + apply passes with the state in
+    place (clipping on); the fused pass (ping-pong state) runs on the same
+    layouts."""
     S = 512.0 if dt == 1 else 1.0
     numels = [5000, 77, 40000]
     run_both(Z, numels, 3, dt, 0, 60 + sum(pads) + dt, hyper32(), S, True, steps=2, state_pad=pads)

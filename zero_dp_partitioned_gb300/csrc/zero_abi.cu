@@ -204,13 +204,6 @@ void number_tiles(StepArgs& a, int vec, int kind) {
         ShardDev& d = a.shards[i];
         d.head = vec == 8 ? shard_head(a, d, kind) : 0;
         if (d.head > d.numel) d.head = d.numel;
-        // The vector loop's element index is a multiple of 8 (so is the
-        // head), so each state array's vectors are 32-byte aligned when its
-        // base is.
-        const uintptr_t st = reinterpret_cast<uintptr_t>(d.mi) | reinterpret_cast<uintptr_t>(d.mmi) |
-                             reinterpret_cast<uintptr_t>(d.vi) | reinterpret_cast<uintptr_t>(d.mo) |
-                             reinterpret_cast<uintptr_t>(d.mmo) | reinterpret_cast<uintptr_t>(d.vo);
-        d.wide = vec == 8 && d.mi && (st & 31u) == 0 ? 1 : 0;
         d.tile_begin = t;
         const int64_t rest = d.numel - d.head;
         t += d.numel == 0 ? 0 : (rest > 0 ? (rest + tile - 1) / tile : 1);
@@ -234,6 +227,44 @@ int pack_slices(StepArgs& a, const void* const* slices, int n_slices) {
 
 // 16-byte vectors are possible when every gradient address a shard starts at
 // and every pointer the vector path loads from are 16-byte aligned.
+// The apply pass's 256-bit state accesses: every shard's six state arrays
+// 32-byte aligned (the vector loop's element index is a multiple of 8, and
+// so is the head), and its gradient stream starting on a 128-byte line.
+// Measured on GB300 (sources alternated in one call): the pass on one
+// 2.0B-element shard, every stream on a line, 8.494 ms against 8.629 ms with
+// 128-bit accesses; on eight 195M-element shards cut from one
+// averaged-gradient buffer (gradient streams 16-112 bytes off a line), 7.08
+// against 6.99 ms (with a per-vector choice), so those keep 128-bit accesses.
+bool state_wide(const StepArgs& a) {
+    for (int i = 0; i < a.n_shards; ++i) {
+        const ShardDev& d = a.shards[i];
+        if (d.numel == 0) continue;
+        const uintptr_t st = reinterpret_cast<uintptr_t>(d.mi) | reinterpret_cast<uintptr_t>(d.mmi) |
+                             reinterpret_cast<uintptr_t>(d.vi) | reinterpret_cast<uintptr_t>(d.mo) |
+                             reinterpret_cast<uintptr_t>(d.mmo) | reinterpret_cast<uintptr_t>(d.vo);
+        const uintptr_t g = reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(d.gshard) + d.head);
+        if (!d.mi || !d.gshard || (st & 31u) != 0 || (g & 127u) != 0) return false;
+    }
+    return true;
+}
+
+// The fused pass's 256-bit state accesses: every shard's six state arrays
+// 32-byte aligned.  Measured on GB300 (sources alternated in one call): the
+// 8-slice GPT-2 pass 9.354 against 9.399 ms, the 4-slice ZeRO-3 partial pass
+// 0.2977 against 0.2999 ms, the 64-slice pass unchanged (2.631 against 2.632
+// ms).
+bool fused_state_wide(const StepArgs& a) {
+    for (int i = 0; i < a.n_shards; ++i) {
+        const ShardDev& d = a.shards[i];
+        if (d.numel == 0) continue;
+        const uintptr_t st = reinterpret_cast<uintptr_t>(d.mi) | reinterpret_cast<uintptr_t>(d.mmi) |
+                             reinterpret_cast<uintptr_t>(d.vi) | reinterpret_cast<uintptr_t>(d.mo) |
+                             reinterpret_cast<uintptr_t>(d.mmo) | reinterpret_cast<uintptr_t>(d.vo);
+        if (!d.mi || (st & 31u) != 0) return false;
+    }
+    return true;
+}
+
 bool vec8_ok(const StepArgs& a, int need) {
     for (int i = 0; i < a.n_shards; ++i) {
         const ShardDev& d = a.shards[i];
@@ -337,7 +368,7 @@ int run_step(StepPlan& sp, cudaStream_t s) {
     if (sp.fused) {
         const int vec = vec8_ok(a, 1) ? 8 : 1;
         number_tiles(a, vec, HEAD_GRADS);
-        const int grid = grid_for(fused_kernel(sp.gdt, sp.pdt, vec, fused_ns(a.n_slices)), a.n_tiles,
+        const int grid = grid_for(fused_fn(a, sp.gdt, sp.pdt, vec), a.n_tiles,
                                   a.n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
         if ((rc = launch_fused(a, sp.gdt, sp.pdt, vec, grid, s)) != ZERO_OK) return rc;
         return launch_recover(a, sp.pdt, s);
@@ -535,7 +566,7 @@ int zero_shard_step_chained(const void* const* grad_slices, int n_slices, int gr
         // the fused pass derives k = fp32(1/S) from chain->loss_scale on the device
         const int vec = vec8_ok(a, 1) ? 8 : 1;
         number_tiles(a, vec, HEAD_GRADS);
-        const int grid = grid_for(fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
+        const int grid = grid_for(fused_fn(a, grad_dtype, param_dtype, vec), a.n_tiles,
                                   n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
         if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
         if ((rc = launch_recover(a, param_dtype, s)) != ZERO_OK) return rc;
@@ -691,8 +722,7 @@ int zero_shard_step_partial(const void* const* grad_slices, int n_slices, int gr
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int vec = vec8_ok(a, 1) ? 8 : 1;
     number_tiles(a, vec, HEAD_GRADS);
-    const void* f = chain ? fused_kernel_chain(grad_dtype, param_dtype, vec, fused_ns(n_slices))
-                          : fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices));
+    const void* f = fused_fn(a, grad_dtype, param_dtype, vec);
     const int bps = n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY;
     const size_t smem = smem_capping(f, bps);
     const int grid = grid_for_smem(f, a.n_tiles, smem, bps);

@@ -4,46 +4,43 @@
 
 namespace zdp {
 
-template <int G, int P, int V>
+template <int G, int P, int V, bool C, bool W>
 static const void* fused_ptr(int ns) {
-    if (ns == 4) return (const void*)k_step_fused<G, P, V, 4>;
-    return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW> : (const void*)k_step_fused<G, P, V, 0>;
+    if (ns == 4) return (const void*)k_step_fused<G, P, V, 4, C, W>;
+    return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW, C, W> : (const void*)k_step_fused<G, P, V, 0, C, W>;
 }
 
-template <int G, int P>
-static const void* fused_ptr_v(int vec, int ns) {
-    return vec == 8 ? fused_ptr<G, P, 8>(ns) : fused_ptr<G, P, 1>(ns);
+template <int G, int P, bool C>
+static const void* fused_ptr_v(int vec, int ns, bool wide) {
+    if (vec != 8) return fused_ptr<G, P, 1, C, false>(ns);
+    return wide ? fused_ptr<G, P, 8, C, true>(ns) : fused_ptr<G, P, 8, C, false>(ns);
 }
 
-const void* fused_kernel(int gdt, int pdt, int vec, int ns) {
-    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_BF16, ZERO_BF16>(vec, ns)
-                                                  : fused_ptr_v<ZERO_BF16, ZERO_F16>(vec, ns);
-    return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_F16, ZERO_BF16>(vec, ns) : fused_ptr_v<ZERO_F16, ZERO_F16>(vec, ns);
+template <bool C>
+static const void* fused_pick(int gdt, int pdt, int vec, int ns, bool wide) {
+    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_BF16, ZERO_BF16, C>(vec, ns, wide)
+                                                  : fused_ptr_v<ZERO_BF16, ZERO_F16, C>(vec, ns, wide);
+    return pdt == ZERO_BF16 ? fused_ptr_v<ZERO_F16, ZERO_BF16, C>(vec, ns, wide) : fused_ptr_v<ZERO_F16, ZERO_F16, C>(vec, ns, wide);
 }
+
+const void* fused_kernel(int gdt, int pdt, int vec, int ns, bool wide) { return fused_pick<false>(gdt, pdt, vec, ns, wide); }
 
 // Chained steps: the same passes, instantiated with the device-side
 // bookkeeping (t, S and the state set read from the chain).
-template <int G, int P, int V>
-static const void* fused_chain_ptr_v(int ns) {
-    if (ns == 4) return (const void*)k_step_fused<G, P, V, 4, true>;
-    return ns == NS_FEW ? (const void*)k_step_fused<G, P, V, NS_FEW, true> : (const void*)k_step_fused<G, P, V, 0, true>;
+const void* fused_kernel_chain(int gdt, int pdt, int vec, int ns, bool wide) {
+    return fused_pick<true>(gdt, pdt, vec, ns, wide);
 }
 
-template <int G, int P>
-static const void* fused_chain_ptr(int vec, int ns) {
-    return vec == 8 ? fused_chain_ptr_v<G, P, 8>(ns) : fused_chain_ptr_v<G, P, 1>(ns);
-}
-
-const void* fused_kernel_chain(int gdt, int pdt, int vec, int ns) {
-    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_BF16, ZERO_BF16>(vec, ns)
-                                                  : fused_chain_ptr<ZERO_BF16, ZERO_F16>(vec, ns);
-    return pdt == ZERO_BF16 ? fused_chain_ptr<ZERO_F16, ZERO_BF16>(vec, ns)
-                            : fused_chain_ptr<ZERO_F16, ZERO_F16>(vec, ns);
+// The fused pass's kernel for these arguments: chained or not, and with
+// 256-bit state accesses when every shard's state arrays allow them.
+const void* fused_fn(const StepArgs& a, int gdt, int pdt, int vec) {
+    const int ns = fused_ns(a.n_slices);
+    const bool wide = vec == 8 && fused_state_wide(a);
+    return a.chain ? fused_kernel_chain(gdt, pdt, vec, ns, wide) : fused_kernel(gdt, pdt, vec, ns, wide);
 }
 
 int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s) {
-    const int ns = fused_ns(a.n_slices);
-    const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec, ns) : fused_kernel(gdt, pdt, vec, ns);
+    const void* f = fused_fn(a, gdt, pdt, vec);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "fused step launch");
 }
@@ -115,8 +112,7 @@ int launch_commit(const StepArgs& a, cudaStream_t s) {
 }
 
 int launch_fused_early(const StepArgs& a, int gdt, int pdt, int vec, int grid, size_t smem, cudaStream_t s) {
-    const int ns = fused_ns(a.n_slices);
-    const void* f = a.chain ? fused_kernel_chain(gdt, pdt, vec, ns) : fused_kernel(gdt, pdt, vec, ns);
+    const void* f = fused_fn(a, gdt, pdt, vec);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(launch_after_previous(f, grid, TILE_THREADS, args, smem, s), "partial fused pass launch");
 }

@@ -131,7 +131,7 @@ static int enqueue_host_step(HostLane& lane, const StepArgs& base, const void* c
         if (fused) {
             const int vec = vec8_ok(a, 1) ? 8 : 1;
             number_tiles(a, vec, HEAD_GRADS);
-            const int grid = grid_for(fused_kernel(grad_dtype, param_dtype, vec, fused_ns(n_slices)), a.n_tiles,
+            const int grid = grid_for(fused_fn(a, grad_dtype, param_dtype, vec), a.n_tiles,
                                       n_slices <= FEW_SLICES ? BPS_FUSED_FEW : BPS_FUSED_MANY);
             if ((rc = launch_fused(a, grad_dtype, param_dtype, vec, grid, s)) != ZERO_OK) return rc;
         } else {

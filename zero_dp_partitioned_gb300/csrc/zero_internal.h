@@ -53,6 +53,7 @@ cudaError_t launch_after_previous(const void* f, int grid, int block, void** arg
 
 // Launchers; each validates nothing (the entry points did) and returns
 // ZERO_OK or ZERO_ECUDA.  vec is 8 or 1.
+const void* fused_fn(const StepArgs& a, int gdt, int pdt, int vec);
 int launch_fused(const StepArgs& a, int gdt, int pdt, int vec, int grid, cudaStream_t s);
 int launch_recover(const StepArgs& a, int pdt, cudaStream_t s);
 int launch_init(const StepArgs& a, int pdt, cudaStream_t s);
@@ -99,6 +100,8 @@ int pack_shards(StepArgs& a, const zero_shard* shards, int n_shards, int need);
 int pack_slices(StepArgs& a, const void* const* slices, int n_slices);
 int check_workspace(StepArgs& a, void* ws, size_t ws_bytes);
 bool vec8_ok(const StepArgs& a, int need);
+bool state_wide(const StepArgs& a);          // the apply pass may take 256-bit state accesses
+bool fused_state_wide(const StepArgs& a);    // the fused pass may take 256-bit state accesses
 bool any_elements(const StepArgs& a);
 bool state_in_place(const zero_shard* shards, int n_shards);
 // Which stream a pass's vector loop aligns to 128 bytes: its dominant one.
@@ -119,10 +122,10 @@ int plan_step(StepPlan& sp, const void* const* grad_slices, int n_slices, int gr
 int run_step(StepPlan& sp, cudaStream_t s);
 
 // Kernel addresses, for the occupancy query.
-const void* fused_kernel(int gdt, int pdt, int vec, int ns);
-const void* fused_kernel_chain(int gdt, int pdt, int vec, int ns);
+const void* fused_kernel(int gdt, int pdt, int vec, int ns, bool wide = false);
+const void* fused_kernel_chain(int gdt, int pdt, int vec, int ns, bool wide = false);
 const void* reduce_kernel(int gdt, int vec, int ns);
-const void* apply_kernel(int gdt, int pdt, int vec);
+const void* apply_kernel(int gdt, int pdt, int vec, bool wide = false);
 
 // The slice-count specialisation of the reduce pass for n slices (0 = the
 // generic loop).

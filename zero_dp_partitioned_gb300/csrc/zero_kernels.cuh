@@ -58,7 +58,6 @@ struct ShardDev {
     const float *mi, *mmi, *vi;     // master, m, v in
     float *mo, *mmo, *vo;           // master, m, v out
     void* gshard;                   // 16-bit reduced gradient shard
-    int64_t wide;                   // all six state arrays 32-byte aligned: 256-bit state accesses (apply pass)
 };
 
 struct AdamScalars {                // fp32, each rounded once from fp64 on the host
@@ -139,17 +138,18 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) { return __ldcs(reinte
 __device__ __forceinline__ float4 ld_stream4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st_stream4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
-// A thread's 8 consecutive fp32 state values in the apply pass.  When the
-// shard's state arrays are 32-byte aligned they move in one 256-bit access
-// each (sm_100 and later): a warp's request then covers 1 KB of one array
-// with every 32-byte sector whole, where two 128-bit accesses each ask for
-// half of every sector of the same 1 KB.  Measured on the clipped Llama-3-8B
-// shard (2.0B elements): the apply pass 8.567 against 8.627 ms and 8.609
-// against 8.638 ms (two GB300s, the sources alternated in one call).  The
-// fused pass keeps 128-bit accesses: 256-bit ones gained 0.1% on the 8-slice
-// pass and lost 0.25% on the 4-slice partial pass.
-__device__ __forceinline__ void ld_state8(const float* p, bool wide, float4& lo, float4& hi) {
-    if (wide) {
+// A thread's 8 consecutive fp32 state values.  WIDE: one 256-bit access
+// (sm_100 and later; the address 32-byte aligned), so that a warp's request
+// covers 1 KB of one array with every 32-byte sector whole, where two 128-bit
+// accesses each ask for half of every sector of the same 1 KB.  The host
+// picks the instantiation for a whole launch (state_wide, fused_state_wide):
+// a per-vector choice inside one kernel cost more than the wider accesses
+// saved.  ld_state8: streaming loads (the apply pass, whose state may be
+// updated in place); ld_state8_ro: the read-only path (the fused pass's *_in
+// state, which no thread writes).
+template <bool WIDE>
+__device__ __forceinline__ void ld_state8(const float* p, float4& lo, float4& hi) {
+    if (WIDE) {
         asm volatile("ld.global.cs.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                      : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
                      : "l"(p));
@@ -159,8 +159,21 @@ __device__ __forceinline__ void ld_state8(const float* p, bool wide, float4& lo,
     }
 }
 
-__device__ __forceinline__ void st_state8(float* p, bool wide, const float (&v)[8]) {
-    if (wide) {
+template <bool WIDE>
+__device__ __forceinline__ void ld_state8_ro(const float* p, float4& lo, float4& hi) {
+    if (WIDE) {
+        asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
+                     : "l"(p));
+    } else {
+        lo = ld_ro4(p);
+        hi = ld_ro4(p + 4);
+    }
+}
+
+template <bool WIDE>
+__device__ __forceinline__ void st_state8(float* p, const float (&v)[8]) {
+    if (WIDE) {
         asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                      :
                      : "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
@@ -530,7 +543,7 @@ __device__ __forceinline__ void apply_elem(const StepArgs& a, const ShardDev& d,
 // NS_FEW, and 0.341 ms with NS = 4 at 3 blocks per SM.
 // CHAIN: a chained step (t, S and the state set from a.chain); the other
 // instantiations take everything from their arguments.
-template <int GDT, int PDT, int VEC, int NS, bool CHAIN = false>
+template <int GDT, int PDT, int VEC, int NS, bool CHAIN = false, bool WIDE = false>
 __global__ void __launch_bounds__(TILE_THREADS, NS == 0 ? (CHAIN ? 3 : 4) : 2)   // chained: 3, so no spills
 k_step_fused(const __grid_constant__ StepArgs a) {
     constexpr int64_t TILE = (int64_t)TILE_THREADS * VEC;
@@ -552,9 +565,10 @@ k_step_fused(const __grid_constant__ StepArgs a) {
         if (j >= d.numel) continue;
         if (VEC == 8 && j + 8 <= d.numel) {
             const StatePtrs p = state_ptrs(d, c.sw);
-            const float4 t0 = ld_ro4(p.mi + j), t1 = ld_ro4(p.mi + j + 4);
-            const float4 m0 = ld_ro4(p.mmi + j), m1 = ld_ro4(p.mmi + j + 4);
-            const float4 v0 = ld_ro4(p.vi + j), v1 = ld_ro4(p.vi + j + 4);
+            float4 t0, t1, m0, m1, v0, v1;
+            ld_state8_ro<WIDE>(p.mi + j, t0, t1);
+            ld_state8_ro<WIDE>(p.mmi + j, m0, m1);
+            ld_state8_ro<WIDE>(p.vi + j, v0, v1);
             float s[8];
             reduce8<GDT, NS>(a, d.grad_off + j, s);
             float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
@@ -576,12 +590,9 @@ k_step_fused(const __grid_constant__ StepArgs a) {
                 hp[e + 1] = w >> 16;
             }
             sumsq.add8(af);
-            st_stream4(p.mo + j, make_float4(th[0], th[1], th[2], th[3]));
-            st_stream4(p.mo + j + 4, make_float4(th[4], th[5], th[6], th[7]));
-            st_stream4(p.mmo + j, make_float4(mm[0], mm[1], mm[2], mm[3]));
-            st_stream4(p.mmo + j + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
-            st_stream4(p.vo + j, make_float4(vv[0], vv[1], vv[2], vv[3]));
-            st_stream4(p.vo + j + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+            st_state8<WIDE>(p.mo + j, th);
+            st_state8<WIDE>(p.mmo + j, mm);
+            st_state8<WIDE>(p.vo + j, vv);
             store8(P, d.param_off + j, hp);
         } else {
             const int64_t end = (VEC == 8) ? d.numel : j + 1;
@@ -715,16 +726,16 @@ __device__ __forceinline__ ApplyLoc apply_locate(const StepArgs& a, int64_t tile
     return L;
 }
 
+template <bool WIDE>
 __device__ __forceinline__ void apply_load(const ApplyLoc& L, bool sw, ApplyVec& x) {
     const StatePtrs p = state_ptrs(*L.d, sw);
-    const bool wide = L.d->wide != 0;
-    ld_state8(p.mi + L.j, wide, x.t0, x.t1);
-    ld_state8(p.mmi + L.j, wide, x.m0, x.m1);
-    ld_state8(p.vi + L.j, wide, x.v0, x.v1);
+    ld_state8<WIDE>(p.mi + L.j, x.t0, x.t1);
+    ld_state8<WIDE>(p.mmi + L.j, x.m0, x.m1);
+    ld_state8<WIDE>(p.vi + L.j, x.v0, x.v1);
     x.w = ld_stream(static_cast<const uint16_t*>(L.d->gshard) + L.j);
 }
 
-template <int GDT, int PDT>
+template <int GDT, int PDT, bool WIDE>
 __device__ __forceinline__ void apply_finish(const StepArgs& a, const ApplyLoc& L, const ApplyVec& x, float k,
                                              const Ctl& c, uint16_t* P) {
     const StatePtrs p = state_ptrs(*L.d, c.sw);
@@ -745,17 +756,17 @@ __device__ __forceinline__ void apply_finish(const StepArgs& a, const ApplyLoc& 
         hp[e] = w & 0xFFFFu;
         hp[e + 1] = w >> 16;
     }
-    const bool wide = L.d->wide != 0;
-    st_state8(p.mo + j, wide, th);
-    st_state8(p.mmo + j, wide, mm);
-    st_state8(p.vo + j, wide, vv);
+    st_state8<WIDE>(p.mo + j, th);
+    st_state8<WIDE>(p.mmo + j, mm);
+    st_state8<WIDE>(p.vo + j, vv);
     store8(P, L.d->param_off + j, hp);
 }
 
 // Every block derives the same skip / clip decision from the statistics.
 // (Issuing the next tile's loads before updating and storing the current
 // one measured 2.5% slower on one shard and no faster on eight.)
-template <int GDT, int PDT, int VEC>
+// WIDE: 256-bit state accesses (every shard's state arrays 32-byte aligned).
+template <int GDT, int PDT, int VEC, bool WIDE = false>
 __global__ void __launch_bounds__(TILE_THREADS)
 k_apply(const __grid_constant__ StepArgs a) {
     const zero_stats st = *a.stats;
@@ -793,8 +804,8 @@ k_apply(const __grid_constant__ StepArgs a) {
         const ApplyLoc L = apply_locate<GDT, PDT>(a, tile, k, c, si);
         if (!L.full) continue;
         ApplyVec x;
-        apply_load(L, c.sw, x);
-        apply_finish<GDT, PDT>(a, L, x, k, c, P);
+        apply_load<WIDE>(L, c.sw, x);
+        apply_finish<GDT, PDT, WIDE>(a, L, x, k, c, P);
     }
 }
 

@@ -24,13 +24,15 @@ const void* reduce_kernel(int gdt, int vec, int ns) {
 }
 
 template <int G, int P>
-static const void* apply_ptr(int vec) {
-    return vec == 8 ? (const void*)k_apply<G, P, 8> : (const void*)k_apply<G, P, 1>;
+static const void* apply_ptr(int vec, bool wide) {
+    if (vec != 8) return (const void*)k_apply<G, P, 1>;
+    return wide ? (const void*)k_apply<G, P, 8, true> : (const void*)k_apply<G, P, 8>;
 }
 
-const void* apply_kernel(int gdt, int pdt, int vec) {
-    if (gdt == ZERO_BF16) return pdt == ZERO_BF16 ? apply_ptr<ZERO_BF16, ZERO_BF16>(vec) : apply_ptr<ZERO_BF16, ZERO_F16>(vec);
-    return pdt == ZERO_BF16 ? apply_ptr<ZERO_F16, ZERO_BF16>(vec) : apply_ptr<ZERO_F16, ZERO_F16>(vec);
+const void* apply_kernel(int gdt, int pdt, int vec, bool wide) {
+    if (gdt == ZERO_BF16)
+        return pdt == ZERO_BF16 ? apply_ptr<ZERO_BF16, ZERO_BF16>(vec, wide) : apply_ptr<ZERO_BF16, ZERO_F16>(vec, wide);
+    return pdt == ZERO_BF16 ? apply_ptr<ZERO_F16, ZERO_BF16>(vec, wide) : apply_ptr<ZERO_F16, ZERO_F16>(vec, wide);
 }
 
 int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s, bool early) {
@@ -42,7 +44,7 @@ int launch_reduce(const StepArgs& a, int gdt, int vec, cudaStream_t s, bool earl
 }
 
 int launch_apply(const StepArgs& a, int gdt, int pdt, int vec, cudaStream_t s) {
-    const void* f = apply_kernel(gdt, pdt, vec);
+    const void* f = apply_kernel(gdt, pdt, vec, vec == 8 && state_wide(a));
     const int grid = grid_for(f, a.n_tiles, BPS_APPLY);
     void* args[] = {const_cast<StepArgs*>(&a)};
     return cuda_fail(cudaLaunchKernel(f, dim3(grid), dim3(TILE_THREADS), args, 0, s), "apply launch");
