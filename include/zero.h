@@ -285,7 +285,14 @@ size_t zero_workspace_bytes(void);
  * round16(master)).  Otherwise two passes: reduce into grad_shard (required
  * then), then apply.  Both run 16-byte vectors where every slice address
  * (+ grad_offset), state pointer and grad_shard is 16-byte aligned, and
- * element by element otherwise.
+ * element by element otherwise; the state moves in 32-byte accesses where
+ * every shard's six state pointers are 32-byte aligned (and, for the apply
+ * pass, every grad_shard's vector loop starts on a 128-byte line).  The
+ * choice changes no result.
+ * Aliasing: apart from *_out == *_in (the in-place update), no output of a
+ * call (a state array, a grad_shard, a shard's parameter range) may overlap
+ * any input or any other output of the same call; the fused pass reads the
+ * *_in state and the slices through the read-only cache while it writes.
  * Errors (all before any work is enqueued): ZERO_EINVAL, ZERO_EALIGN (16-bit
  * pointers must be 2-byte aligned, fp32 pointers 4-byte aligned),
  * ZERO_EWORKSPACE, ZERO_ELIMIT; ZERO_ECUDA if a launch fails. */
