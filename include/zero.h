@@ -609,8 +609,8 @@ int zero_shard_step_commit(const zero_shard* shards, int n_shards, void* flat_pa
  * they are serialised on the host, and a ring must not be shared by calls
  * that are not ordered on the device.  Those streams and their events are
  * made by the first call on a device and kept until the process exits; they
- * do not survive cudaDeviceReset (later calls on that device then fail with
- * ZERO_ECUDA).
+ * do not survive cudaDeviceReset, so after a reset of a device this call must
+ * not be made on it again in the same process.
  * Errors: ZERO_EINVAL (also for a host buffer that is not page-locked),
  * ZERO_EALIGN, ZERO_EWORKSPACE (also for a ring of fewer than 64 elements per
  * chunk), ZERO_ELIMIT, before any work is enqueued; ZERO_ECUDA. */
