@@ -54,6 +54,13 @@
  *  - ZERO_ENOMEM_WS                              -> ZERO_EWORKSPACE
  *  - an out-parameter "overflow flag + norm"     -> zero_result (overflow,
  *    applied, sumsq, grad_norm, clip_coef, grad_mult)
+ *  - grad_slices / n_slices inside each shard    -> one grad_slices array per
+ *    call (every shard of a step reads the same N_d slices) and a
+ *    grad_offset per shard
+ *  - zero3_reduce_bucket's separate device sumsq and overflow accumulators
+ *                                                -> one zero_stats, an
+ *    `accumulate` flag (0 starts it afresh) and the workspace for the
+ *    per-block partial sums
  */
 #ifndef ZERO_GB300_H
 #define ZERO_GB300_H
